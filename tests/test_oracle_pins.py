@@ -1,0 +1,254 @@
+"""Pins of the fp64 oracle against what the pages and plain mathematics fix.
+
+None of these re-types the oracle's step loop: each compares it with a
+different statement of the same quantity (a closed form, a hand-worked
+example, a special case that reduces to the textbook delta rule, an explicit
+product of transition matrices, or an invariant).  Sources: page
+"Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.1 (KDA update, delta rule),
+§3.2 (step order), §3.3 (lower-bounded gate, 16-token tile bound), and page
+"Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽" ("KDA 到底在算什么",
+"最被低估的一个细节：下界衰减").
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_inputs(rng, n, d_k, d_v, unit=True):
+    q = rng.normal(size=(n, d_k))
+    k = rng.normal(size=(n, d_k))
+    if unit:
+        q /= np.linalg.norm(q, axis=1, keepdims=True)
+        k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.normal(size=(n, d_v))
+    g = 2.0 * rng.normal(size=(n, d_k))
+    beta = (1.0 / (1.0 + np.exp(-rng.normal(size=n)))).astype(np.float32)
+    return q, k, v, g, beta
+
+
+@pytest.mark.parametrize("name", ["delta_rule_worked_example.json", "erase_full_decay_example.json"])
+def test_hand_worked_examples(name):
+    """Hand-derived values (derivation stored with each fixture)."""
+    fx = json.load(open(os.path.join(GOLDEN, name)))
+    q = np.array(fx["q"], dtype=np.float64)
+    k = np.array(fx["k"], dtype=np.float64)
+    v = np.array(fx["v"], dtype=np.float64)
+    if fx["g"] == "-inf":
+        g = np.full(q.shape, -np.inf)
+    else:
+        g = np.array(fx["g"], dtype=np.float64)
+    beta = np.array(fx["beta"], dtype=np.float32)
+    s0 = np.array(fx["S0"], dtype=np.float64) if "S0" in fx else None
+    o, S = oracle.recurrence(q, k, v, g, beta, s0)
+    np.testing.assert_allclose(o, np.array(fx["o"]), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(S, np.array(fx["S_final"]), rtol=0, atol=1e-13)
+
+
+def test_gate_special_values():
+    """Gate map of §3.3: logit 0 -> alpha = e^{-5/2}; +inf -> e^{-5} (the
+    lower bound); -inf -> 1.  Probed through beta = 0 (pure decay), where
+    S_1 = Diag(alpha) S_0 and o_1 = S_1^T q."""
+    d = 3
+    s0 = np.arange(1.0, 1.0 + d * d).reshape(d, d)
+    g = np.array([[0.0, np.inf, -np.inf]])
+    q = np.eye(d)[[0]]  # o_1 = S_1^T e_0 = row 0 of S_1
+    o, S = oracle.recurrence(q, np.zeros((1, d)), np.zeros((1, d)), g, np.zeros(1, np.float32), s0)
+    expect = s0 * np.array([math.exp(-2.5), math.exp(-5.0), 1.0])[:, None]
+    np.testing.assert_allclose(S, expect, rtol=1e-15, atol=0)
+    np.testing.assert_allclose(o[0], expect[0], rtol=1e-15, atol=0)
+
+
+def test_pure_decay_closed_form():
+    """beta = 0: S_t = Diag(exp(sum_{tau<=t} log alpha_tau)) S_0 and
+    o_t = S_t^T q_t, with log alpha = -5 * Sigmoid(logit)."""
+    rng = np.random.default_rng(11)
+    n, d_k, d_v = 40, 5, 7
+    q, k, v, g, _ = _rand_inputs(rng, n, d_k, d_v)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = oracle.recurrence(q, k, v, g, np.zeros(n, np.float32), s0)
+    logdecay = -5.0 / (1.0 + np.exp(-g))              # [n, d_k]
+    cum = np.cumsum(logdecay, axis=0)
+    for t in range(n):
+        St = np.exp(cum[t])[:, None] * s0
+        np.testing.assert_allclose(o[t], St.T @ q[t], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S, np.exp(cum[-1])[:, None] * s0, rtol=1e-12, atol=1e-300)
+
+
+def test_no_decay_is_textbook_delta_rule():
+    """alpha == 1 (logit -1e4 => Sigmoid underflows to 0 in fp64) reduces KDA to
+    the ungated delta rule of §3.1, written here in its projector form
+    S_t = (I - beta k k^T) S_{t-1} + beta k v^T."""
+    rng = np.random.default_rng(12)
+    n, d_k, d_v = 30, 6, 4
+    q, k, v, _, beta = _rand_inputs(rng, n, d_k, d_v)
+    g = np.full((n, d_k), -1.0e4)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = oracle.recurrence(q, k, v, g, beta, s0)
+    St = s0.copy()
+    for t in range(n):
+        b = float(beta[t])
+        St = (np.eye(d_k) - b * np.outer(k[t], k[t])) @ St + b * np.outer(k[t], v[t])
+        np.testing.assert_allclose(o[t], St.T @ q[t], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(S, St, rtol=1e-11, atol=1e-12)
+
+
+def test_full_write_recalls_value():
+    """beta = 1 and unit-norm k: the erase removes the whole old prediction along
+    k, so S_t^T k_t = v_t.  Read through o_t with q_t = k_t."""
+    rng = np.random.default_rng(13)
+    n, d_k, d_v = 50, 8, 5
+    _, k, v, g, _ = _rand_inputs(rng, n, d_k, d_v)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, _ = oracle.recurrence(k, k, v, g, np.ones(n, np.float32), s0)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-12 * np.abs(v).max())
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_brute_force_transition_product(seed):
+    """Tiny inputs, d_k != d_v so a transposed operand cannot pass: build
+    M_t = (I - beta_t k_t k_t^T) Diag(alpha_t) explicitly and compare
+    S_t = M_t...M_1 S_0 + sum_{tau<=t} M_t...M_{tau+1} beta_tau k_tau v_tau^T
+    and o_t = S_t^T q_t with the oracle at every t."""
+    rng = np.random.default_rng(100 + seed)
+    n, d_k, d_v = 8, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(d_k, d_v))
+    alpha = np.exp(-5.0 / (1.0 + np.exp(-g)))
+    Ms = [(np.eye(d_k) - float(beta[t]) * np.outer(k[t], k[t])) @ np.diag(alpha[t]) for t in range(n)]
+
+    def prod(a, b):  # M_b ... M_a (a <= b), identity if empty
+        P = np.eye(d_k)
+        for t in range(a, b + 1):
+            P = Ms[t] @ P
+        return P
+
+    for m in range(1, n + 1):
+        o, S = oracle.recurrence(q[:m], k[:m], v[:m], g[:m], beta[:m], s0)
+        St = prod(0, m - 1) @ s0
+        for tau in range(m):
+            St = St + prod(tau + 1, m - 1) @ (float(beta[tau]) * np.outer(k[tau], v[tau]))
+        np.testing.assert_allclose(S, St, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(o[m - 1], St.T @ q[m - 1], rtol=1e-12, atol=1e-13)
+
+
+def test_gate_lower_bound_tile_edge():
+    """All logits +30: alpha sits on the e^{-5} bound, and 16 steps reach a
+    cumulative log-decay of -80, the edge of the 16-token tile bound (§3.3).
+    The oracle stays finite and matches the closed form there."""
+    n, d = 16, 4
+    s0 = np.full((d, d), 1.0e30)
+    g = np.full((n, d), 30.0)
+    o, S = oracle.recurrence(np.ones((n, d)), np.zeros((n, d)), np.zeros((n, d)), g, np.zeros(n, np.float32), s0)
+    sig30 = 1.0 / (1.0 + math.exp(-30.0))
+    expect = math.exp(-5.0 * sig30 * n) * 1.0e30
+    assert np.isfinite(S).all() and np.isfinite(o).all()
+    np.testing.assert_allclose(S, expect, rtol=1e-12)
+    assert abs(-5.0 * sig30 * n + 80.0) < 1e-11
+
+
+def test_storage_dtypes_read_exactly():
+    """bf16 inputs (bit patterns) and fp32 inputs give the same result as the
+    same values passed in fp64 (the oracle widens exactly)."""
+    rng = np.random.default_rng(14)
+    n, d_k, d_v = 20, 4, 3
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v)
+    s0 = rng.normal(size=(d_k, d_v))
+    q32, k32, v32, g32 = (x.astype(np.float32) for x in (q, k, v, g))
+    o32, S32 = oracle.recurrence(q32, k32, v32, g32, beta, s0, dtype=oracle.F32)
+    o64, S64 = oracle.recurrence(*(x.astype(np.float64) for x in (q32, k32, v32, g32)), beta, s0)
+    np.testing.assert_array_equal(o32, o64)
+    np.testing.assert_array_equal(S32, S64)
+    # bf16: truncate fp32 bit patterns (exactly representable values)
+    def tobits(x):
+        return (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+    def widen(b):
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    qb, kb, vb, gb = (tobits(x) for x in (q, k, v, g))
+    ob, Sb = oracle.recurrence(qb, kb, vb, gb, beta, s0, dtype=oracle.BF16)
+    ow, Sw = oracle.recurrence(*(widen(x) for x in (qb, kb, vb, gb)), beta, s0)
+    np.testing.assert_array_equal(ob, ow)
+    np.testing.assert_array_equal(Sb, Sw)
+
+
+def test_chains_match_single_runs_and_split():
+    """Batch entry point: strided chains equal separate calls, and running a
+    sequence in two pieces with the state handed over equals one run."""
+    rng = np.random.default_rng(15)
+    T, H, d_k, d_v = 24, 3, 4, 5
+    q, k, v, g, beta = _rand_inputs(rng, T * H, d_k, d_v)
+    s0 = rng.normal(size=(H, d_k, d_v))
+    outs, S, _ = oracle.chains(q, k, v, g, beta, oracle.F64, d_k, d_v, H, list(range(H)), [T] * H, s0)
+    for h in range(H):
+        sl = slice(h, None, H)
+        o1, S1 = oracle.recurrence(q[sl], k[sl], v[sl], g[sl], beta[sl], s0[h])
+        np.testing.assert_array_equal(outs[h], o1)
+        np.testing.assert_array_equal(S[h], S1)
+        oa, Sa = oracle.recurrence(q[sl][:10], k[sl][:10], v[sl][:10], g[sl][:10], beta[sl][:10], s0[h])
+        ob, Sb = oracle.recurrence(q[sl][10:], k[sl][10:], v[sl][10:], g[sl][10:], beta[sl][10:], Sa)
+        np.testing.assert_allclose(np.concatenate([oa, ob]), o1, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(Sb, S1, rtol=1e-13, atol=1e-14)
+
+
+MUTANTS = {
+    "decay scales columns": ("S[(int64_t)i * d_v + c] *= alpha[i];", "S[(int64_t)i * d_v + c] *= alpha[c % d_k];"),
+    "beta dropped": ("err[c] = b * (", "err[c] = ("),
+    "write sign": ("S[(int64_t)i * d_v + c] += kk[i] * err[c];", "S[(int64_t)i * d_v + c] -= kk[i] * err[c];"),
+    "transposed read": ("vhat += S[(int64_t)i * d_v + c] * kk[i];",
+                        "vhat += S[(int64_t)(c % d_k) * d_v + (i % d_v)] * kk[i];"),
+    "gate complement": ("return exp(-5.0 * sig);", "return exp(-5.0 * (1.0 - sig));"),
+    "read-out with k": ("acc += S[(int64_t)i * d_v + c] * qq[i];", "acc += S[(int64_t)i * d_v + c] * kk[i];"),
+    "no erase": ("vhat += S[(int64_t)i * d_v + c] * kk[i];", "vhat += 0.0 * S[(int64_t)i * d_v + c] * kk[i];"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistakes_fail_a_pin(mutant, tmp_path):
+    """Plant one plausible mistake in a compiled copy of the oracle's C source
+    and check that the brute-force transition-product pin rejects it."""
+    import ctypes
+    import subprocess
+
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[mutant]
+    assert src.count(old) == 1, mutant
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fopenmp", "-fPIC", "-shared", str(mpath), "-o", str(so), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.kda_oracle_chains.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.kda_oracle_chains.restype = ctypes.c_int
+
+    rng = np.random.default_rng(16)
+    n, d_k, d_v = 8, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(d_k, d_v))
+    o = np.zeros((n, d_v))
+    S = np.zeros((d_k, d_v))
+    r0 = np.zeros(1, np.int64)
+    nn = np.array([n], np.int64)
+    off = np.zeros(1, np.int64)
+    arrs = [np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, g)]
+    lib.kda_oracle_chains(*(a.ctypes.data for a in arrs), oracle.F64, beta.ctypes.data, 1, d_k, d_v, 1,
+                          r0.ctypes.data, nn.ctypes.data, s0.ctypes.data, o.ctypes.data, off.ctypes.data,
+                          S.ctypes.data)
+    alpha = np.exp(-5.0 / (1.0 + np.exp(-g)))
+    St = s0.copy()
+    o_ref = np.zeros((n, d_v))
+    for t in range(n):
+        M = (np.eye(d_k) - float(beta[t]) * np.outer(k[t], k[t])) @ np.diag(alpha[t])
+        St = M @ St + float(beta[t]) * np.outer(k[t], v[t])
+        o_ref[t] = St.T @ q[t]
+    err = max(np.abs(o - o_ref).max(), np.abs(S - St).max())
+    assert err > 1e-6, f"mutant '{mutant}' was not caught (err {err:g})"
