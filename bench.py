@@ -1,0 +1,493 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA recurrence library on GB300.
+
+Headline: chunked-prefill tokens/s on B=1, H=32, T=65536, d_k=d_v=128 (bf16
+q/k/v/g, fp32 beta and state, initial state N(0, 0.01)), inputs resident in
+HBM (2.1 GB of inputs per step, larger than the 129 MB L2, so no flush is
+needed between steps).  One step = one kda_chunk_fwd call over the whole
+workload.  Also reported on the same JSON line:
+
+* ``roofline``: the dominant kernel's algorithmic bytes per launch over its
+  mean launch time (CUDA events recorded by the library around each launch on
+  its stream during the timed region), against the measured HBM copy peak;
+* ``path_roofline``: the same for the whole step;
+* ``e2e``: the same metric through the Python API with pinned host buffers
+  (inputs copied in and o + final state copied out inside every timed step);
+* ``decode``: 100 decode steps of 256 sequences x 96 heads (fp32 state
+  128x128 per head), GB/s against the same peak;
+* ``cpu_baseline``: the fp64 CPU oracle on a bounded sample of the workload;
+* ``clocks``: nvidia-smi samples taken during the timed region.
+
+``--impl reference`` times the CPU oracle instead (the only reference this
+method has), on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = "prefill_b1_h32_t65536_d128"
+METRIC = "KDA prefill tokens/s (H=32,d=128,T=64K); decode GB/s; % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kda", "reference"], default="kda")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=100)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def _selector(self):
+        import torch
+
+        try:
+            u = torch.cuda.get_device_properties(self.dev).uuid
+            return ["-i", "GPU-" + str(u)]
+        except Exception:
+            return []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "50",
+               *self._selector()]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if re.match(r"^[0-9.]+$", r[1])]
+        smax = [float(r[2]) for r in rows if re.match(r"^[0-9.]+$", r[2])]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------ library profiling hook
+def _prof(lib, on: bool):
+    lib.kda_profile_enable.argtypes = [ctypes.c_int32]
+    lib.kda_profile_enable(1 if on else 0)
+
+
+def _collect(lib, max_records=4096):
+    lib.kda_profile_collect.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+    lib.kda_profile_collect.restype = ctypes.c_int32
+    names = ctypes.create_string_buffer(64 * max_records)
+    ms = (ctypes.c_float * max_records)()
+    seen = lib.kda_profile_collect(names, ms, max_records)
+    recs = []
+    for i in range(min(seen, max_records)):
+        nm = names.raw[64 * i: 64 * i + 64].split(b"\0", 1)[0].decode()
+        recs.append((nm, float(ms[i])))
+    return seen, recs
+
+
+def _kernel_src_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "linear_attention_recurrence_chunk_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profiles(kernel: str, units_per_launch: float):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summaries, if
+    they were taken on the current kernel sources (else None)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = _kernel_src_sha()
+    pat = re.compile(r"^traffic:\s+kernel=(\S+)\s+dram_bytes_per_unit=([0-9.eE+-]+)\s+src_sha=(\S+)")
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        for line in open(os.path.join(pdir, fn)):
+            m = pat.match(line.strip())
+            if m and m.group(1) == kernel and m.group(3) == sha:
+                return float(m.group(2)) * units_per_launch
+    return None
+
+
+# ---------------------------------------------------------------- workloads
+def prefill_alg_bytes(w, kernel: str) -> float:
+    """Algorithmic bytes the kernel must move per launch: the path's inputs
+    (q, k, g, v, beta) belong to the kernel that reads them, its outputs (o,
+    final state) and the initial state to the kernel that writes / reads them."""
+    eb = 2 if w.dtype == "bf16" else 4
+    ht = w.tokens * w.H
+    inputs = ht * ((3 * w.d_k + w.d_v) * eb + 4)
+    outputs = ht * w.d_v * eb
+    states = w.num_seqs * w.H * w.d_k * w.d_v * 4 * (2 if w.s0_std is not None else 1)
+    if "prep" in kernel:
+        return float(inputs)
+    if "chain" in kernel:
+        return float(outputs + states)
+    if "fused" in kernel or kernel == "path":
+        return float(inputs + outputs + states)
+    return 0.0
+
+
+def dist_setup(args):
+    import torch
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and args.impl == "kda":
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def bench_prefill(args, ws_size, local):
+    import torch
+
+    import kda_synth as ks
+    import linear_attention_recurrence_chunk_gb300 as kda
+    from kda_synth.torchio import prefill_inputs
+
+    w = ks.workloads()[WORKLOAD]
+    t = prefill_inputs(w, "cuda")
+    lib = kda.load_library()
+    stream = torch.cuda.current_stream()
+    o = torch.empty_like(t["v"])
+    sf = torch.empty((w.num_seqs, w.H, w.d_k, w.d_v), dtype=torch.float32, device="cuda")
+    ws_bytes = kda.kda_chunk_fwd_workspace_size(w.B, w.T, w.H, w.d_k, w.d_v, w.num_seqs, torch.bfloat16)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def step():
+        kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["s0"], o=o, final_state=sf,
+                          workspace=wsp, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, code = kda.kda_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {code} during warm-up")
+
+    sampler = ClockSampler(local)
+    barrier(ws_size)
+    torch.cuda.synchronize()
+    sampler.start()
+    _prof(lib, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _prof(lib, False)
+    barrier(ws_size)
+    clocks = sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    seen, recs = _collect(lib)
+    max_ms = max_over_ranks(elapsed_ms, ws_size)
+
+    per_kernel = {}
+    for nm, ms in recs:
+        per_kernel.setdefault(nm, []).append(ms)
+    return {"w": w, "t": t, "elapsed_ms": elapsed_ms, "max_ms": max_ms, "launches": seen,
+            "per_kernel": per_kernel, "clocks": clocks, "o": o, "sf": sf, "wsp": wsp}
+
+
+def bench_e2e(args, w, wsp, steps):
+    """Same metric through the Python API from pinned host buffers."""
+    import torch
+
+    import linear_attention_recurrence_chunk_gb300 as kda
+    from kda_synth.torchio import prefill_inputs
+
+    host = {k: v for k, v in prefill_inputs(w, "cpu", pin=True).items() if k != "cu" and v is not None}
+    dev = {k: torch.empty(v.shape, dtype=v.dtype, device="cuda") for k, v in host.items()}
+    o_host = torch.empty(dev["v"].shape, dtype=dev["v"].dtype).pin_memory()
+    sf_host = torch.empty((w.num_seqs, w.H, w.d_k, w.d_v), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size() + sf_host.numel() * 4
+
+    def step():
+        for k_ in host:
+            dev[k_].copy_(host[k_], non_blocking=True)
+        o, sf = kda.kda_chunk_fwd(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], initial_state=dev["s0"],
+                                  workspace=wsp, stream=stream)
+        o_host.copy_(o, non_blocking=True)
+        sf_host.copy_(sf, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        step()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = e0.elapsed_time(e1)
+    return {"value": w.tokens * steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": ms / steps,
+            "wall_s": round(wall, 3)}
+
+
+def bench_decode(args, peak_gbs):
+    import torch
+
+    import kda_synth as ks
+    import linear_attention_recurrence_chunk_gb300 as kda
+
+    d = ks.workloads()["decode_n256_h96_d128_x100"]
+    steps = min(args.decode_steps, d.steps)
+    heads = d.N * d.H
+    lib = kda.load_library()
+    state = torch.from_numpy(d.fill_state()).reshape(d.N, d.H, d.d_k, d.d_v).cuda()
+    toks = []
+    for s in range(steps):
+        x = {}
+        for name, width in (("q", d.d_k), ("k", d.d_k), ("v", d.d_v), ("g", d.d_k)):
+            a = d.fill_step(s, name)
+            x[name] = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).reshape(d.N, d.H, width).cuda()
+        x["beta"] = torch.from_numpy(d.fill_step(s, "beta")).reshape(d.N, d.H).cuda()
+        toks.append(x)
+    o = torch.empty((d.N, d.H, d.d_v), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    # warm-up on a scratch copy of the state (the timed steps start from the seeded state)
+    scratch = state.clone()
+    for s in range(3):
+        x = toks[s]
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], scratch, o=o, stream=stream)
+    del scratch
+    torch.cuda.synchronize()
+    _prof(lib, True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        x = toks[s]
+        kda.kda_decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], state, o=o, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _prof(lib, False)
+    seen, recs = _collect(lib)
+    ms = e0.elapsed_time(e1)
+    per_step_bytes = heads * (2 * d.d_k * d.d_v * 4 + (3 * d.d_k + d.d_v) * 2 + 4 + d.d_v * 2)
+    kms = [m for n, m in recs if n == "decode_step"]
+    kmean = statistics.mean(kms) if kms else ms / steps
+    gbs = per_step_bytes / (kmean / 1e3) / 1e9
+    return {"workload": d.name, "steps": steps, "ms_per_step": ms / steps, "kernel_ms": kmean,
+            "bytes_per_step": per_step_bytes, "GB/s": gbs, "frac": gbs / peak_gbs, "gpu_launches": seen}
+
+
+def oracle_sample(w, ntok):
+    """The fp64 oracle, as it stands, on every head of sequence 0 over its
+    first ``ntok`` tokens.  Returns (outputs, threads used)."""
+    import oracle
+
+    ins = [w.chain_inputs(0, h, ntok) for h in range(w.H)]
+    n = [len(x["beta"]) for x in ins]
+    cat = {k: np.concatenate([x[k] for x in ins]) for k in ("q", "k", "v", "g", "beta")}
+    s0 = None if w.s0_std is None else np.stack([x["s0"] for x in ins]).astype(np.float64)
+    row0 = np.concatenate([[0], np.cumsum(n)[:-1]])
+    dt = oracle.BF16 if w.dtype == "bf16" else oracle.F32
+    outs, _, threads = oracle.chains(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"], dt, w.d_k, w.d_v, 1,
+                                     row0, n, s0)
+    return outs, threads
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The fp64 oracle as it stands, on all heads over the first n tokens
+    (n picked from a short probe so that the run takes about ``target_s``)."""
+    import oracle
+
+    probe_tok = 512
+    t0 = time.perf_counter()
+    _, threads = oracle_sample(w, probe_tok)
+    probe = time.perf_counter() - t0
+    n = int(min(w.T, max(1024, probe_tok * target_s / max(probe, 1e-3))))
+    n = max(1024, (n // 1024) * 1024)
+    t0 = time.perf_counter()
+    _, threads = oracle_sample(w, n)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {w.H} heads x first {n} tokens of {w.name} (fp64 C oracle, OpenMP over heads)",
+            "seconds": round(dt, 3), "max_threads": oracle.max_threads()}
+
+
+def run_reference(args):
+    """CPU oracle arm: each step runs the oracle on a bounded sample of the
+    workload (all heads, n tokens), n sized so that warm-up + steps take about
+    a minute."""
+    import kda_synth as ks
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = ks.workloads()[WORKLOAD]
+    t0 = time.perf_counter()
+    _, threads = oracle_sample(w, 256)
+    probe = time.perf_counter() - t0
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    n = int(max(16, min(w.T, 256 * budget / max(probe, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_sample(w, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(w, n)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "d_k": w.d_k, "d_v": w.d_v},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"per step: all {w.H} heads x first {n} tokens of {w.name}"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    ws_size, rank, local = dist_setup(args)
+    peak, peak_kind = peaks()
+    r = bench_prefill(args, ws_size, local)
+    w = r["w"]
+    steps = args.steps
+    value = ws_size * w.tokens * steps / (r["max_ms"] / 1e3)
+
+    # dominant kernel = largest total time in the timed region
+    totals = {k: sum(v) for k, v in r["per_kernel"].items()}
+    dom = max(totals, key=totals.get) if totals else None
+    roof = None
+    if dom:
+        mean_ms = statistics.mean(r["per_kernel"][dom])
+        alg = prefill_alg_bytes(w, dom)
+        ach = alg / (mean_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_source": peak_kind, "alg_bytes_per_launch": alg, "mean_launch_ms": mean_ms,
+                "traffic": _traffic_from_profiles(dom, w.tokens * w.H),
+                "share": totals[dom] / max(sum(totals.values()), 1e-9)}
+    path_alg = prefill_alg_bytes(w, "path")
+    path_ach = path_alg / (r["max_ms"] / steps / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_size, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": r["max_ms"] / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "d_k": w.d_k, "d_v": w.d_v,
+                   "state": "fp32, S0 ~ N(0, 0.01)", "chunk": 64,
+                   "l2": "no flush: 2.1 GB of inputs per step, larger than L2"},
+        "roofline": roof,
+        "path_roofline": {"bound": "hbm", "achieved": path_ach, "peak": peak, "unit": "GB/s",
+                          "frac": path_ach / peak, "alg_bytes_per_step": path_alg},
+        "kernels": {k: {"launches": len(v), "mean_ms": statistics.mean(v), "share": totals[k] / sum(totals.values())}
+                    for k, v in r["per_kernel"].items()},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if not args.no_e2e:
+        line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
+        if ws_size > 1:
+            line["e2e"]["value"] = max_over_ranks(-line["e2e"]["value"], ws_size) * -1 * ws_size
+    del r
+    torch.cuda.empty_cache()
+    if not args.no_decode:
+        line["decode"] = bench_decode(args, peak)
+    if rank == 0 and ws_size == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws_size > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) recurrence library for one
+ * GB300 GPU (sm_103a).
+ *
+ * The operation (per sequence and head; S is d_k x d_v, rows = key channels):
+ *
+ *     log alpha_t = -5 * Sigmoid(g_t)                      (per key channel)
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t                                       (after the update)
+ *
+ * Sources: page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读", §3.1 (the KDA
+ * equation; Diag(alpha) scales the rows of S), §3.2 (decay, read, write the
+ * beta-weighted error, read out from the updated state; the single-token
+ * interface (x_t, S_{t-1}) -> (y_t, S_t)), §3.3 (chunked prefill
+ * (X_[c], S_in) -> (Y_[c], S_out) with S_in[c+1] = S_out[c]; the lower-bounded
+ * decay with g_min = -5); page "Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽",
+ * sections "KDA 到底在算什么" and "最被低估的一个细节：下界衰减".
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned, dense and contiguous in the layouts given below.  The library
+ *    allocates no memory; kda_chunk_fwd takes its scratch space from the caller.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
+ *    errors are detected on the host and returned before anything is launched.
+ *    A launch failure returns KDA_ERR_CUDA.  Conditions only the device can see
+ *    (a malformed cu_seqlens array, a bounded device-side wait that ran out)
+ *    set a per-device error word instead; read and clear it with
+ *    kda_device_error() after the work has finished.
+ *  - q and k are used as given (any L2 normalisation happens upstream); g is
+ *    the raw decay logit (any per-head scale is already folded into it); beta is
+ *    the write strength, already in (0, 1), as fp32.  No 1/sqrt(d_k) factor is
+ *    applied to q.  o has the input dtype; states are always fp32.
+ *  - Supported head sizes: d_k, d_v in {64, 128}; other values return
+ *    KDA_ERR_UNSUPPORTED.
+ */
+#ifndef KDA_GB300_KDA_H
+#define KDA_GB300_KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment, alias or workspace */
+  KDA_ERR_UNSUPPORTED = 2,    /* valid request outside what the kernels cover (head size) */
+  KDA_ERR_CUDA = 3,           /* a CUDA runtime call or a launch failed */
+  KDA_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (see kda_device_error) */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+KDA_API const char* kda_status_string(kda_status s);
+
+/*
+ * Bytes of device scratch memory kda_chunk_fwd needs for this problem size
+ * (same arguments as kda_chunk_fwd; with cu_seqlens, pass B = 1, T = total
+ * packed tokens and num_seqs = number of sequences).  Returns SIZE_MAX when the
+ * arguments are invalid or unsupported.
+ */
+KDA_API size_t kda_chunk_fwd_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v,
+                                    int32_t num_seqs, kda_dtype dt);
+
+/*
+ * Chunked prefill: runs the recurrence over whole sequences, chunk by chunk
+ * (page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.3: intra-chunk work as
+ * matrix products, the state passed only across chunk boundaries).
+ *
+ *  q, k, g   [B, T, H, d_k]   dtype dt (token-major, heads interleaved)
+ *  v, o      [B, T, H, d_v]   dtype dt
+ *  beta      [B, T, H]        fp32
+ *  initial_state [S, H, d_k, d_v] fp32 (d_v contiguous) or NULL for zeros
+ *  final_state   [S, H, d_k, d_v] fp32, or NULL when not wanted; it may be the
+ *                same pointer as initial_state (updated in place)
+ *  Without cu_seqlens: S = B = num_seqs sequences of T tokens each.
+ *  With cu_seqlens (device int32[num_seqs + 1]): B must be 1, the T tokens are
+ *    num_seqs packed sequences, sequence s covering tokens
+ *    [cu_seqlens[s], cu_seqlens[s+1]); the array must start at 0, never
+ *    decrease and end at T.  A malformed array is detected on the device: no
+ *    output is written and kda_device_error() then reports
+ *    KDA_ERR_INVALID_ARG.  Empty sequences are allowed.
+ *  o must not overlap any input.  T = 0 (or an empty sequence) writes the
+ *  initial state (or zeros) to final_state.
+ *  workspace: device memory of at least kda_chunk_fwd_workspace_size(...)
+ *  bytes, 256-byte aligned, owned by the caller; its contents on entry do not
+ *  matter and on return are unspecified.  Two calls in flight at once need two
+ *  workspaces.
+ */
+KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs,
+                         int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                         void* o, float* final_state, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * One decode step for N independent sequences (one new token each), the
+ * single-token interface of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读"
+ * §3.2 restricted to the recurrence: (q, k, v, g, beta, S_{t-1}) -> (o_t, S_t).
+ *
+ *  q, k, g [N, H, d_k] dtype dt;  v, o [N, H, d_v] dtype dt;  beta [N, H] fp32
+ *  state   [N, H, d_k, d_v] fp32, read and overwritten in place with S_t.
+ *  o must not overlap any input or the state.  N = 0 is a no-op.
+ */
+KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                           float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                           void* o, cudaStream_t stream);
+
+/*
+ * Reads and clears this device's error word (on the current device), after
+ * waiting for `stream`.  *code receives the raw word (0 = none).  Returns
+ * KDA_OK when it was 0, KDA_ERR_INVALID_ARG for a malformed cu_seqlens,
+ * KDA_ERR_DEVICE_TIMEOUT for a device-side wait that ran out, KDA_ERR_CUDA if
+ * the read itself failed.
+ */
+KDA_API kda_status kda_device_error(cudaStream_t stream, int32_t* code);
+
+/*
+ * Measurement hook (the pages have no counterpart: it exists so that a
+ * benchmark can time each kernel of a call on the stream it runs on).
+ * kda_profile_enable(1) makes every later launch of this library record a
+ * CUDA event pair around itself on its stream (at most 4096 pairs are kept;
+ * later launches are counted but not timed); kda_profile_enable(0) stops it.
+ * kda_profile_collect() waits for the recorded events, writes up to
+ * max_records kernel names (NUL-terminated, 64 bytes each) and durations in
+ * milliseconds, returns the number of launches seen since the last collect
+ * (timed or not) and clears the record.  Host-side bookkeeping only; not
+ * thread safe; the events are created once and reused.
+ */
+KDA_API kda_status kda_profile_enable(int32_t on);
+KDA_API int32_t kda_profile_collect(char* names, float* ms, int32_t max_records);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_KDA_H */

@@ -1,0 +1,152 @@
+"""KDA (Kimi Delta Attention) recurrence on one GB300 GPU.
+
+Thin ctypes binding of the C ABI in ``include/kda.h`` (``libkda_gb300.so``,
+built in-tree by ``_build.build()``).  This module only marshals arguments:
+torch supplies device memory and the current CUDA stream; every step of the
+recurrence runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing or fails to load, the functions raise.
+
+Functions keep the C names:
+
+* ``kda_chunk_fwd(q, k, v, g, beta, initial_state=None, cu_seqlens=None, ...)``
+  -> ``(o, final_state)``: chunked prefill (page "Kimi K3：架构、训练与百万 Token
+  Agentic RL 技术解读" §3.3), q/k/g ``[B, T, H, d_k]``, v ``[B, T, H, d_v]``,
+  beta ``[B, T, H]`` fp32, states ``[S, H, d_k, d_v]`` fp32.
+* ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
+  sequence (same page §3.2), state updated in place.
+* ``kda_chunk_fwd_workspace_size(...)``, ``kda_device_error()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+__all__ = ["kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
+           "KdaError", "library_path", "load_library", "STATUS"]
+
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+          4: "KDA_ERR_DEVICE_TIMEOUT"}
+_DT = {torch.float32: 0, torch.bfloat16: 1}
+SIZE_MAX = (1 << 64) - 1
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+_lib = None
+
+
+def load_library():
+    """Load ``libkda_gb300.so`` (building it first if it is missing or stale and
+    nvcc is available).  Raises if it cannot be loaded."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _build.up_to_date():
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_chunk_fwd_workspace_size.argtypes = [i64, i64, i32, i32, i32, i32, ctypes.c_int]
+    lib.kda_chunk_fwd_workspace_size.restype = sz
+    lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int, vp, vp,
+                                  vp, sz, vp]
+    lib.kda_chunk_fwd.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp, vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_device_error.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.kda_device_error.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise KdaError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    return _DT[t.dtype]
+
+
+def kda_chunk_fwd_workspace_size(B: int, T: int, H: int, d_k: int, d_v: int, num_seqs: int,
+                                 dtype: torch.dtype) -> int:
+    n = load_library().kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, _DT[dtype])
+    if n == SIZE_MAX:
+        raise KdaError(1, "kda_chunk_fwd_workspace_size")
+    return int(n)
+
+
+def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  initial_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                  output_final_state: bool = True, o: Optional[torch.Tensor] = None,
+                  final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill.  Returns ``(o, final_state)`` (``final_state`` is None
+    when ``output_final_state`` is False).  ``final_state`` may be passed as the
+    same tensor as ``initial_state`` to update it in place."""
+    lib = load_library()
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    num_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((num_seqs, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    ws_bytes = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens),
+                           num_seqs, B, T, H, d_k, d_v, _dtype_code(q), _ptr(o), _ptr(final_state),
+                           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "kda_chunk_fwd")
+    return o, final_state
+
+
+def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                    state: torch.Tensor, o: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step: q/k/g ``[N, H, d_k]``, v ``[N, H, d_v]``, beta ``[N, H]``
+    fp32, state ``[N, H, d_k, d_v]`` fp32 (updated in place).  Returns o."""
+    lib = load_library()
+    N, H, d_k = q.shape
+    d_v = v.shape[-1]
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), N, H, d_k, d_v,
+                             _dtype_code(q), _ptr(o), _stream(stream))
+    _check(st, "kda_decode_step")
+    return o
+
+
+def kda_device_error(stream=None) -> Tuple[int, int]:
+    """(status, raw device error word) after waiting for ``stream``; clears the word."""
+    code = ctypes.c_int32(0)
+    st = load_library().kda_device_error(_stream(stream), ctypes.byref(code))
+    return int(st), int(code.value)

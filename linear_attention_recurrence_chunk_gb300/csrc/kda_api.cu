@@ -1,0 +1,215 @@
+// C ABI of the KDA recurrence library: argument validation, workspace sizing,
+// the per-device error word and dispatch to the kernel launchers.
+#include <limits.h>
+#include <stdint.h>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+// Per-device error word (one instance per device that loads the module).
+__device__ int32_t g_kda_device_error = 0;
+
+cudaError_t device_error_word(int32_t** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_kda_device_error);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool head_dims_supported(int32_t d_k, int32_t d_v) {
+  return (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128);
+}
+
+size_t dtype_bytes(kda_dtype dt) { return dt == KDA_F32 ? 4 : 2; }
+
+// [a, a+na) and [b, b+nb) overlap (byte ranges; empty ranges never overlap)
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Shared shape checks of kda_chunk_fwd and its workspace query.
+kda_status check_chunk_shape(int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v, int32_t num_seqs,
+                             kda_dtype dt, bool varlen) {
+  if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || H <= 0 || num_seqs < 0) return KDA_ERR_INVALID_ARG;
+  if (varlen ? (B != 1 || num_seqs < 1) : (num_seqs != B)) return KDA_ERR_INVALID_ARG;
+  if (B * T > (int64_t)INT32_MAX - 1) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)num_seqs * H > (int64_t)INT32_MAX / 2 || H > 65535) return KDA_ERR_INVALID_ARG;
+  if (!head_dims_supported(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+// Measurement hook state (host side).
+constexpr int kProfMax = 4096;
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t ev[2];
+};
+bool g_prof_on = false;
+int g_prof_n = 0;          // timed records in use
+int g_prof_launches = 0;   // launches seen since the last collect
+ProfRecord g_prof[kProfMax] = {};
+
+}  // namespace
+
+namespace kda {
+
+void prof_begin(cudaStream_t s, const char* name) {
+  if (!g_prof_on) return;
+  ++g_prof_launches;
+  if (g_prof_n >= kProfMax) return;
+  ProfRecord& r = g_prof[g_prof_n];
+  if (!r.ev[0]) {
+    if (cudaEventCreate(&r.ev[0]) != cudaSuccess || cudaEventCreate(&r.ev[1]) != cudaSuccess) return;
+  }
+  r.name = name;
+  cudaEventRecord(r.ev[0], s);
+}
+
+void prof_end(cudaStream_t s) {
+  if (!g_prof_on || g_prof_n >= kProfMax || !g_prof[g_prof_n].name) return;
+  cudaEventRecord(g_prof[g_prof_n].ev[1], s);
+  ++g_prof_n;
+}
+
+}  // namespace kda
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v, int32_t num_seqs,
+                                    kda_dtype dt) {
+  // The varlen form (B = 1, num_seqs sequences) and the batched form
+  // (num_seqs = B) need the same space for the same total token count.
+  const bool varlen = !(num_seqs == B);
+  if (check_chunk_shape(B, T, H, d_k, d_v, num_seqs, dt, varlen) != KDA_OK) return SIZE_MAX;
+  return kda::chunk_workspace_layout(B * T, num_seqs, H, d_k, d_v, dt).bytes;
+}
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
+                         int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o, float* final_state,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const bool varlen = cu_seqlens != nullptr;
+  kda_status st = check_chunk_shape(B, T, H, d_k, d_v, num_seqs, dt, varlen);
+  if (st != KDA_OK) return st;
+  const int64_t tokens = B * T;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
+  if (!workspace) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_INVALID_ARG;
+  const kda::Workspace ws = kda::chunk_workspace_layout(tokens, num_seqs, H, d_k, d_v, dt);
+  if (workspace_bytes < ws.bytes) return KDA_ERR_INVALID_ARG;
+
+  // o must not overlap any input; the workspace must not overlap anything.
+  const size_t eb = dtype_bytes(dt);
+  const size_t nqk = (size_t)tokens * H * d_k * eb, nv = (size_t)tokens * H * d_v * eb;
+  const size_t nb = (size_t)tokens * H * sizeof(float);
+  const size_t ns = (size_t)num_seqs * H * d_k * d_v * sizeof(float);
+  const size_t ncu = varlen ? sizeof(int32_t) * ((size_t)num_seqs + 1) : 0;
+  struct Range { const void* p; size_t n; };
+  const Range inputs[] = {{q, nqk}, {k, nqk}, {g, nqk}, {v, nv}, {beta, nb}, {initial_state, ns},
+                          {cu_seqlens, ncu}};
+  for (const Range& r : inputs) {
+    if (overlaps(o, nv, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+    if (overlaps(final_state, ns, r.p, r.n) && r.p != initial_state) return KDA_ERR_INVALID_ARG;
+    if (overlaps(workspace, ws.bytes, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, nv, final_state, ns) || overlaps(workspace, ws.bytes, o, nv) ||
+      overlaps(workspace, ws.bytes, final_state, ns))
+    return KDA_ERR_INVALID_ARG;
+  if (final_state && initial_state && final_state != initial_state && overlaps(final_state, ns, initial_state, ns))
+    return KDA_ERR_INVALID_ARG;
+
+  if (num_seqs == 0) return KDA_OK;
+
+  int32_t* dev_err = nullptr;
+  if (device_error_word(&dev_err) != cudaSuccess) return KDA_ERR_CUDA;
+
+  kda::ChunkProblem p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = initial_state;
+  p.cu = cu_seqlens; p.num_seqs = num_seqs; p.T_seq = varlen ? 0 : T; p.total_tokens = tokens;
+  p.H = H; p.d_k = d_k; p.d_v = d_v; p.dt = dt; p.o = o; p.s_final = final_state; p.dev_err = dev_err;
+  return kda::launch_chunk_fwd(p, ws, workspace, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                           float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                           cudaStream_t stream) {
+  if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)N * H > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (!head_dims_supported(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  const void* ptrs[] = {q, k, v, g, beta, state, o};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  const size_t eb = dtype_bytes(dt), heads = (size_t)N * H;
+  const size_t nqk = heads * d_k * eb, nv = heads * d_v * eb, ns = heads * d_k * d_v * sizeof(float);
+  struct Range { const void* p; size_t n; };
+  const Range others[] = {{q, nqk}, {k, nqk}, {g, nqk}, {v, nv}, {beta, heads * sizeof(float)}};
+  for (const Range& r : others) {
+    if (overlaps(o, nv, r.p, r.n) || overlaps(state, ns, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, nv, state, ns)) return KDA_ERR_INVALID_ARG;
+  return kda::launch_decode_step(q, k, v, g, beta, state, N, H, d_k, d_v, dt, o, stream) == cudaSuccess
+             ? KDA_OK
+             : KDA_ERR_CUDA;
+}
+
+kda_status kda_profile_enable(int32_t on) {
+  g_prof_on = on != 0;
+  return KDA_OK;
+}
+
+int32_t kda_profile_collect(char* names, float* ms, int32_t max_records) {
+  const int32_t seen = g_prof_launches;
+  for (int i = 0; i < g_prof_n; ++i) {
+    ProfRecord& r = g_prof[i];
+    if (i < max_records) {
+      float t = -1.f;
+      if (cudaEventSynchronize(r.ev[1]) != cudaSuccess || cudaEventElapsedTime(&t, r.ev[0], r.ev[1]) != cudaSuccess)
+        t = -1.f;
+      if (ms) ms[i] = t;
+      if (names) {
+        int j = 0;
+        for (; j < 63 && r.name[j]; ++j) names[64 * i + j] = r.name[j];
+        names[64 * i + j] = 0;
+      }
+    }
+    r.name = nullptr;
+  }
+  g_prof_n = 0;
+  g_prof_launches = 0;
+  return seen;
+}
+
+kda_status kda_device_error(cudaStream_t stream, int32_t* code) {
+  if (!code) return KDA_ERR_INVALID_ARG;
+  int32_t* dev_err = nullptr;
+  if (device_error_word(&dev_err) != cudaSuccess) return KDA_ERR_CUDA;
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, dev_err, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaMemsetAsync(dev_err, 0, sizeof h, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+  *code = h;
+  if (h == 0) return KDA_OK;
+  if (h == kda::kDevErrBadSeqlens) return KDA_ERR_INVALID_ARG;
+  return KDA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+// Fused single-token decode step of the KDA recurrence.
+//
+// Page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.2 gives the step as
+// decay -> read -> write error -> read out:
+//   S_bar = Diag(alpha) S,  v_hat = S_bar^T k,  S = S_bar + beta k (v - v_hat)^T,  o = S^T q.
+// Since S^T q = S_bar^T q + (k.q) beta (v - v_hat), the read-out needs only the
+// column sums S_bar^T k and S_bar^T q of the decayed state, so each state is
+// read from HBM once and written once:
+//   delta = beta (v - S_bar^T k),  o = S_bar^T q + (k.q) delta,  S = S_bar + k delta^T.
+//
+// One CTA per (sequence, head).  256 threads: a warp row of d_v/4 threads
+// covers one state row with float4 accesses (512 B per row for d_v = 128), and
+// the d_k rows are spread over the remaining thread dimension; every thread
+// holds its d_k*d_v/1024 float4s in registers between the read and the write.
+// The state streams through with evict-first hints (it is touched once per step).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const T* __restrict__ q,
+                                                                     const T* __restrict__ k,
+                                                                     const T* __restrict__ v,
+                                                                     const T* __restrict__ g,
+                                                                     const float* __restrict__ beta,
+                                                                     float* __restrict__ state,
+                                                                     T* __restrict__ o) {
+  constexpr int TX = DV / 4;                 // float4 columns of a state row
+  constexpr int TY = kDecodeThreads / TX;    // rows processed side by side
+  constexpr int RPT = DK / TY;               // rows per thread
+  static_assert(RPT * TY == DK, "row split");
+
+  __shared__ float s_k[DK], s_q[DK], s_alpha[DK];
+  __shared__ __align__(16) float s_red[2][TY][DV];
+  __shared__ __align__(16) float s_delta[DV];
+  __shared__ float s_kq;
+
+  const int64_t head = blockIdx.x;          // n * H + h
+  const int tid = threadIdx.x;
+  const int tx = tid % TX;
+  const int ty = tid / TX;
+
+  // Issue the state loads first: they do not depend on the token vectors.
+  float4* st = reinterpret_cast<float4*>(state + head * DK * DV);
+  float4 S[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) S[i] = __ldcs(st + (ty + i * TY) * TX + tx);
+
+  for (int i = tid; i < DK; i += kDecodeThreads) {
+    s_k[i] = to_f32(k[head * DK + i]);
+    s_q[i] = to_f32(q[head * DK + i]);
+    s_alpha[i] = expf(log_decay(to_f32(g[head * DK + i])));
+  }
+  __syncthreads();
+
+  if (tid < 32) {  // k . q
+    float acc = 0.f;
+    for (int i = tid; i < DK; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (tid == 0) s_kq = acc;
+  }
+
+  float4 vh = make_float4(0.f, 0.f, 0.f, 0.f), aq = vh;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int row = ty + i * TY;
+    const float al = s_alpha[row], kr = s_k[row], qr = s_q[row];
+    S[i].x *= al; S[i].y *= al; S[i].z *= al; S[i].w *= al;
+    vh.x += S[i].x * kr; vh.y += S[i].y * kr; vh.z += S[i].z * kr; vh.w += S[i].w * kr;
+    aq.x += S[i].x * qr; aq.y += S[i].y * qr; aq.z += S[i].z * qr; aq.w += S[i].w * qr;
+  }
+  reinterpret_cast<float4*>(&s_red[0][ty][0])[tx] = vh;
+  reinterpret_cast<float4*>(&s_red[1][ty][0])[tx] = aq;
+  __syncthreads();
+
+  if (tid < DV) {
+    float vhat = 0.f, a = 0.f;
+#pragma unroll
+    for (int y = 0; y < TY; ++y) {
+      vhat += s_red[0][y][tid];
+      a += s_red[1][y][tid];
+    }
+    const float d = beta[head] * (to_f32(v[head * DV + tid]) - vhat);
+    s_delta[tid] = d;
+    o[head * DV + tid] = from_f32<T>(a + s_kq * d);
+  }
+  __syncthreads();
+
+  const float4 d4 = reinterpret_cast<const float4*>(s_delta)[tx];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float kr = s_k[ty + i * TY];
+    S[i].x += kr * d4.x; S[i].y += kr * d4.y; S[i].z += kr * d4.z; S[i].w += kr * d4.w;
+    __stcs(st + (ty + i * TY) * TX + tx, S[i]);
+  }
+}
+
+template <typename T>
+cudaError_t launch_typed(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                         float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, void* o,
+                         cudaStream_t stream) {
+  const dim3 grid((unsigned)((int64_t)N * H));
+  const T* qq = static_cast<const T*>(q);
+  const T* kk = static_cast<const T*>(k);
+  const T* vv = static_cast<const T*>(v);
+  const T* gg = static_cast<const T*>(g);
+  T* oo = static_cast<T*>(o);
+  prof_begin(stream, "decode_step");
+  if (d_k == 128 && d_v == 128)
+    decode_step_kernel<128, 128, T><<<grid, kDecodeThreads, 0, stream>>>(qq, kk, vv, gg, beta, state, oo);
+  else if (d_k == 128 && d_v == 64)
+    decode_step_kernel<128, 64, T><<<grid, kDecodeThreads, 0, stream>>>(qq, kk, vv, gg, beta, state, oo);
+  else if (d_k == 64 && d_v == 128)
+    decode_step_kernel<64, 128, T><<<grid, kDecodeThreads, 0, stream>>>(qq, kk, vv, gg, beta, state, oo);
+  else
+    decode_step_kernel<64, 64, T><<<grid, kDecodeThreads, 0, stream>>>(qq, kk, vv, gg, beta, state, oo);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                               float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                               void* o, cudaStream_t stream) {
+  if (dt == KDA_F32) return launch_typed<float>(q, k, v, g, beta, state, N, H, d_k, d_v, o, stream);
+  return launch_typed<__nv_bfloat16>(q, k, v, g, beta, state, N, H, d_k, d_v, o, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,75 @@
+"""Shared helpers of the GPU parity tests: move seeded inputs to the device,
+run the oracle on sampled chains, and apply the tolerances.
+
+Tolerances (the target's accuracy contract):
+  fp32 inputs : max |o - o_ref| <= 1e-4 * rms(o_ref)
+  bf16 inputs : max |o - o_ref| <= 2e-2 * rms(o_ref)
+  final state : ||S - S_ref||_F / ||S_ref||_F <= 1e-2
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import kda_synth as ks
+import oracle
+from kda_synth.torchio import prefill_inputs
+
+O_TOL = {"f32": 1e-4, "bf16": 2e-2}
+S_TOL = 1e-2
+ORACLE_DT = {"f32": oracle.F32, "bf16": oracle.BF16}
+
+
+def prefill_device_inputs(w: ks.PrefillWorkload, device="cuda"):
+    """Device tensors q, k, v, g [B, T, H, d], beta [B, T, H], s0 or None,
+    cu_seqlens or None (varlen workloads are B = 1, T = total)."""
+    return prefill_inputs(w, device)
+
+
+def oracle_chains(w: ks.PrefillWorkload, pairs, ntok=None):
+    """Oracle (o [n, d_v], S [d_k, d_v]) for each (seq, head) in ``pairs``
+    (first ``ntok`` tokens of each sequence if given), OpenMP across chains."""
+    ins = [w.chain_inputs(s, h, ntok) for s, h in pairs]
+    n = [len(x["beta"]) for x in ins]
+    cat = {k: np.concatenate([x[k] for x in ins]) for k in ("q", "k", "v", "g", "beta")}
+    s0 = None
+    if w.s0_std is not None:
+        s0 = np.stack([x["s0"] for x in ins]).astype(np.float64)
+    row0 = np.concatenate([[0], np.cumsum(n)[:-1]])
+    outs, states, _ = oracle.chains(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"], ORACLE_DT[w.dtype],
+                                    w.d_k, w.d_v, 1, row0, n, s0)
+    return outs, states
+
+
+def gpu_chain_outputs(w: ks.PrefillWorkload, o: torch.Tensor, pairs, ntok=None):
+    """The GPU's o rows of each (seq, head) chain, as fp64 numpy."""
+    flat = o.reshape(w.tokens, w.H, w.d_v)
+    res = []
+    for s, h in pairs:
+        tok0, L = w.seq_bounds(s)
+        n = L if ntok is None else min(ntok, L)
+        res.append(flat[tok0: tok0 + n, h].float().cpu().numpy().astype(np.float64))
+    return res
+
+
+def assert_o_close(o_gpu_list, o_ref_list, dtype: str, what: str = "o"):
+    ref = np.concatenate([x.reshape(-1) for x in o_ref_list])
+    got = np.concatenate([x.reshape(-1) for x in o_gpu_list])
+    assert np.isfinite(got).all(), f"{what}: non-finite GPU output"
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.abs(got - ref).max())
+    tol = O_TOL[dtype] * rms
+    assert err <= tol, f"{what}: max|dO| {err:.3e} > {O_TOL[dtype]} * rms {rms:.3e}"
+    return err / max(rms, 1e-300)
+
+
+def assert_state_close(s_gpu, s_ref, what: str = "state"):
+    s_gpu = np.asarray(s_gpu, dtype=np.float64)
+    s_ref = np.asarray(s_ref, dtype=np.float64)
+    assert np.isfinite(s_gpu).all(), f"{what}: non-finite GPU state"
+    nr = np.linalg.norm(s_ref)
+    rel = np.linalg.norm(s_gpu - s_ref) / nr if nr > 0 else np.linalg.norm(s_gpu)
+    assert rel <= S_TOL, f"{what}: relative Frobenius error {rel:.3e} > {S_TOL}"
+    return rel
