@@ -17,8 +17,9 @@
  * sections "KDA 到底在算什么" and "最被低估的一个细节：下界衰减".
  *
  * Conventions shared by every entry point
- *  - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
- *    aligned, dense and contiguous in the layouts given below.  The library
+ *  - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *    contiguous in the layouts given below, 16-byte aligned (beta and
+ *    cu_seqlens: 4-byte aligned).  The library
  *    allocates no memory; kda_chunk_fwd takes its scratch space from the caller.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
  *    errors are detected on the host and returned before anything is launched.

@@ -15,6 +15,7 @@ cudaError_t device_error_word(int32_t** ptr) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool head_dims_supported(int32_t d_k, int32_t d_v) {
   return (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128);
@@ -108,9 +109,10 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
   const int64_t tokens = B * T;
   if (tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
   if (!workspace) return KDA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, o, final_state};
+  const void* ptrs[] = {q, k, v, g, initial_state, o, final_state};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if ((beta && !aligned4(beta)) || (cu_seqlens && !aligned4(cu_seqlens))) return KDA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_INVALID_ARG;
   const kda::Workspace ws = kda::chunk_workspace_layout(tokens, num_seqs, H, d_k, d_v, dt);
   if (workspace_bytes < ws.bytes) return KDA_ERR_INVALID_ARG;
@@ -155,9 +157,10 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
   if ((int64_t)N * H > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (!head_dims_supported(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
   if (N == 0) return KDA_OK;
-  const void* ptrs[] = {q, k, v, g, beta, state, o};
+  const void* ptrs[] = {q, k, v, g, state, o};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (!beta || !aligned4(beta)) return KDA_ERR_INVALID_ARG;
   const size_t eb = dtype_bytes(dt), heads = (size_t)N * H;
   const size_t nqk = heads * d_k * eb, nv = heads * d_v * eb, ns = heads * d_k * d_v * sizeof(float);
   struct Range { const void* p; size_t n; };

@@ -3,8 +3,14 @@ run the oracle on sampled chains, and apply the tolerances.
 
 Tolerances (the target's accuracy contract):
   fp32 inputs : max |o - o_ref| <= 1e-4 * rms(o_ref)
-  bf16 inputs : max |o - o_ref| <= 2e-2 * rms(o_ref)
+  bf16 inputs : max (|o - o_ref| - ulp_bf16(o)/2) <= 2e-2 * rms(o_ref)
   final state : ||S - S_ref||_F / ||S_ref||_F <= 1e-2
+bf16 outputs are stored in bf16, and rounding a value to bf16 moves it by up
+to half a bf16 ulp of that value.  On these inputs max|o| is 10-20x rms(o), so
+that storage rounding alone reaches 2-4% of rms(o): the exactly rounded fp64
+result itself would fail a bare 2e-2*rms bound (test_bf16_rounding_reading
+shows it).  The bound is therefore applied to the computation, with each
+stored value's own half-ulp rounding allowed on top.
 """
 from __future__ import annotations
 
@@ -52,6 +58,21 @@ def gpu_chain_outputs(w: ks.PrefillWorkload, o: torch.Tensor, pairs, ntok=None):
     return res
 
 
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp of each (bf16-representable) value: the most that
+    rounding a real number to that bf16 value can have moved it."""
+    _, e = np.frexp(np.abs(np.asarray(x, dtype=np.float64)))
+    return np.where(x == 0, 0.0, np.ldexp(1.0, e - 9))
+
+
+def o_excess(got: np.ndarray, ref: np.ndarray, dtype: str) -> np.ndarray:
+    """|got - ref| minus the storage-rounding allowance of the output dtype."""
+    err = np.abs(got - ref)
+    if dtype == "bf16":
+        err = err - half_ulp_bf16(got)
+    return err
+
+
 def assert_o_close(o_gpu_list, o_ref_list, dtype: str, what: str = "o"):
     ref = np.concatenate([x.reshape(-1) for x in o_ref_list])
     got = np.concatenate([x.reshape(-1) for x in o_gpu_list])
@@ -59,9 +80,9 @@ def assert_o_close(o_gpu_list, o_ref_list, dtype: str, what: str = "o"):
     if ref.size == 0:
         return 0.0
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    err = float(np.abs(got - ref).max())
+    err = float(o_excess(got, ref, dtype).max())
     tol = O_TOL[dtype] * rms
-    assert err <= tol, f"{what}: max|dO| {err:.3e} > {O_TOL[dtype]} * rms {rms:.3e}"
+    assert err <= tol, f"{what}: max(|dO| - rounding) {err:.3e} > {O_TOL[dtype]} * rms {rms:.3e}"
     return err / max(rms, 1e-300)
 
 

@@ -75,6 +75,7 @@ def test_chunk_fwd_rejects_bad_arguments_on_host():
     assert _chunk(lib, dv=32) == 2
     assert _chunk(lib, dt=5) == 1
     assert _chunk(lib, q=FAKE + 8) == 1                         # 16-byte alignment
+    assert _chunk(lib, beta=FAKE + (4 << 30) + 2) == 1          # beta: 4-byte alignment
     assert _chunk(lib, ws=FAKE + (6 << 30) + 16) == 1          # 256-byte workspace alignment
     assert _chunk(lib, wsb=1024) == 1                           # workspace too small
     assert _chunk(lib, o=FAKE + 4096) == 1                      # o overlaps q

@@ -252,3 +252,28 @@ def test_planted_mistakes_fail_a_pin(mutant, tmp_path):
         o_ref[t] = St.T @ q[t]
     err = max(np.abs(o - o_ref).max(), np.abs(S - St).max())
     assert err > 1e-6, f"mutant '{mutant}' was not caught (err {err:g})"
+
+
+def test_bf16_rounding_reading():
+    """Reading of the bf16 output tolerance: rounding the exact (fp64 oracle)
+    outputs of a bf16 workload to bf16 already moves them by more than
+    2e-2 * rms(o) (max|o| is 10-20x rms here), so the bound can only apply to
+    the computation with each stored value's half-ulp rounding allowed on top;
+    with that allowance the exactly rounded result passes (excess at the fp32
+    rounding level only)."""
+    import kda_synth as ks
+    from kda_testutil import half_ulp_bf16, o_excess
+
+    w = ks.PrefillWorkload("x", "bf16", 1, 300, 3, 128, 128, seed=5, s0_std=0.05)
+    worst_bare = 0.0
+    for h in range(w.H):
+        ci = w.chain_inputs(0, h)
+        o, _ = oracle.recurrence(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], ci["s0"].astype(np.float64),
+                                 dtype=oracle.BF16)
+        ob = ks.bf16_bits_to_f64(ks.f32_to_bf16_bits(o.astype(np.float32)))
+        rms = np.sqrt(np.mean(o ** 2))
+        worst_bare = max(worst_bare, np.abs(ob - o).max() / rms)
+        # (fp64 -> fp32 -> bf16 double rounding adds at most an fp32 ulp)
+        assert o_excess(ob, o, "bf16").max() <= 1e-6 * rms
+        assert (np.abs(ob - o) <= half_ulp_bf16(ob) * (1 + 2.0 ** -13)).all()
+    assert worst_bare > 2e-2

@@ -9,7 +9,7 @@ import torch
 import kda_synth as ks
 import oracle
 import linear_attention_recurrence_chunk_gb300 as kda
-from kda_testutil import (assert_o_close, assert_state_close, gpu_chain_outputs, oracle_chains,
+from kda_testutil import (assert_o_close, assert_state_close, gpu_chain_outputs, o_excess, oracle_chains,
                           prefill_device_inputs)
 
 pytestmark = pytest.mark.gpu
@@ -134,10 +134,10 @@ def test_split_prefill_hands_state_over():
     o2, _ = kda.kda_chunk_fwd(rest["q"], rest["k"], rest["v"], rest["g"], rest["beta"],
                               initial_state=rest["s0"], final_state=rest["s0"])
     torch.cuda.synchronize()
-    ref = o_full.float()
-    rms = ref.pow(2).mean().sqrt().item()
-    got = torch.cat([o1, o2], dim=1).float()
-    assert (got - ref).abs().max().item() <= 2e-2 * rms
+    ref = o_full.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
+    got = torch.cat([o1, o2], dim=1).float().cpu().numpy()
+    assert o_excess(got, ref, "bf16").max() <= 2e-2 * rms
     rel = ((rest["s0"] - s_full).norm() / s_full.norm()).item()
     assert rel <= 1e-2
 
@@ -155,9 +155,9 @@ def test_varlen_equals_separate_calls():
                                      initial_state=t["s0"][s:s + 1].contiguous())
         torch.cuda.synchronize()
         if L:
-            ref = o[:, a:b].float()
-            rms = ref.pow(2).mean().sqrt().item()
-            assert (o_s.float() - ref).abs().max().item() <= 2e-2 * rms
+            ref = o[:, a:b].float().cpu().numpy()
+            rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
+            assert o_excess(o_s.float().cpu().numpy(), ref, "bf16").max() <= 2e-2 * rms
         assert ((s_s[0] - sf[s]).norm() / sf[s].norm()).item() <= 1e-2
 
 
@@ -276,7 +276,8 @@ def test_decode_steps_equal_prefill():
                                         t["v"][:, i].contiguous(), t["g"][:, i].contiguous(),
                                         t["beta"][:, i].contiguous(), state))
     torch.cuda.synchronize()
-    o_d = torch.stack(outs, dim=1).float()
-    rms = o_p.float().pow(2).mean().sqrt().item()
-    assert (o_d - o_p.float()).abs().max().item() <= 2e-2 * rms
+    o_d = torch.stack(outs, dim=1).float().cpu().numpy()
+    o_pn = o_p.float().cpu().numpy()
+    rms = float(np.sqrt(np.mean(o_pn.astype(np.float64) ** 2)))
+    assert o_excess(o_d, o_pn, "bf16").max() <= 2e-2 * rms
     assert ((state - s_p).norm() / s_p.norm()).item() <= 1e-2
