@@ -127,6 +127,35 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
 KDA_API kda_status kda_device_error(cudaStream_t stream, int32_t* code);
 
 /*
+ * Allocation-free variant of kda_chunk_fwd (the pages have no counterpart).
+ *
+ * For callers that cannot call cudaMalloc, for example a serving engine that
+ * reserves almost all device memory for its caches at start-up, or a plug-in
+ * whose host owns the device allocator.  Arguments, layouts, results and
+ * error behaviour are those of kda_chunk_fwd, except that there is no
+ * workspace argument: the scratch space is a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory on
+ * every GPU that loads it, until the process exits.  The caller still
+ * provides every input and output.
+ *  - A problem whose kda_chunk_fwd_workspace_size(...) exceeds
+ *    KDA_NOALLOC_SCRATCH_BYTES is rejected with KDA_ERR_INVALID_ARG before
+ *    anything is launched.
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress (on the current device) and caches it; make that
+ *    first call before any stream capture.
+ *  - Nothing is allocated or freed by the call.
+ *  - All calls share the one array: calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on it and must not overlap.
+ *    Its contents on entry do not matter.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+KDA_API kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                         const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                                         int32_t num_seqs, int64_t B, int64_t T, int32_t H, int32_t d_k,
+                                         int32_t d_v, kda_dtype dt, void* o, float* final_state,
+                                         cudaStream_t stream);
+
+/*
  * Measurement hook (the pages have no counterpart: it exists so that a
  * benchmark can time each kernel of a call on the stream it runs on).
  * kda_profile_enable(1) makes every later launch of this library record a
