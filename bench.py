@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 WORKLOAD = "prefill_b1_h32_t65536_d128"
+PROFILE_WORKLOAD = "prefill_b1_h32_t8192_d128"   # same shape and recipe, 8192 tokens (268 MB of inputs)
 METRIC = "KDA prefill tokens/s (H=32,d=128,T=64K); decode GB/s; % of GB300 roofline"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -55,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=100)
+    ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD], default=WORKLOAD,
+                    help="the headline workload, or a T=8192 cut of it for profiler captures")
     return ap.parse_args()
 
 
@@ -188,6 +191,16 @@ def prefill_alg_bytes(w, kernel: str) -> float:
     return 0.0
 
 
+def get_workload(name):
+    import kda_synth as ks
+
+    if name == PROFILE_WORKLOAD:
+        w = ks.workloads()[WORKLOAD]
+        w.name, w.T = PROFILE_WORKLOAD, 8192
+        return w
+    return ks.workloads()[name]
+
+
 def dist_setup(args):
     import torch
 
@@ -229,7 +242,7 @@ def bench_prefill(args, ws_size, local):
     import linear_attention_recurrence_chunk_gb300 as kda
     from kda_synth.torchio import prefill_inputs
 
-    w = ks.workloads()[WORKLOAD]
+    w = get_workload(args.workload)
     t = prefill_inputs(w, "cuda")
     lib = kda.load_library()
     stream = torch.cuda.current_stream()

@@ -80,26 +80,6 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restri
   if (tid == 0) seq_chunk0[num_seqs] = min(s_carry, max_chunks);
 }
 
-// Where chunk j of the map lives in the packed token array.
-struct ChunkPos {
-  int32_t seq;
-  int64_t t0;
-  int32_t len;
-};
-
-__device__ __forceinline__ bool locate_chunk(const ChunkMap& m, const int32_t* cu, int32_t num_seqs, int64_t T_seq,
-                                             int32_t j, ChunkPos& p) {
-  if (j >= m.seq_chunk0[num_seqs]) return false;
-  const int32_t s = m.chunk_seq[j];
-  const int32_t local = j - m.seq_chunk0[s];
-  const int64_t start = cu ? (int64_t)cu[s] : (int64_t)s * T_seq;
-  const int64_t end = cu ? (int64_t)cu[s + 1] : start + T_seq;
-  p.seq = s;
-  p.t0 = start + (int64_t)local * kChunk;
-  p.len = (int32_t)min((int64_t)kChunk, end - p.t0);
-  return p.len > 0;
-}
-
 // Intermediate record of one (chunk, head) in the workspace (fp32 SIMT path).
 template <int DK, int DV>
 struct InterF32 {
@@ -415,15 +395,26 @@ static size_t inter_floats(int32_t d_k, int32_t d_v) {
 }
 
 Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
-                                 kda_dtype /*dt*/) {
+                                 kda_dtype dt) {
   Workspace w{};
   const int64_t max_chunks = (total_tokens + kChunk - 1) / kChunk + num_seqs;
   w.max_chunks = (int32_t)max_chunks;
-  w.inter_bytes_per_chunk_head = sizeof(float) * inter_floats(d_k, d_v);
+  w.tc = tc_path_supported(d_k, d_v, dt);
+  w.inter_bytes_per_chunk_head = w.tc ? tc_record_bytes(d_k, d_v) : sizeof(float) * inter_floats(d_k, d_v);
   w.off_seq_chunk0 = 0;
   w.off_chunk_seq = align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
   w.off_inter = w.off_chunk_seq + align256(sizeof(int32_t) * (size_t)std::max<int64_t>(max_chunks, 1));
-  w.bytes = w.off_inter + align256(w.inter_bytes_per_chunk_head * (size_t)max_chunks * (size_t)H);
+  const size_t R = (size_t)max_chunks * (size_t)H;
+  if (w.tc) {
+    w.off_wq = w.off_inter;
+    w.off_p = w.off_wq + align256(R * 128 * d_k * 2);
+    w.off_kt = w.off_p + align256(R * kChunk * kChunk * 2);
+    w.off_u = w.off_kt + align256(R * d_k * kChunk * 2);
+    w.off_gam = w.off_u + align256(R * kChunk * d_v * 2);
+    w.bytes = w.off_gam + align256(R * d_k * 4);
+  } else {
+    w.bytes = w.off_inter + align256(w.inter_bytes_per_chunk_head * R);
+  }
   return w;
 }
 
@@ -476,6 +467,7 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& p, const Workspace& ws, void* w
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (ws.tc) return launch_chunk_tc(p, ws, map, base, stream);
   if (p.dt == KDA_F32) return launch_simt_dims<float>(p, ws, map, inter, stream);
   return launch_simt_dims<__nv_bfloat16>(p, ws, map, inter, stream);
 }

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kda.h"
@@ -46,6 +47,26 @@ struct ChunkMap {
   int32_t max_chunks;    // upper bound used to size the grid
 };
 
+// Where chunk j of the map lives in the packed token array.
+struct ChunkPos {
+  int32_t seq;
+  int64_t t0;
+  int32_t len;
+};
+
+__device__ __forceinline__ bool locate_chunk(const ChunkMap& m, const int32_t* cu, int32_t num_seqs, int64_t T_seq,
+                                             int32_t j, ChunkPos& p) {
+  if (j >= m.seq_chunk0[num_seqs]) return false;
+  const int32_t s = m.chunk_seq[j];
+  const int32_t local = j - m.seq_chunk0[s];
+  const int64_t start = cu ? (int64_t)cu[s] : (int64_t)s * T_seq;
+  const int64_t end = cu ? (int64_t)cu[s + 1] : start + T_seq;
+  p.seq = s;
+  p.t0 = start + (int64_t)local * kChunk;
+  p.len = (int32_t)min((int64_t)kChunk, end - p.t0);
+  return p.len > 0;
+}
+
 // Problem description handed to the launchers (validated by the API layer).
 struct ChunkProblem {
   const void* q;
@@ -65,13 +86,30 @@ struct ChunkProblem {
   int32_t* dev_err;
 };
 
-// Workspace layout (all offsets 256-byte aligned).
+// Workspace layout (all offsets 256-byte aligned).  `tc` selects the bf16
+// tensor-core path (d_k = 128), whose per-(chunk, head) records are split into
+// separate arrays so that each can be read with 2D TMA tiles.
 struct Workspace {
   size_t bytes;
   size_t off_seq_chunk0, off_chunk_seq, off_inter;
   int32_t max_chunks;
   size_t inter_bytes_per_chunk_head;
+  bool tc;
+  size_t off_wq, off_p, off_kt, off_u, off_gam;   // tensor-core path arrays
 };
+
+// fp16 records of the tensor-core path, R = max_chunks * H records each.
+struct TcRecords {
+  __half* wq;           // [R][128][d_k]: rows 0-63 w = X Diag(beta)(k e^G), rows 64-127 q e^G
+  __half* p;            // [R][64][64]:   P (inclusive lower triangle)
+  __half* kt;           // [R][d_k][64]:  (k e^{G_last - G})^T, tokens contiguous
+  __half* u;            // [R][64][d_v]:  u = X Diag(beta) V
+  float* gam;           // [R][d_k]:      e^{G_last}
+};
+bool tc_path_supported(int32_t d_k, int32_t d_v, kda_dtype dt);
+size_t tc_record_bytes(int32_t d_k, int32_t d_v);
+cudaError_t launch_chunk_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap& map, char* base,
+                            cudaStream_t stream);
 Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v,
                                  kda_dtype dt);
 
