@@ -91,6 +91,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
+// (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
+__device__ __forceinline__ float fast_log_decay(float x) { return -5.f * __frcp_rn(1.f + __expf(-x)); }
+
+// bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi).
 __device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
   hi = __float2bfloat16_rn(x);
@@ -134,6 +146,12 @@ struct PrepTcSmem {
   static_assert(kBytes <= 232448, "fits the 227 KB shared-memory limit");
 };
 
+// A/P jobs per warp: (kind, row block a, column block b), kind 1 = A, 2 = P, 0 = none.
+__constant__ int8_t kApJobs[8][3][3] = {
+    {{2, 3, 3}, {2, 0, 0}, {0, 0, 0}}, {{2, 3, 2}, {2, 1, 0}, {0, 0, 0}}, {{2, 3, 1}, {1, 3, 3}, {1, 3, 2}},
+    {{2, 3, 0}, {1, 3, 1}, {1, 3, 0}}, {{2, 2, 2}, {1, 2, 2}, {1, 2, 1}}, {{2, 2, 1}, {1, 2, 0}, {1, 1, 1}},
+    {{2, 2, 0}, {1, 1, 0}, {1, 0, 0}}, {{2, 1, 1}, {0, 0, 0}, {0, 0, 0}}};
+
 // First row (in the column-operand area) of block-row a's column operand.
 __device__ __forceinline__ int cop_row0(int a) { return a == 0 ? 0 : (a == 1 ? 16 : (a == 2 ? 48 : 96)); }
 
@@ -175,21 +193,30 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) chunk_prep_tc(const bf16* _
   f16* o_u = out.u + rec * C * DV;
   float* o_gam = out.gam + rec * DK;
 
-  // 1. log-decay of every (row, channel); rows past the sequence end decay by 0
-  for (int idx = tid; idx < C * (DK / 8); idx += kPrepTcThreads) {
-    const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-    float lg[8];
+  // 1. log-decay of every (row, channel); rows past the sequence end decay by 0.
+  //    All four 16-byte loads of a thread are issued before any is used.
+  {
+    constexpr int kPer = C * (DK / 8) / kPrepTcThreads;   // 4
+    uint4 raw[kPer];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) lg[e] = 0.f;
-    if (r < pos.len) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(g + ((pos.t0 + r) * H + h) * DK + c8);
-      const bf16* x = reinterpret_cast<const bf16*>(&raw);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) lg[e] = log_decay(__bfloat162float(x[e]));
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = tid + j * kPrepTcThreads;
+      const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
+      raw[j] = r < pos.len ? *reinterpret_cast<const uint4*>(g + ((pos.t0 + r) * H + h) * DK + c8)
+                           : make_uint4(0u, 0u, 0u, 0u);
     }
-    float4* dst = reinterpret_cast<float4*>(sG + r * DK + c8);
-    dst[0] = make_float4(lg[0], lg[1], lg[2], lg[3]);
-    dst[1] = make_float4(lg[4], lg[5], lg[6], lg[7]);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = tid + j * kPrepTcThreads;
+      const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
+      const bf16* x = reinterpret_cast<const bf16*>(&raw[j]);
+      float lg[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) lg[e] = r < pos.len ? fast_log_decay(__bfloat162float(x[e])) : 0.f;
+      float4* dst = reinterpret_cast<float4*>(sG + r * DK + c8);
+      dst[0] = make_float4(lg[0], lg[1], lg[2], lg[3]);
+      dst[1] = make_float4(lg[4], lg[5], lg[6], lg[7]);
+    }
   }
   if (tid < C) sBeta[tid] = tid < pos.len ? beta[(pos.t0 + tid) * H + h] : 0.f;
   __syncthreads();
@@ -231,146 +258,231 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) chunk_prep_tc(const bf16* _
   }
   __syncthreads();
 
-  // 4. elementwise operands.  Thread -> channel c; rows of block a = tid/128 + 2*pass.
-  for (int pass = 0; pass < 2; ++pass) {
-    const int a = (tid >> 7) + 2 * pass, c = tid & (DK - 1);
-    const float gs = fGs[a * DK + c], lam = fLam[a * DK + c], psi = fPsi[a * DK + c];
-    float om[4];
+  // 4. elementwise operands.  Thread -> channel pair (c, c+1) and the 16 rows of
+  //    block a = tid / 64; every 16-bit operand is stored as a 32-bit pair.
+  {
+    const int a = tid >> 6, c = (tid & 63) * 2;
+    float2 gs, lam, psi, om[4];
+    gs = make_float2(fGs[a * DK + c], fGs[a * DK + c + 1]);
+    lam = make_float2(fLam[a * DK + c], fLam[a * DK + c + 1]);
+    psi = make_float2(fPsi[a * DK + c], fPsi[a * DK + c + 1]);
 #pragma unroll
-    for (int a2 = 0; a2 < 4; ++a2) om[a2] = a2 >= a ? fOm[(a2 * 4 + a) * DK + c] : 0.f;
-    uint32_t ktp[8];
+    for (int a2 = 0; a2 < 4; ++a2)
+      om[a2] = a2 >= a ? make_float2(fOm[(a2 * 4 + a) * DK + c], fOm[(a2 * 4 + a) * DK + c + 1]) : make_float2(0.f, 0.f);
+    // this thread's 16 rows of k and q (bf16 pairs), all loads in flight together
+    __nv_bfloat162 kq[16], qq[16];
 #pragma unroll
-    for (int rr = 0; rr < 16; rr += 2) {
-      float kt2[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int r = 16 * a + rr + e;
-        float kv = 0.f, qv = 0.f;
-        if (r < pos.len) {
-          const int64_t off = ((pos.t0 + r) * H + h) * DK + c;
-          kv = __bfloat162float(k[off]);
-          qv = __bfloat162float(q[off]);
-        }
-        const float ef = expf(sG[r * DK + c] - gs);   // e^{G_r - G_s} in (e^-80, 1]
-        const float ff = 1.f / ef;                    // e^{G_s - G_r} in [1, e^80)
-        const float kf = kv * ff;
-        sKE[r * LDB + c] = __float2bfloat16_rn(kv * ef);
-        split_bf16(qv * ef, sQE[r * LDB + c], sQEl[r * LDB + c]);
-#pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2)
-          if (a2 >= a) split_bf16(kf * om[a2], sCop[(cop_row0(a2) + r) * LDB + c], sCopl[(cop_row0(a2) + r) * LDB + c]);
-        sKV[r * LDKV + c] = __float2half_rn(sBeta[r] * kv * ef * lam);
-        o_wq[(C + r) * DK + c] = __float2half_rn(qv * ef * lam);
-        kt2[e] = kf * psi;
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * a + rr;
+      kq[rr] = __floats2bfloat162_rn(0.f, 0.f);
+      qq[rr] = kq[rr];
+      if (r < pos.len) {
+        const int64_t off = ((pos.t0 + r) * H + h) * DK + c;
+        kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(k + off);
+        qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(q + off);
       }
-      ktp[rr / 2] = pack_f16x2(kt2[0], kt2[1]);
     }
-    uint4* ktdst = reinterpret_cast<uint4*>(o_kt + c * C + 16 * a);
-    ktdst[0] = make_uint4(ktp[0], ktp[1], ktp[2], ktp[3]);
-    ktdst[1] = make_uint4(ktp[4], ktp[5], ktp[6], ktp[7]);
+    uint32_t kt0[8], kt1[8];   // K~^T rows c and c+1, tokens 16a..16a+15, fp16 pairs
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * a + rr;
+      const float2 gr = *reinterpret_cast<const float2*>(sG + r * DK + c);
+      const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
+      const float f0 = __frcp_rn(e0), f1 = __frcp_rn(e1);                 // e^{G_s - G_r} in [1, e^80)
+      const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
+      const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
+      const float br = sBeta[r];
+      *reinterpret_cast<__nv_bfloat162*>(sKE + r * LDB + c) = __floats2bfloat162_rn(k0 * e0, k1 * e1);
+      uint32_t hi, lo;
+      split_bf16x2(q0 * e0, q1 * e1, hi, lo);
+      *reinterpret_cast<uint32_t*>(sQE + r * LDB + c) = hi;
+      *reinterpret_cast<uint32_t*>(sQEl + r * LDB + c) = lo;
+      const float kf0 = k0 * f0, kf1 = k1 * f1;
+#pragma unroll
+      for (int a2 = 0; a2 < 4; ++a2) {
+        if (a2 >= a) {
+          split_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y, hi, lo);
+          *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = hi;
+          *reinterpret_cast<uint32_t*>(sCopl + (cop_row0(a2) + r) * LDB + c) = lo;
+        }
+      }
+      *reinterpret_cast<uint32_t*>(sKV + r * LDKV + c) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
+      *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
+      const __half2 kt = __floats2half2_rn(kf0 * psi.x, kf1 * psi.y);
+      const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
+      if (rr & 1) {
+        kt0[rr >> 1] |= lo16 << 16;
+        kt1[rr >> 1] |= hi16 << 16;
+      } else {
+        kt0[rr >> 1] = lo16;
+        kt1[rr >> 1] = hi16;
+      }
+    }
+    uint4* d0 = reinterpret_cast<uint4*>(o_kt + c * C + 16 * a);
+    uint4* d1 = reinterpret_cast<uint4*>(o_kt + (c + 1) * C + 16 * a);
+    d0[0] = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
+    d0[1] = make_uint4(kt0[4], kt0[5], kt0[6], kt0[7]);
+    d1[0] = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
+    d1[1] = make_uint4(kt1[4], kt1[5], kt1[6], kt1[7]);
   }
-  for (int idx = tid; idx < C * DV; idx += kPrepTcThreads) {
-    const int r = idx / DV, cc = idx % DV;
-    const float vv = r < pos.len ? __bfloat162float(v[((pos.t0 + r) * H + h) * DV + cc]) : 0.f;
-    sKV[r * LDKV + DK + cc] = __float2half_rn(sBeta[r] * vv);
+  {  // beta V, loads first (16-byte vectors)
+    constexpr int kPer = C * (DV / 8) / kPrepTcThreads;   // 4 or 2
+    uint4 raw[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = tid + j * kPrepTcThreads;
+      const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
+      raw[j] = r < pos.len ? *reinterpret_cast<const uint4*>(v + ((pos.t0 + r) * H + h) * DV + c8)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = tid + j * kPrepTcThreads;
+      const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
+      const bf16* x = reinterpret_cast<const bf16*>(&raw[j]);
+      const float br = sBeta[r];
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pk[e] = pack_f16x2(br * __bfloat162float(x[2 * e]), br * __bfloat162float(x[2 * e + 1]));
+      *reinterpret_cast<uint4*>(sKV + r * LDKV + DK + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
   }
   __syncthreads();
 
-  // 5. A (warps 0,2,4,6) and P (warps 1,3,5,7) of block-row a = warp/2:
-  //    [16 rows of block a] x [16(a+1) columns] over K = d_k, via m16n8k16.
-  const int a = warp >> 1;
-  const bool isP = warp & 1;
+  // 5. A and P, one 16x16 block (row block a, column block b <= a) per job; a
+  //    P block costs three MMAs per K step (split operands), an A block one, and
+  //    the jobs are spread so that every warp does five or six units of work.
   const int gq = lane >> 2, tq = lane & 3;
-  float acc[8][4];
+  float acc[3][2][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  {
-    // A: bf16 operands.  P: (hi + lo) x (hi + lo) without the lo*lo term.
+  for (int j = 0; j < 3; ++j)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
+    if (kind == 0) continue;
+    const bool isP = kind == 2;
     const bf16* rowop = (isP ? sQE : sKE) + (16 * a) * LDB;
     const bf16* rowlo = sQEl + (16 * a) * LDB;
-    const bf16* colop = sCop + cop_row0(a) * LDB;
-    const bf16* collo = sCopl + cop_row0(a) * LDB;
+    const bf16* colop = sCop + (cop_row0(a) + 16 * b) * LDB;
+    const bf16* collo = sCopl + (cop_row0(a) + 16 * b) * LDB;
 #pragma unroll
     for (int ks = 0; ks < DK / 16; ++ks) {
       const int aoff = (lane & 15) * LDB + ks * 16 + (lane >> 4) * 8;
-      uint32_t a0, a1, a2, a3, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+      const int boff = ((lane & 7) + (lane >> 4) * 8) * LDB + ks * 16 + ((lane >> 3) & 1) * 8;
+      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
       ldsm_x4(tc::smem_u32(rowop + aoff), a0, a1, a2, a3);
-      if (isP) ldsm_x4(tc::smem_u32(rowlo + aoff), l0, l1, l2, l3);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        if (np <= a) {
-          const int boff = (16 * np + (lane & 7) + (lane >> 4) * 8) * LDB + ks * 16 + ((lane >> 3) & 1) * 8;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
-          mma16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-          mma16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-          if (isP) {
-            mma16816(acc[2 * np], l0, l1, l2, l3, b0, b1);
-            mma16816(acc[2 * np + 1], l0, l1, l2, l3, b2, b3);
-            ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
-            mma16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-            mma16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-          }
-        }
+      ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
+      mma16816(acc[j][0], a0, a1, a2, a3, b0, b1);
+      mma16816(acc[j][1], a0, a1, a2, a3, b2, b3);
+      if (isP) {
+        uint32_t l0, l1, l2, l3;
+        ldsm_x4(tc::smem_u32(rowlo + aoff), l0, l1, l2, l3);
+        mma16816(acc[j][0], l0, l1, l2, l3, b0, b1);
+        mma16816(acc[j][1], l0, l1, l2, l3, b2, b3);
+        ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
+        mma16816(acc[j][0], a0, a1, a2, a3, b0, b1);
+        mma16816(acc[j][1], a0, a1, a2, a3, b2, b3);
       }
     }
   }
-  if (isP) {  // P (inclusive lower triangle) straight to the record; zeros elsewhere
+  // P blocks straight to the record (inclusive lower triangle), zeros above the block diagonal
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int i0 = 8 * nt + 2 * tq;
+  for (int j = 0; j < 3; ++j) {
+    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
+    if (kind != 2) continue;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int i0 = 16 * b + 8 * nt + 2 * tq;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = 16 * a + gq + 8 * hr;
-        const float v0 = (nt < 2 * (a + 1) && i0 <= r) ? acc[nt][2 * hr] : 0.f;
-        const float v1 = (nt < 2 * (a + 1) && i0 + 1 <= r) ? acc[nt][2 * hr + 1] : 0.f;
+        const float v0 = i0 <= r ? acc[j][nt][2 * hr] : 0.f;
+        const float v1 = i0 + 1 <= r ? acc[j][nt][2 * hr + 1] : 0.f;
         *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(v0, v1);
       }
     }
   }
+  for (int idx = tid; idx < 6 * 128; idx += kPrepTcThreads) {   // the 6 blocks above the diagonal, as pairs
+    const int blk = idx >> 7, e = idx & 127;
+    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+    const int r = 16 * a + (e >> 3), i = 16 * b + (e & 7) * 2;
+    *reinterpret_cast<uint32_t*>(o_p + r * C + i) = 0u;
+  }
   __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
-  if (!isP) {  // A = beta_r * (strictly lower part); zeros elsewhere
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int i0 = 8 * nt + 2 * tq;
+  for (int j = 0; j < 3; ++j) {   // A = beta_r * (strictly lower part)
+    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
+    if (kind != 1) continue;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int i0 = 16 * b + 8 * nt + 2 * tq;
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
         const int r = 16 * a + gq + 8 * hr;
         const float br = sBeta[r];
-        sA[r * LDA + i0] = (nt < 2 * (a + 1) && i0 < r) ? br * acc[nt][2 * hr] : 0.f;
-        sA[r * LDA + i0 + 1] = (nt < 2 * (a + 1) && i0 + 1 < r) ? br * acc[nt][2 * hr + 1] : 0.f;
+        sA[r * LDA + i0] = i0 < r ? br * acc[j][nt][2 * hr] : 0.f;
+        sA[r * LDA + i0 + 1] = i0 + 1 < r ? br * acc[j][nt][2 * hr + 1] : 0.f;
       }
     }
+  }
+  for (int idx = tid; idx < 6 * 256; idx += kPrepTcThreads) {   // zeros above the block diagonal of A
+    const int blk = idx >> 8, e = idx & 255;
+    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+    sA[(16 * a + (e >> 4)) * LDA + 16 * b + (e & 15)] = 0.f;
   }
   for (int idx = tid; idx < C * LDA; idx += kPrepTcThreads) sX[idx] = 0.f;
   __syncthreads();
 
   // 6. X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one
   //    column per thread, then X_ab = -X_aa sum_{b<=m<a} A_am X_mb.
-  if (tid < C) {
+  if (tid < C) {   // thread -> column j of diagonal block tid/16, kept in registers
     const int base = (tid / kSub) * kSub, j = tid % kSub;
-    for (int r = j; r < kSub; ++r) {
+    float xc[kSub];
+#pragma unroll
+    for (int r = 0; r < kSub; ++r) {
       float accx = (r == j) ? 1.f : 0.f;
-      for (int i = j; i < r; ++i) accx -= sA[(base + r) * LDA + base + i] * sX[(base + i) * LDA + base + j];
-      sX[(base + r) * LDA + base + j] = accx;
+#pragma unroll
+      for (int i = 0; i < r; ++i) accx -= sA[(base + r) * LDA + base + i] * xc[i];
+      xc[r] = r < j ? 0.f : accx;
     }
+#pragma unroll
+    for (int r = 0; r < kSub; ++r) sX[(base + r) * LDA + base + j] = xc[r];
   }
   __syncthreads();
-  for (int ab = 1; ab < C / kSub; ++ab) {
-    for (int e = tid; e < ab * kSub * kSub; e += kPrepTcThreads) {
-      const int b = e / (kSub * kSub), rr = (e / kSub) % kSub, cc = e % kSub;
-      float accy = 0.f;
-      for (int m = b * kSub; m < ab * kSub; ++m) accy += sA[(ab * kSub + rr) * LDA + m] * sX[m * LDA + b * kSub + cc];
-      sY[e] = accy;
+  {  // off-diagonal blocks, one element (row rr, column cc of the block) per thread
+    const int rr = tid >> 4, cc = tid & 15;
+#pragma unroll
+    for (int ab = 1; ab < C / kSub; ++ab) {
+#pragma unroll
+      for (int b = 0; b < ab; ++b) {   // Y_b = sum_{b <= m < ab} A_{ab,m} X_{m,b}
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int m = b * kSub; m < ab * kSub; m += 4) {
+          const float* arow = sA + (ab * kSub + rr) * LDA + m;
+          p0 += arow[0] * sX[(m + 0) * LDA + b * kSub + cc];
+          p1 += arow[1] * sX[(m + 1) * LDA + b * kSub + cc];
+          p2 += arow[2] * sX[(m + 2) * LDA + b * kSub + cc];
+          p3 += arow[3] * sX[(m + 3) * LDA + b * kSub + cc];
+        }
+        sY[(b * kSub + rr) * kSub + cc] = (p0 + p1) + (p2 + p3);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int b = 0; b < ab; ++b) {   // X_{ab,b} = -X_{ab,ab} Y_b (X_{ab,ab} is zero above its diagonal)
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < kSub; t += 2) {
+          p0 += sX[(ab * kSub + rr) * LDA + ab * kSub + t] * sY[(b * kSub + t) * kSub + cc];
+          p1 += sX[(ab * kSub + rr) * LDA + ab * kSub + t + 1] * sY[(b * kSub + t + 1) * kSub + cc];
+        }
+        sX[(ab * kSub + rr) * LDA + b * kSub + cc] = -(p0 + p1);
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int e = tid; e < ab * kSub * kSub; e += kPrepTcThreads) {
-      const int b = e / (kSub * kSub), rr = (e / kSub) % kSub, cc = e % kSub;
-      float accy = 0.f;
-      for (int t = 0; t <= rr; ++t) accy += sX[(ab * kSub + rr) * LDA + ab * kSub + t] * sY[b * kSub * kSub + t * kSub + cc];
-      sX[(ab * kSub + rr) * LDA + b * kSub + cc] = -accy;
-    }
-    __syncthreads();
   }
   for (int idx = tid; idx < C * C; idx += kPrepTcThreads) {
     const int r = idx / C, i = idx % C;
