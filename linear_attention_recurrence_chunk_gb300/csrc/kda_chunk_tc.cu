@@ -103,11 +103,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi).
-__device__ __forceinline__ void split_bf16(float x, bf16& hi, bf16& lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -532,7 +527,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) chunk_prep_tc(const bf16* _
 
 // -------------------------------------------------------------- chain kernel
 constexpr int kChainTcThreads = 160;          // 4 consumer warps (TMEM lanes 0-127) + 1 TMA producer warp
-constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, BV);
+// K-major A (TMA-staged tiles), MN-major B (the state block / V_new written by the threads), fp16,
+// M = 128, N = 32.
+constexpr uint32_t kIdescMN = tc::idesc_f16_f32(128, BV) | (1u << 16);
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemD12 = 0;    // two buffers of 32 columns (chunk parity)
+constexpr uint32_t kTmemD3 = 64;
 
 struct ChainTcSmem {
   // one pipeline stage (all tiles 1024-byte aligned, 128-byte swizzle unless noted)
@@ -543,21 +543,21 @@ struct ChainTcSmem {
   static constexpr uint32_t oGam = 69632;      // e^{G_last}, 128 fp32
   static constexpr uint32_t kStage = 71680;    // 70 KB, keeps the next stage 1024-aligned
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
-  static constexpr uint32_t oS = 2 * kStage;   // S block as the B operand: [32 value cols][128 keys], 2 atoms
-  static constexpr uint32_t oVN = oS + 8192;   // V_new as the B operand: [32 value cols][64 tokens]
+  static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
+  static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
   static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain
   static constexpr uint32_t oTmem = oBar + 7 * 8;
   static constexpr uint32_t kBytes = oTmem + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
 
-__device__ __forceinline__ void store_s_operand(uint8_t* sS, int c, const float (&S)[32]) {
-  // element (value column n, key c) of the K-major fp16 B operand
-  uint8_t* atom = sS + (c >> 6) * 4096;
-  const int col = c & 63;
+// 32 fp32 values of K row `k` of an MN-major SW64 operand, as fp16, in four 16-byte stores.
+__device__ __forceinline__ void store_mn_row(uint8_t* tile, int k, const float (&x)[32]) {
 #pragma unroll
-  for (int n = 0; n < BV; ++n)
-    *reinterpret_cast<f16*>(atom + tc::sw128_offset(n, col)) = __float2half_rn(S[n]);
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(tile + tc::sw64_chunk_offset(k, j)) =
+        make_uint4(pack_f16x2(x[8 * j + 0], x[8 * j + 1]), pack_f16x2(x[8 * j + 2], x[8 * j + 3]),
+                   pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
 }
 
 template <int DV>
@@ -597,14 +597,14 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     *reinterpret_cast<uint4*>(sm + st * L::kStage + L::oPZ + off) = make_uint4(0u, 0u, 0u, 0u);
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 64);
+    tc::tmem_alloc(tslot, kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = *tslot;   // columns [0, 32): D12, [32, 64): D3
+  const uint32_t tmem = *tslot;
 
   if (warp == 4) {
     // ---------------- TMA producer
@@ -648,33 +648,53 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         S[n] = x.x; S[n + 1] = x.y; S[n + 2] = x.z; S[n + 3] = x.w;
       }
     }
-    store_s_operand(sS, c, S);
+    store_mn_row(sS, c, S);
+    // Operand descriptors: B tiles never move; A tiles differ per stage only by
+    // the stage offset, and K slices by constant offsets added to the start field.
+    const uint64_t dS0 = tc::desc_mnmajor_sw64(tc::smem_u32(sS));
+    const uint64_t dV0 = tc::desc_mnmajor_sw64(tc::smem_u32(sVN));
+    const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));   // stage 0 base
     bool bad = false;
     bool issued = false;   // thread 0: some MMA was issued
     int i = 0;
+    int64_t prev_t0 = 0;
+    int64_t prev_len = 0;
     for (; i < nch; ++i) {
       const int st = i & 1;
       uint8_t* stg = sm + st * L::kStage;
+      const uint32_t d12 = tmem + kTmemD12 + (uint32_t)st * 32;
       bad |= !tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (tc::bar_sync_or(1, 128, bad)) break;
       tc::tc_fence_after();
+      const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
       if (tid == 0) {   // round 1: D12 = [w; q e^G] . S
-        const uint32_t aw = tc::smem_u32(stg + L::oWQ), bs = tc::smem_u32(sS);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk)
-          tc::mma_16bit(tmem, tc::desc_kmajor_sw128(aw + (kk >> 2) * 16384 + (kk & 3) * 32),
-                       tc::desc_kmajor_sw128(bs + (kk >> 2) * 4096 + (kk & 3) * 32), kIdesc, kk > 0);
+          tc::mma_16bit(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN,
+                        kk > 0);
         tc::mma_commit(mma1);
         issued = true;
+      }
+      if (i > 0 && warp >= 2 && !bad) {   // previous chunk's o rows (tokens) = lanes 64-127 of the other buffer
+        const int r = tid - 64;
+        float ov[32];
+        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)(st ^ 1) * 32), ov);
+        if (r < prev_len) {
+          uint4* dst = reinterpret_cast<uint4*>(o + ((prev_t0 + r) * H + h) * DV + n0);
+#pragma unroll
+          for (int q4 = 0; q4 < BV / 8; ++q4)
+            dst[q4] = make_uint4(pack_bf16x2(ov[8 * q4 + 0], ov[8 * q4 + 1]), pack_bf16x2(ov[8 * q4 + 2], ov[8 * q4 + 3]),
+                                 pack_bf16x2(ov[8 * q4 + 4], ov[8 * q4 + 5]), pack_bf16x2(ov[8 * q4 + 6], ov[8 * q4 + 7]));
+        }
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
       tc::tc_fence_after();
-      if (!bad && warp < 2) {   // V_new rows (tokens) 0-63: u - w S, as the K-major B operand
+      if (!bad && warp < 2) {   // V_new rows (tokens) 0-63: u - w S
         float d[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 0), d);
+        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)st * 32), d);
         const int r = tid;
         const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + r * BV * 2);
 #pragma unroll
@@ -682,26 +702,21 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
           const uint4 raw = urow[q4];
           const f16* uv = reinterpret_cast<const f16*>(&raw);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int n = q4 * 8 + e;
-            *reinterpret_cast<f16*>(sVN + tc::sw128_offset(n, r)) = __float2half_rn(__half2float(uv[e]) - d[n]);
-          }
+          for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
         }
+        store_mn_row(sVN, r, d);
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       if (tc::bar_sync_or(1, 128, bad)) break;
       tc::tc_fence_after();
       if (tid == 0) {   // round 2: D12 += [0; P] . V_new ; D3 = K~^T . V_new
-        const uint32_t bv = tc::smem_u32(sVN);
-        const uint32_t ap = tc::smem_u32(stg + L::oPZ), ak = tc::smem_u32(stg + L::oKT);
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          tc::mma_16bit(tmem, tc::desc_kmajor_sw128(ap + kk * 32), tc::desc_kmajor_sw128(bv + kk * 32), kIdesc, 1);
+          tc::mma_16bit(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, 1);
 #pragma unroll
         for (int kk = 0; kk < C / 16; ++kk)
-          tc::mma_16bit(tmem + 32, tc::desc_kmajor_sw128(ak + kk * 32), tc::desc_kmajor_sw128(bv + kk * 32), kIdesc,
-                       kk > 0);
+          tc::mma_16bit(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, kk > 0);
         tc::mma_commit(mma2);
         tc::mma_commit(empty + st);
       }
@@ -709,24 +724,24 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       tc::tc_fence_after();
       if (!bad) {
         float d[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 32), d);
+        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD3), d);
 #pragma unroll
         for (int n = 0; n < BV; ++n) S[n] = gam * S[n] + d[n];
-        store_s_operand(sS, c, S);
-        if (warp >= 2) {   // o rows (tokens) = TMEM lanes 64-127
-          const int r = tid - 64;
-          const int64_t t0 = seq_start + (int64_t)i * C;
-          const int64_t len = min((int64_t)C, seq_end - t0);
-          float ov[32];
-          tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, 0), ov);
-          if (r < len) {
-            uint4* dst = reinterpret_cast<uint4*>(o + ((t0 + r) * H + h) * DV + n0);
+        store_mn_row(sS, c, S);
+      }
+      prev_t0 = seq_start + (int64_t)i * C;
+      prev_len = min((int64_t)C, seq_end - prev_t0);
+    }
+    if (i == nch && !bad && nch > 0 && warp >= 2) {   // the last chunk's o
+      const int r = tid - 64;
+      float ov[32];
+      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32), ov);
+      if (r < prev_len) {
+        uint4* dst = reinterpret_cast<uint4*>(o + ((prev_t0 + r) * H + h) * DV + n0);
 #pragma unroll
-            for (int q4 = 0; q4 < BV / 8; ++q4)
-              dst[q4] = make_uint4(pack_bf16x2(ov[8 * q4 + 0], ov[8 * q4 + 1]), pack_bf16x2(ov[8 * q4 + 2], ov[8 * q4 + 3]),
-                                   pack_bf16x2(ov[8 * q4 + 4], ov[8 * q4 + 5]), pack_bf16x2(ov[8 * q4 + 6], ov[8 * q4 + 7]));
-          }
-        }
+        for (int q4 = 0; q4 < BV / 8; ++q4)
+          dst[q4] = make_uint4(pack_bf16x2(ov[8 * q4 + 0], ov[8 * q4 + 1]), pack_bf16x2(ov[8 * q4 + 2], ov[8 * q4 + 3]),
+                               pack_bf16x2(ov[8 * q4 + 4], ov[8 * q4 + 5]), pack_bf16x2(ov[8 * q4 + 6], ov[8 * q4 + 7]));
       }
     }
     if (i < nch || bad) {
@@ -743,7 +758,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 64);
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // --------------------------------------------------------------- host side

@@ -144,6 +144,26 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t addr) {
   return d;
 }
 
+// Descriptor of an MN-major 16-bit operand with 64-byte swizzle: each K row
+// holds 32 MN elements (64 bytes), 8-row K groups are 512 bytes apart, the
+// 16-byte chunks of K row k XOR-ed with (k / 2) % 4.  `addr` is the shared
+// address of the first K row of the slice (K slices of 16 rows are 1024 bytes
+// apart); the tile must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw64(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);   // start address >> 4
+  d |= (uint64_t)1u << 16;                  // leading byte offset (one 32-element MN group: unused)
+  d |= (uint64_t)(512u >> 4) << 32;         // stride byte offset: 8 K rows x 64 B
+  d |= (uint64_t)1u << 46;                  // descriptor version 1
+  d |= (uint64_t)4u << 61;                  // 64-byte swizzle
+  return d;
+}
+
+// Byte offset of the 16-byte chunk j (MN elements 8j..8j+7) of K row k in that layout.
+__host__ __device__ __forceinline__ uint32_t sw64_chunk_offset(uint32_t k, uint32_t j) {
+  return k * 64u + (((j ^ (k >> 1)) & 3u) << 4);
+}
+
 // Byte offset of element (row, col) inside a [rows x 64] bf16 tile stored in
 // the 128-byte swizzle pattern.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
@@ -177,6 +197,25 @@ __device__ __forceinline__ void mma_16bit(uint32_t d_tmem, uint64_t a_desc, uint
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Same with the A operand already in TMEM (lane = row, 16-bit K elements packed
+// two per column, a K = 16 slice spanning 8 columns).
+__device__ __forceinline__ void mma_16bit_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Asynchronous copy of a 128-row x 32-byte (one K = 16 slice of 16-bit values)
+// operand slice, described by a shared-memory matrix descriptor, into TMEM.
+// Ordered with the MMAs issued later by the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
 }
 
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
