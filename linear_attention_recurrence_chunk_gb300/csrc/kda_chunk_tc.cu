@@ -38,6 +38,7 @@
 // the block); across blocks both factors are <= 1.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -110,7 +111,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // --------------------------------------------------------------- prep kernel
-constexpr int kPrepTcThreads = 256;
+constexpr int kPrepTcThreads = 512;
 
 template <int DV>
 struct PrepTcSmem {
@@ -141,24 +142,27 @@ struct PrepTcSmem {
   static_assert(kBytes <= 232448, "fits the 227 KB shared-memory limit");
 };
 
-// A/P jobs per warp: (kind, row block a, column block b), kind 1 = A, 2 = P, 0 = none.
-__constant__ int8_t kApJobs[8][3][3] = {
-    {{2, 3, 3}, {2, 0, 0}, {0, 0, 0}}, {{2, 3, 2}, {2, 1, 0}, {0, 0, 0}}, {{2, 3, 1}, {1, 3, 3}, {1, 3, 2}},
-    {{2, 3, 0}, {1, 3, 1}, {1, 3, 0}}, {{2, 2, 2}, {1, 2, 2}, {1, 2, 1}}, {{2, 2, 1}, {1, 2, 0}, {1, 1, 1}},
-    {{2, 2, 0}, {1, 1, 0}, {1, 0, 0}}, {{2, 1, 1}, {0, 0, 0}, {0, 0, 0}}};
+// A/P jobs per warp (16 warps): (kind, row block a, column block b), kind 1 = A,
+// 2 = P, 0 = none.  Warps 0-9 take one P block each (three MMAs per K step),
+// warps 10-15 share the ten A blocks (one MMA per K step).
+__constant__ int8_t kApJobs[16][2][3] = {
+    {{2, 3, 3}, {0, 0, 0}}, {{2, 3, 2}, {0, 0, 0}}, {{2, 3, 1}, {0, 0, 0}}, {{2, 3, 0}, {0, 0, 0}},
+    {{2, 2, 2}, {0, 0, 0}}, {{2, 2, 1}, {0, 0, 0}}, {{2, 2, 0}, {0, 0, 0}}, {{2, 1, 1}, {0, 0, 0}},
+    {{2, 1, 0}, {0, 0, 0}}, {{2, 0, 0}, {0, 0, 0}}, {{1, 3, 3}, {1, 3, 2}}, {{1, 3, 1}, {1, 3, 0}},
+    {{1, 2, 2}, {1, 2, 1}}, {{1, 2, 0}, {1, 1, 1}}, {{1, 1, 0}, {0, 0, 0}}, {{1, 0, 0}, {0, 0, 0}}};
 
 // First row (in the column-operand area) of block-row a's column operand.
 __device__ __forceinline__ int cop_row0(int a) { return a == 0 ? 0 : (a == 1 ? 16 : (a == 2 ? 48 : 96)); }
 
 
 template <int DV>
-__global__ void __launch_bounds__(kPrepTcThreads, 1) chunk_prep_tc(const bf16* __restrict__ q, const bf16* __restrict__ k,
-                                                                  const bf16* __restrict__ v, const bf16* __restrict__ g,
-                                                                  const float* __restrict__ beta,
-                                                                  const int32_t* __restrict__ cu, int32_t num_seqs,
-                                                                  int64_t T_seq, int32_t H, ChunkMap map, TcRecords out) {
+__global__ void __launch_bounds__(kPrepTcThreads, 1)
+    chunk_prep_tc(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+                  const bf16* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
+                  int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map, TcRecords out, int64_t n_tasks) {
   using L = PrepTcSmem<DV>;
   constexpr int LDB = L::LDB, LDKV = L::LDKV, LDX = L::LDX, LDA = L::LDA;
+  constexpr int NTH = kPrepTcThreads;
   extern __shared__ __align__(16) uint8_t smem[];
   float* sG = reinterpret_cast<float*>(smem + L::oG);
   bf16* sKE = reinterpret_cast<bf16*>(smem + L::oKE);
@@ -176,352 +180,371 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1) chunk_prep_tc(const bf16* _
   float* sX = reinterpret_cast<float*>(smem + L::oX);
   float* sY = reinterpret_cast<float*>(smem + L::oY);
   f16* sXb = reinterpret_cast<f16*>(smem + L::oXb);
-
-  ChunkPos pos;
-  if (!locate_chunk(map, cu, num_seqs, T_seq, blockIdx.x, pos)) return;
-  const int h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t rec = (int64_t)blockIdx.x * H + h;
-  f16* o_wq = out.wq + rec * 128 * DK;
-  f16* o_p = out.p + rec * C * C;
-  f16* o_kt = out.kt + rec * DK * C;
-  f16* o_u = out.u + rec * C * DV;
-  float* o_gam = out.gam + rec * DK;
-
-  // 1. log-decay of every (row, channel); rows past the sequence end decay by 0.
-  //    All four 16-byte loads of a thread are issued before any is used.
-  {
-    constexpr int kPer = C * (DK / 8) / kPrepTcThreads;   // 4
-    uint4 raw[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int idx = tid + j * kPrepTcThreads;
-      const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-      raw[j] = r < pos.len ? *reinterpret_cast<const uint4*>(g + ((pos.t0 + r) * H + h) * DK + c8)
-                           : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int idx = tid + j * kPrepTcThreads;
-      const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-      const bf16* x = reinterpret_cast<const bf16*>(&raw[j]);
-      float lg[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) lg[e] = r < pos.len ? fast_log_decay(__bfloat162float(x[e])) : 0.f;
-      float4* dst = reinterpret_cast<float4*>(sG + r * DK + c8);
-      dst[0] = make_float4(lg[0], lg[1], lg[2], lg[3]);
-      dst[1] = make_float4(lg[4], lg[5], lg[6], lg[7]);
-    }
-  }
-  if (tid < C) sBeta[tid] = tid < pos.len ? beta[(pos.t0 + tid) * H + h] : 0.f;
-  __syncthreads();
-
-  // 2. inclusive cumulative sum over the chunk's rows: two half-scans, then the fix-up
-  {
-    const int c = tid & (DK - 1), half = tid >> 7;
-    float run = 0.f;
-    for (int r = 32 * half; r < 32 * half + 32; ++r) {
-      run += sG[r * DK + c];
-      sG[r * DK + c] = run;
-    }
-  }
-  __syncthreads();
-  if (tid >= DK) {
-    const int c = tid - DK;
-    const float add = sG[31 * DK + c];
-    for (int r = 32; r < C; ++r) sG[r * DK + c] += add;
-  }
-  __syncthreads();
-
-  // 3. per (16-row block, channel) factors
-  if (tid < DK) {
-    const int c = tid;
-    const float gl = sG[(C - 1) * DK + c];
-    float gs[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      gs[a] = a ? sG[(16 * a - 1) * DK + c] : 0.f;
-      fGs[a * DK + c] = gs[a];
-      fLam[a * DK + c] = expf(gs[a]);
-      fPsi[a * DK + c] = expf(gl - gs[a]);
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b <= a; ++b) fOm[(a * 4 + b) * DK + c] = a == b ? 1.f : expf(gs[a] - gs[b]);
-    o_gam[c] = expf(gl);
-  }
-  __syncthreads();
-
-  // 4. elementwise operands.  Thread -> channel pair (c, c+1) and the 16 rows of
-  //    block a = tid / 64; every 16-bit operand is stored as a 32-bit pair.
-  {
-    const int a = tid >> 6, c = (tid & 63) * 2;
-    float2 gs, lam, psi, om[4];
-    gs = make_float2(fGs[a * DK + c], fGs[a * DK + c + 1]);
-    lam = make_float2(fLam[a * DK + c], fLam[a * DK + c + 1]);
-    psi = make_float2(fPsi[a * DK + c], fPsi[a * DK + c + 1]);
-#pragma unroll
-    for (int a2 = 0; a2 < 4; ++a2)
-      om[a2] = a2 >= a ? make_float2(fOm[(a2 * 4 + a) * DK + c], fOm[(a2 * 4 + a) * DK + c + 1]) : make_float2(0.f, 0.f);
-    // this thread's 16 rows of k and q (bf16 pairs), all loads in flight together
-    __nv_bfloat162 kq[16], qq[16];
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = 16 * a + rr;
-      kq[rr] = __floats2bfloat162_rn(0.f, 0.f);
-      qq[rr] = kq[rr];
-      if (r < pos.len) {
-        const int64_t off = ((pos.t0 + r) * H + h) * DK + c;
-        kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(k + off);
-        qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(q + off);
-      }
-    }
-    uint32_t kt0[8], kt1[8];   // K~^T rows c and c+1, tokens 16a..16a+15, fp16 pairs
-#pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = 16 * a + rr;
-      const float2 gr = *reinterpret_cast<const float2*>(sG + r * DK + c);
-      const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
-      const float f0 = __frcp_rn(e0), f1 = __frcp_rn(e1);                 // e^{G_s - G_r} in [1, e^80)
-      const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
-      const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
-      const float br = sBeta[r];
-      *reinterpret_cast<__nv_bfloat162*>(sKE + r * LDB + c) = __floats2bfloat162_rn(k0 * e0, k1 * e1);
-      uint32_t hi, lo;
-      split_bf16x2(q0 * e0, q1 * e1, hi, lo);
-      *reinterpret_cast<uint32_t*>(sQE + r * LDB + c) = hi;
-      *reinterpret_cast<uint32_t*>(sQEl + r * LDB + c) = lo;
-      const float kf0 = k0 * f0, kf1 = k1 * f1;
-#pragma unroll
-      for (int a2 = 0; a2 < 4; ++a2) {
-        if (a2 >= a) {
-          split_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y, hi, lo);
-          *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = hi;
-          *reinterpret_cast<uint32_t*>(sCopl + (cop_row0(a2) + r) * LDB + c) = lo;
-        }
-      }
-      *reinterpret_cast<uint32_t*>(sKV + r * LDKV + c) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
-      *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
-      const __half2 kt = __floats2half2_rn(kf0 * psi.x, kf1 * psi.y);
-      const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
-      if (rr & 1) {
-        kt0[rr >> 1] |= lo16 << 16;
-        kt1[rr >> 1] |= hi16 << 16;
-      } else {
-        kt0[rr >> 1] = lo16;
-        kt1[rr >> 1] = hi16;
-      }
-    }
-    uint4* d0 = reinterpret_cast<uint4*>(o_kt + c * C + 16 * a);
-    uint4* d1 = reinterpret_cast<uint4*>(o_kt + (c + 1) * C + 16 * a);
-    d0[0] = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
-    d0[1] = make_uint4(kt0[4], kt0[5], kt0[6], kt0[7]);
-    d1[0] = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
-    d1[1] = make_uint4(kt1[4], kt1[5], kt1[6], kt1[7]);
-  }
-  {  // beta V, loads first (16-byte vectors)
-    constexpr int kPer = C * (DV / 8) / kPrepTcThreads;   // 4 or 2
-    uint4 raw[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int idx = tid + j * kPrepTcThreads;
-      const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
-      raw[j] = r < pos.len ? *reinterpret_cast<const uint4*>(v + ((pos.t0 + r) * H + h) * DV + c8)
-                           : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int idx = tid + j * kPrepTcThreads;
-      const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
-      const bf16* x = reinterpret_cast<const bf16*>(&raw[j]);
-      const float br = sBeta[r];
-      uint32_t pk[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) pk[e] = pack_f16x2(br * __bfloat162float(x[2 * e]), br * __bfloat162float(x[2 * e + 1]));
-      *reinterpret_cast<uint4*>(sKV + r * LDKV + DK + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-  }
-  __syncthreads();
-
-  // 5. A and P, one 16x16 block (row block a, column block b <= a) per job; a
-  //    P block costs three MMAs per K step (split operands), an A block one, and
-  //    the jobs are spread so that every warp does five or six units of work.
   const int gq = lane >> 2, tq = lane & 3;
-  float acc[3][2][4];
-#pragma unroll
-  for (int j = 0; j < 3; ++j)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
-    if (kind == 0) continue;
-    const bool isP = kind == 2;
-    const bf16* rowop = (isP ? sQE : sKE) + (16 * a) * LDB;
-    const bf16* rowlo = sQEl + (16 * a) * LDB;
-    const bf16* colop = sCop + (cop_row0(a) + 16 * b) * LDB;
-    const bf16* collo = sCopl + (cop_row0(a) + 16 * b) * LDB;
-#pragma unroll
-    for (int ks = 0; ks < DK / 16; ++ks) {
-      const int aoff = (lane & 15) * LDB + ks * 16 + (lane >> 4) * 8;
-      const int boff = ((lane & 7) + (lane >> 4) * 8) * LDB + ks * 16 + ((lane >> 3) & 1) * 8;
-      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      ldsm_x4(tc::smem_u32(rowop + aoff), a0, a1, a2, a3);
-      ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
-      mma16816(acc[j][0], a0, a1, a2, a3, b0, b1);
-      mma16816(acc[j][1], a0, a1, a2, a3, b2, b3);
-      if (isP) {
-        uint32_t l0, l1, l2, l3;
-        ldsm_x4(tc::smem_u32(rowlo + aoff), l0, l1, l2, l3);
-        mma16816(acc[j][0], l0, l1, l2, l3, b0, b1);
-        mma16816(acc[j][1], l0, l1, l2, l3, b2, b3);
-        ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
-        mma16816(acc[j][0], a0, a1, a2, a3, b0, b1);
-        mma16816(acc[j][1], a0, a1, a2, a3, b2, b3);
+
+  // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
+  for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+    const int32_t j = (int32_t)(task / H);
+    const int h = (int)(task % H);
+    ChunkPos pos;
+    if (!locate_chunk(map, cu, num_seqs, T_seq, j, pos)) continue;
+    const int64_t rec = task;   // == j * H + h
+    f16* o_wq = out.wq + rec * 128 * DK;
+    f16* o_p = out.p + rec * C * C;
+    f16* o_kt = out.kt + rec * DK * C;
+    f16* o_u = out.u + rec * C * DV;
+    float* o_gam = out.gam + rec * DK;
+
+    {  // pull this CTA's next task's input rows into L2 (one 128-byte line per thread)
+      const int64_t nt = task + gridDim.x;
+      ChunkPos np;
+      if (nt < n_tasks && locate_chunk(map, cu, num_seqs, T_seq, (int32_t)(nt / H), np)) {
+        const int tensor = tid >> 7, r = (tid & 127) >> 1, half = tid & 1;
+        const int d = tensor == 3 ? DV : DK;
+        if (r < np.len && half * 64 < d) {
+          const bf16* base = tensor == 0 ? g : (tensor == 1 ? k : (tensor == 2 ? q : v));
+          const bf16* p = base + ((np.t0 + r) * H + (int)(nt % H)) * d + half * 64;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
       }
     }
-  }
-  // P blocks straight to the record (inclusive lower triangle), zeros above the block diagonal
+
+    // 1. log-decay of every (row, channel); rows past the sequence end decay by 0
+    {
+      constexpr int kPer = C * (DK / 8) / NTH;   // 2
+      uint4 raw[kPer];
 #pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
-    if (kind != 2) continue;
+      for (int e2 = 0; e2 < kPer; ++e2) {
+        const int idx = tid + e2 * NTH;
+        const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
+        raw[e2] = r < pos.len ? *reinterpret_cast<const uint4*>(g + ((pos.t0 + r) * H + h) * DK + c8)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int i0 = 16 * b + 8 * nt + 2 * tq;
+      for (int e2 = 0; e2 < kPer; ++e2) {
+        const int idx = tid + e2 * NTH;
+        const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
+        const bf16* x = reinterpret_cast<const bf16*>(&raw[e2]);
+        float lg[8];
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = 16 * a + gq + 8 * hr;
-        const float v0 = i0 <= r ? acc[j][nt][2 * hr] : 0.f;
-        const float v1 = i0 + 1 <= r ? acc[j][nt][2 * hr + 1] : 0.f;
-        *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(v0, v1);
+        for (int e = 0; e < 8; ++e) lg[e] = r < pos.len ? fast_log_decay(__bfloat162float(x[e])) : 0.f;
+        float4* dst = reinterpret_cast<float4*>(sG + r * DK + c8);
+        dst[0] = make_float4(lg[0], lg[1], lg[2], lg[3]);
+        dst[1] = make_float4(lg[4], lg[5], lg[6], lg[7]);
       }
     }
-  }
-  for (int idx = tid; idx < 6 * 128; idx += kPrepTcThreads) {   // the 6 blocks above the diagonal, as pairs
-    const int blk = idx >> 7, e = idx & 127;
-    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-    const int r = 16 * a + (e >> 3), i = 16 * b + (e & 7) * 2;
-    *reinterpret_cast<uint32_t*>(o_p + r * C + i) = 0u;
-  }
-  __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
+    if (tid < C) sBeta[tid] = tid < pos.len ? beta[(pos.t0 + tid) * H + h] : 0.f;
+    __syncthreads();
+
+    // 2. inclusive cumulative sum over the chunk's rows: four 16-row scans, then the fix-up
+    {
+      const int c = tid & (DK - 1), qt = tid >> 7;
+      float run = 0.f;
 #pragma unroll
-  for (int j = 0; j < 3; ++j) {   // A = beta_r * (strictly lower part)
-    const int kind = kApJobs[warp][j][0], a = kApJobs[warp][j][1], b = kApJobs[warp][j][2];
-    if (kind != 1) continue;
+      for (int r = 16 * qt; r < 16 * qt + 16; ++r) {
+        run += sG[r * DK + c];
+        sG[r * DK + c] = run;
+      }
+      __syncthreads();
+      float add = 0.f;
+      for (int q2 = 0; q2 < qt; ++q2) add += sG[(16 * q2 + 15) * DK + c];
+      __syncthreads();
+      if (qt > 0) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int i0 = 16 * b + 8 * nt + 2 * tq;
+        for (int r = 16 * qt; r < 16 * qt + 16; ++r) sG[r * DK + c] += add;
+      }
+    }
+    __syncthreads();
+
+    // 3. per (16-row block, channel) factors
+    if (tid < DK) {
+      const int c = tid;
+      const float gl = sG[(C - 1) * DK + c];
+      float gs[4];
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = 16 * a + gq + 8 * hr;
+      for (int a = 0; a < 4; ++a) {
+        gs[a] = a ? sG[(16 * a - 1) * DK + c] : 0.f;
+        fGs[a * DK + c] = gs[a];
+        fLam[a * DK + c] = expf(gs[a]);
+        fPsi[a * DK + c] = expf(gl - gs[a]);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b <= a; ++b) fOm[(a * 4 + b) * DK + c] = a == b ? 1.f : expf(gs[a] - gs[b]);
+      o_gam[c] = expf(gl);
+    }
+    __syncthreads();
+
+    // 4. elementwise operands.  Thread -> channel pair (c, c+1) and 8 rows of
+    //    block a; every 16-bit operand is stored as a 32-bit pair.
+    {
+      const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2;
+      const int r0 = 16 * a + 8 * (rg & 1);
+      const float2 gs = make_float2(fGs[a * DK + c], fGs[a * DK + c + 1]);
+      const float2 lam = make_float2(fLam[a * DK + c], fLam[a * DK + c + 1]);
+      const float2 psi = make_float2(fPsi[a * DK + c], fPsi[a * DK + c + 1]);
+      float2 om[4];
+#pragma unroll
+      for (int a2 = 0; a2 < 4; ++a2)
+        om[a2] = a2 >= a ? make_float2(fOm[(a2 * 4 + a) * DK + c], fOm[(a2 * 4 + a) * DK + c + 1]) : make_float2(0.f, 0.f);
+      __nv_bfloat162 kq[8], qq[8];
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = r0 + rr;
+        kq[rr] = __floats2bfloat162_rn(0.f, 0.f);
+        qq[rr] = kq[rr];
+        if (r < pos.len) {
+          const int64_t off = ((pos.t0 + r) * H + h) * DK + c;
+          kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(k + off);
+          qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(q + off);
+        }
+      }
+      uint32_t kt0[4], kt1[4];   // K~^T rows c and c+1, tokens r0..r0+7, fp16 pairs
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = r0 + rr;
+        const float2 gr = *reinterpret_cast<const float2*>(sG + r * DK + c);
+        const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
+        const float f0 = __frcp_rn(e0), f1 = __frcp_rn(e1);                 // e^{G_s - G_r} in [1, e^80)
+        const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
+        const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
         const float br = sBeta[r];
-        sA[r * LDA + i0] = i0 < r ? br * acc[j][nt][2 * hr] : 0.f;
-        sA[r * LDA + i0 + 1] = i0 + 1 < r ? br * acc[j][nt][2 * hr + 1] : 0.f;
+        *reinterpret_cast<__nv_bfloat162*>(sKE + r * LDB + c) = __floats2bfloat162_rn(k0 * e0, k1 * e1);
+        uint32_t hi, lo;
+        split_bf16x2(q0 * e0, q1 * e1, hi, lo);
+        *reinterpret_cast<uint32_t*>(sQE + r * LDB + c) = hi;
+        *reinterpret_cast<uint32_t*>(sQEl + r * LDB + c) = lo;
+        const float kf0 = k0 * f0, kf1 = k1 * f1;
+#pragma unroll
+        for (int a2 = 0; a2 < 4; ++a2) {
+          if (a2 >= a) {
+            split_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y, hi, lo);
+            *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = hi;
+            *reinterpret_cast<uint32_t*>(sCopl + (cop_row0(a2) + r) * LDB + c) = lo;
+          }
+        }
+        *reinterpret_cast<uint32_t*>(sKV + r * LDKV + c) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
+        *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
+        const __half2 kt = __floats2half2_rn(kf0 * psi.x, kf1 * psi.y);
+        const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
+        if (rr & 1) {
+          kt0[rr >> 1] |= lo16 << 16;
+          kt1[rr >> 1] |= hi16 << 16;
+        } else {
+          kt0[rr >> 1] = lo16;
+          kt1[rr >> 1] = hi16;
+        }
+      }
+      *reinterpret_cast<uint4*>(o_kt + c * C + r0) = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
+      *reinterpret_cast<uint4*>(o_kt + (c + 1) * C + r0) = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
+    }
+    {  // beta V, loads first (16-byte vectors)
+      constexpr int kPer = C * (DV / 8) / NTH;   // 2 or 1
+      uint4 raw[kPer];
+#pragma unroll
+      for (int e2 = 0; e2 < kPer; ++e2) {
+        const int idx = tid + e2 * NTH;
+        const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
+        raw[e2] = r < pos.len ? *reinterpret_cast<const uint4*>(v + ((pos.t0 + r) * H + h) * DV + c8)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int e2 = 0; e2 < kPer; ++e2) {
+        const int idx = tid + e2 * NTH;
+        const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
+        const bf16* x = reinterpret_cast<const bf16*>(&raw[e2]);
+        const float br = sBeta[r];
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[e] = pack_f16x2(br * __bfloat162float(x[2 * e]), br * __bfloat162float(x[2 * e + 1]));
+        *reinterpret_cast<uint4*>(sKV + r * LDKV + DK + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
-  }
-  for (int idx = tid; idx < 6 * 256; idx += kPrepTcThreads) {   // zeros above the block diagonal of A
-    const int blk = idx >> 8, e = idx & 255;
-    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-    sA[(16 * a + (e >> 4)) * LDA + 16 * b + (e & 15)] = 0.f;
-  }
-  for (int idx = tid; idx < C * LDA; idx += kPrepTcThreads) sX[idx] = 0.f;
-  __syncthreads();
+    __syncthreads();
 
-  // 6. X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one
-  //    column per thread, then X_ab = -X_aa sum_{b<=m<a} A_am X_mb.
-  if (tid < C) {   // thread -> column j of diagonal block tid/16, kept in registers
-    const int base = (tid / kSub) * kSub, j = tid % kSub;
-    float xc[kSub];
+    // 5. A and P, one 16x16 block (row block a, column block b <= a) per job;
+    //    a P block (split operands) costs three MMAs per K step, an A block one.
+    float acc[2][2][4];
 #pragma unroll
-    for (int r = 0; r < kSub; ++r) {
-      float accx = (r == j) ? 1.f : 0.f;
+    for (int jb = 0; jb < 2; ++jb)
 #pragma unroll
-      for (int i = 0; i < r; ++i) accx -= sA[(base + r) * LDA + base + i] * xc[i];
-      xc[r] = r < j ? 0.f : accx;
+      for (int nt = 0; nt < 2; ++nt) acc[jb][nt][0] = acc[jb][nt][1] = acc[jb][nt][2] = acc[jb][nt][3] = 0.f;
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {
+      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
+      if (kind == 0) continue;
+      const bool isP = kind == 2;
+      const bf16* rowop = (isP ? sQE : sKE) + (16 * a) * LDB;
+      const bf16* rowlo = sQEl + (16 * a) * LDB;
+      const bf16* colop = sCop + (cop_row0(a) + 16 * b) * LDB;
+      const bf16* collo = sCopl + (cop_row0(a) + 16 * b) * LDB;
+#pragma unroll
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        const int aoff = (lane & 15) * LDB + ks * 16 + (lane >> 4) * 8;
+        const int boff = ((lane & 7) + (lane >> 4) * 8) * LDB + ks * 16 + ((lane >> 3) & 1) * 8;
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(tc::smem_u32(rowop + aoff), a0, a1, a2, a3);
+        ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
+        mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
+        mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
+        if (isP) {
+          uint32_t l0, l1, l2, l3;
+          ldsm_x4(tc::smem_u32(rowlo + aoff), l0, l1, l2, l3);
+          mma16816(acc[jb][0], l0, l1, l2, l3, b0, b1);
+          mma16816(acc[jb][1], l0, l1, l2, l3, b2, b3);
+          ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
+          mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
+          mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
+        }
+      }
     }
 #pragma unroll
-    for (int r = 0; r < kSub; ++r) sX[(base + r) * LDA + base + j] = xc[r];
-  }
-  __syncthreads();
-  {  // off-diagonal blocks, one element (row rr, column cc of the block) per thread
-    const int rr = tid >> 4, cc = tid & 15;
+    for (int jb = 0; jb < 2; ++jb) {   // P blocks straight to the record (inclusive lower triangle)
+      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
+      if (kind != 2) continue;
 #pragma unroll
-    for (int ab = 1; ab < C / kSub; ++ab) {
+      for (int nt = 0; nt < 2; ++nt) {
+        const int i0 = 16 * b + 8 * nt + 2 * tq;
 #pragma unroll
-      for (int b = 0; b < ab; ++b) {   // Y_b = sum_{b <= m < ab} A_{ab,m} X_{m,b}
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-        for (int m = b * kSub; m < ab * kSub; m += 4) {
-          const float* arow = sA + (ab * kSub + rr) * LDA + m;
-          p0 += arow[0] * sX[(m + 0) * LDA + b * kSub + cc];
-          p1 += arow[1] * sX[(m + 1) * LDA + b * kSub + cc];
-          p2 += arow[2] * sX[(m + 2) * LDA + b * kSub + cc];
-          p3 += arow[3] * sX[(m + 3) * LDA + b * kSub + cc];
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = 16 * a + gq + 8 * hr;
+          const float v0 = i0 <= r ? acc[jb][nt][2 * hr] : 0.f;
+          const float v1 = i0 + 1 <= r ? acc[jb][nt][2 * hr + 1] : 0.f;
+          *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(v0, v1);
         }
-        sY[(b * kSub + rr) * kSub + cc] = (p0 + p1) + (p2 + p3);
       }
-      __syncthreads();
-#pragma unroll
-      for (int b = 0; b < ab; ++b) {   // X_{ab,b} = -X_{ab,ab} Y_b (X_{ab,ab} is zero above its diagonal)
-        float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-        for (int t = 0; t < kSub; t += 2) {
-          p0 += sX[(ab * kSub + rr) * LDA + ab * kSub + t] * sY[(b * kSub + t) * kSub + cc];
-          p1 += sX[(ab * kSub + rr) * LDA + ab * kSub + t + 1] * sY[(b * kSub + t + 1) * kSub + cc];
-        }
-        sX[(ab * kSub + rr) * LDA + b * kSub + cc] = -(p0 + p1);
-      }
-      __syncthreads();
     }
-  }
-  for (int idx = tid; idx < C * C; idx += kPrepTcThreads) {
-    const int r = idx / C, i = idx % C;
-    sXb[r * LDX + i] = __float2half_rn(sX[r * LDA + i]);
-  }
-  __syncthreads();
+    for (int idx = tid; idx < 6 * 128; idx += NTH) {   // the 6 blocks of P above the block diagonal, as pairs
+      const int blk = idx >> 7, e = idx & 127;
+      const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      *reinterpret_cast<uint32_t*>(o_p + (16 * a + (e >> 3)) * C + 16 * b + (e & 7) * 2) = 0u;
+    }
+    __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
+#pragma unroll
+    for (int jb = 0; jb < 2; ++jb) {   // A = beta_r * (strictly lower part)
+      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
+      if (kind != 1) continue;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int i0 = 16 * b + 8 * nt + 2 * tq;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = 16 * a + gq + 8 * hr;
+          const float br = sBeta[r];
+          sA[r * LDA + i0] = i0 < r ? br * acc[jb][nt][2 * hr] : 0.f;
+          sA[r * LDA + i0 + 1] = i0 + 1 < r ? br * acc[jb][nt][2 * hr + 1] : 0.f;
+        }
+      }
+    }
+    for (int idx = tid; idx < 6 * 256; idx += NTH) {   // zeros above the block diagonal of A
+      const int blk = idx >> 8, e = idx & 255;
+      const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      sA[(16 * a + (e >> 4)) * LDA + 16 * b + (e & 15)] = 0.f;
+    }
+    for (int idx = tid; idx < C * LDA; idx += NTH) sX[idx] = 0.f;
+    __syncthreads();
 
-  // 7. [w | u] = X [beta k e^G | beta V]: warp -> 16 rows (mt) x half of the columns.
-  {
-    constexpr int NH = (DK + DV) / 2;     // columns per warp: 128 or 96
-    constexpr int NT = NH / 8;
-    const int mt = warp & 3, nh = warp >> 2;
-    float accw[NT][4];
+    // 6. X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one
+    //    column per thread in registers, then X_ab = -X_aa sum_{b<=m<a} A_am X_mb.
+    if (tid < C) {
+      const int base = (tid / kSub) * kSub, jc = tid % kSub;
+      float xc[kSub];
 #pragma unroll
-    for (int i = 0; i < NT; ++i) accw[i][0] = accw[i][1] = accw[i][2] = accw[i][3] = 0.f;
+      for (int r = 0; r < kSub; ++r) {
+        float accx = (r == jc) ? 1.f : 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      if (ks <= mt) {   // X is lower triangular by 16-row blocks
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(tc::smem_u32(sXb + (16 * mt + (lane & 15)) * LDX + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+        for (int i = 0; i < r; ++i) accx -= sA[(base + r) * LDA + base + i] * xc[i];
+        xc[r] = r < jc ? 0.f : accx;
+      }
 #pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          const int n0 = nh * NH + 16 * np;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(tc::smem_u32(sKV + (16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8) * LDKV + n0 + (lane >> 4) * 8),
-                    b0, b1, b2, b3);
-          mma16816_f16(accw[2 * np], a0, a1, a2, a3, b0, b1);
-          mma16816_f16(accw[2 * np + 1], a0, a1, a2, a3, b2, b3);
+      for (int r = 0; r < kSub; ++r) sX[(base + r) * LDA + base + jc] = xc[r];
+    }
+    __syncthreads();
+    {
+      const int rr = (tid >> 4) & 15, cc = tid & 15;
+      const bool act = tid < 256;
+#pragma unroll
+      for (int ab = 1; ab < C / kSub; ++ab) {
+        if (act) {
+#pragma unroll
+          for (int b = 0; b < ab; ++b) {   // Y_b = sum_{b <= m < ab} A_{ab,m} X_{m,b}
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int m = b * kSub; m < ab * kSub; m += 4) {
+              const float* arow = sA + (ab * kSub + rr) * LDA + m;
+              p0 += arow[0] * sX[(m + 0) * LDA + b * kSub + cc];
+              p1 += arow[1] * sX[(m + 1) * LDA + b * kSub + cc];
+              p2 += arow[2] * sX[(m + 2) * LDA + b * kSub + cc];
+              p3 += arow[3] * sX[(m + 3) * LDA + b * kSub + cc];
+            }
+            sY[(b * kSub + rr) * kSub + cc] = (p0 + p1) + (p2 + p3);
+          }
+        }
+        __syncthreads();
+        if (act) {
+#pragma unroll
+          for (int b = 0; b < ab; ++b) {   // X_{ab,b} = -X_{ab,ab} Y_b
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int t = 0; t < kSub; t += 2) {
+              p0 += sX[(ab * kSub + rr) * LDA + ab * kSub + t] * sY[(b * kSub + t) * kSub + cc];
+              p1 += sX[(ab * kSub + rr) * LDA + ab * kSub + t + 1] * sY[(b * kSub + t + 1) * kSub + cc];
+            }
+            sX[(ab * kSub + rr) * LDA + b * kSub + cc] = -(p0 + p1);
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int idx = tid; idx < C * C; idx += NTH) {
+      const int r = idx / C, i = idx % C;
+      sXb[r * LDX + i] = __float2half_rn(sX[r * LDA + i]);
+    }
+    __syncthreads();
+
+    // 7. [w | u] = X [beta k e^G | beta V]: warp -> 16 rows (mt) x a quarter of the columns
+    {
+      constexpr int NQ = (DK + DV) / 4;   // 64 or 48 columns per warp
+      constexpr int NT = NQ / 8;
+      const int mt = warp & 3, nq = warp >> 2;
+      float accw[NT][4];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) accw[i][0] = accw[i][1] = accw[i][2] = accw[i][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (ks <= mt) {   // X is lower triangular by 16-row blocks
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(tc::smem_u32(sXb + (16 * mt + (lane & 15)) * LDX + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+#pragma unroll
+          for (int np = 0; np < NT / 2; ++np) {
+            const int n0 = nq * NQ + 16 * np;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(tc::smem_u32(sKV + (16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8) * LDKV + n0 + (lane >> 4) * 8),
+                      b0, b1, b2, b3);
+            mma16816_f16(accw[2 * np], a0, a1, a2, a3, b0, b1);
+            mma16816_f16(accw[2 * np + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = nq * NQ + 8 * nt + 2 * tq;
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = 16 * mt + gq + 8 * hr;
+          const uint32_t pv = pack_f16x2(accw[nt][2 * hr], accw[nt][2 * hr + 1]);
+          if (n < DK)
+            *reinterpret_cast<uint32_t*>(o_wq + r * DK + n) = pv;
+          else
+            *reinterpret_cast<uint32_t*>(o_u + r * DV + (n - DK)) = pv;
         }
       }
     }
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = nh * NH + 8 * nt + 2 * tq;
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = 16 * mt + gq + 8 * hr;
-        const uint32_t pv = pack_f16x2(accw[nt][2 * hr], accw[nt][2 * hr + 1]);
-        if (n < DK)
-          *reinterpret_cast<uint32_t*>(o_wq + r * DK + n) = pv;
-        else
-          *reinterpret_cast<uint32_t*>(o_u + r * DV + (n - DK)) = pv;
-      }
-    }
+    __syncthreads();   // shared memory is reused by the next task
   }
 }
 
@@ -803,10 +826,15 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const size_t smem = PrepTcSmem<DV>::kBytes;
     e = cudaFuncSetAttribute(chunk_prep_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
+    const int grid = (int)std::min<int64_t>(n_tasks, sms);
     prof_begin(stream, "chunk_prep_tc");
-    chunk_prep_tc<DV><<<dim3(ws.max_chunks, p.H), kPrepTcThreads, smem, stream>>>(
+    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(
         static_cast<const bf16*>(p.q), static_cast<const bf16*>(p.k), static_cast<const bf16*>(p.v),
-        static_cast<const bf16*>(p.g), p.beta, p.cu, p.num_seqs, p.T_seq, p.H, map, rec);
+        static_cast<const bf16*>(p.g), p.beta, p.cu, p.num_seqs, p.T_seq, p.H, map, rec, n_tasks);
     prof_end(stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
