@@ -92,6 +92,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
 // (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
 __device__ __forceinline__ float fast_log_decay(float x) { return -5.f * __frcp_rn(1.f + __expf(-x)); }
@@ -132,10 +140,14 @@ struct PrepTcSmem {
   static constexpr size_t kBytes = oBeta + (size_t)C * 4;
   // reused once A and P are in registers
   static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]
-  static constexpr size_t oX = oA + (size_t)C * LDA * 4;              // fp32 [64][LDA]
-  static constexpr size_t oY = oX + (size_t)C * LDA * 4;              // fp32 [3][16][16]
-  static constexpr size_t oXb = oY + (size_t)3 * kSub * kSub * 4;     // fp16 [64][LDX]
-  static_assert(oXb + (size_t)C * LDX * 2 <= oKV, "aliases fit in the operand area");
+  static constexpr size_t oXb = oA + (size_t)C * LDA * 4;             // fp16 [64][LDX]  X
+  static constexpr size_t oAh = oXb + (size_t)C * LDX * 2;           // fp16 [64][LDX] copy of A
+  static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
+  // the next task's raw inputs (bf16 [64][d]: g, k, q, v), staged while this task finishes
+  static constexpr size_t oRaw = (oYh + 3 * 16 * 24 * 2 + 1023) / 1024 * 1024;
+  static constexpr size_t oRawK = oRaw + (size_t)C * DK * 2, oRawQ = oRawK + (size_t)C * DK * 2,
+                          oRawV = oRawQ + (size_t)C * DK * 2;
+  static_assert(oRawV + (size_t)C * DV * 2 <= oKV, "aliases fit in the operand area");
   static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
                     (oXb % 16) == 0,
                 "ldmatrix alignment");
@@ -177,18 +189,58 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   float* fOm = fPsi + 4 * DK;                                // [4][4][DK] e^{G_s(a) - G_s(b)}, b <= a
   float* sBeta = reinterpret_cast<float*>(smem + L::oBeta);
   float* sA = reinterpret_cast<float*>(smem + L::oA);
-  float* sX = reinterpret_cast<float*>(smem + L::oX);
-  float* sY = reinterpret_cast<float*>(smem + L::oY);
   f16* sXb = reinterpret_cast<f16*>(smem + L::oXb);
+  f16* sAh = reinterpret_cast<f16*>(smem + L::oAh);
+  f16* sYh = reinterpret_cast<f16*>(smem + L::oYh);
+  const bf16* rawG = reinterpret_cast<const bf16*>(smem + L::oRaw);
+  const bf16* rawK = reinterpret_cast<const bf16*>(smem + L::oRawK);
+  const bf16* rawQ = reinterpret_cast<const bf16*>(smem + L::oRawQ);
+  const bf16* rawV = reinterpret_cast<const bf16*>(smem + L::oRawV);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
+
+  // Start copying a task's raw g, k, q, v rows into the staging area (rows past
+  // the sequence end are zero-filled).  Uniform across the CTA.
+  auto stage_inputs = [&](int64_t t) {
+    ChunkPos np;
+    if (t >= n_tasks || !locate_chunk(map, cu, num_seqs, T_seq, (int32_t)(t / H), np)) return;
+    const int hn = (int)(t % H);
+    constexpr int kRow = DK / 8, kRowV = DV / 8;   // 16-byte chunks per row
+    for (int idx = tid; idx < 3 * C * kRow + C * kRowV; idx += NTH) {
+      const bf16* base;
+      int r, c8, d;
+      size_t dst;
+      if (idx < 3 * C * kRow) {
+        const int tsel = idx / (C * kRow), x = idx % (C * kRow);
+        r = x / kRow;
+        c8 = (x % kRow) * 8;
+        d = DK;
+        base = tsel == 0 ? g : (tsel == 1 ? k : q);
+        dst = L::oRaw + (size_t)tsel * C * DK * 2 + (size_t)(r * DK + c8) * 2;
+      } else {
+        const int x = idx - 3 * C * kRow;
+        r = x / kRowV;
+        c8 = (x % kRowV) * 8;
+        d = DV;
+        base = v;
+        dst = L::oRawV + (size_t)(r * DV + c8) * 2;
+      }
+      const bool ok = r < np.len;
+      cp_async16(smem + dst, ok ? base + ((np.t0 + r) * H + hn) * d + c8 : base, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  stage_inputs(blockIdx.x);
 
   // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
     const int32_t j = (int32_t)(task / H);
     const int h = (int)(task % H);
     ChunkPos pos;
-    if (!locate_chunk(map, cu, num_seqs, T_seq, j, pos)) continue;
+    if (!locate_chunk(map, cu, num_seqs, T_seq, j, pos)) {
+      stage_inputs(task + gridDim.x);
+      continue;
+    }
     const int64_t rec = task;   // == j * H + h
     f16* o_wq = out.wq + rec * 128 * DK;
     f16* o_p = out.p + rec * C * C;
@@ -196,21 +248,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     f16* o_u = out.u + rec * C * DV;
     float* o_gam = out.gam + rec * DK;
 
-    {  // pull this CTA's next task's input rows into L2 (one 128-byte line per thread)
-      const int64_t nt = task + gridDim.x;
-      ChunkPos np;
-      if (nt < n_tasks && locate_chunk(map, cu, num_seqs, T_seq, (int32_t)(nt / H), np)) {
-        const int tensor = tid >> 7, r = (tid & 127) >> 1, half = tid & 1;
-        const int d = tensor == 3 ? DV : DK;
-        if (r < np.len && half * 64 < d) {
-          const bf16* base = tensor == 0 ? g : (tensor == 1 ? k : (tensor == 2 ? q : v));
-          const bf16* p = base + ((np.t0 + r) * H + (int)(nt % H)) * d + half * 64;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-        }
-      }
-    }
-
     // 1. log-decay of every (row, channel); rows past the sequence end decay by 0
+    cp_async_wait_all();   // this task's raw rows, staged during the previous task
+    __syncthreads();
     {
       constexpr int kPer = C * (DK / 8) / NTH;   // 2
       uint4 raw[kPer];
@@ -218,8 +258,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       for (int e2 = 0; e2 < kPer; ++e2) {
         const int idx = tid + e2 * NTH;
         const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-        raw[e2] = r < pos.len ? *reinterpret_cast<const uint4*>(g + ((pos.t0 + r) * H + h) * DK + c8)
-                              : make_uint4(0u, 0u, 0u, 0u);
+        raw[e2] = *reinterpret_cast<const uint4*>(rawG + r * DK + c8);
       }
 #pragma unroll
       for (int e2 = 0; e2 < kPer; ++e2) {
@@ -292,15 +331,18 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       __nv_bfloat162 kq[8], qq[8];
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        const int r = r0 + rr;
-        kq[rr] = __floats2bfloat162_rn(0.f, 0.f);
-        qq[rr] = kq[rr];
-        if (r < pos.len) {
-          const int64_t off = ((pos.t0 + r) * H + h) * DK + c;
-          kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(k + off);
-          qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(q + off);
-        }
+        kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawK + (r0 + rr) * DK + c);
+        qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawQ + (r0 + rr) * DK + c);
       }
+      // the staged raw v rows of this thread, before any operand write reuses the area
+      constexpr int kPerV = C * (DV / 8) / NTH;   // 2 or 1
+      uint4 vraw[kPerV];
+#pragma unroll
+      for (int e2 = 0; e2 < kPerV; ++e2) {
+        const int idx = tid + e2 * NTH;
+        vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
+      }
+      __syncthreads();
       uint32_t kt0[4], kt1[4];   // K~^T rows c and c+1, tokens r0..r0+7, fp16 pairs
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
@@ -339,22 +381,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       }
       *reinterpret_cast<uint4*>(o_kt + c * C + r0) = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
       *reinterpret_cast<uint4*>(o_kt + (c + 1) * C + r0) = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
-    }
-    {  // beta V, loads first (16-byte vectors)
-      constexpr int kPer = C * (DV / 8) / NTH;   // 2 or 1
-      uint4 raw[kPer];
 #pragma unroll
-      for (int e2 = 0; e2 < kPer; ++e2) {
+      for (int e2 = 0; e2 < kPerV; ++e2) {   // beta V (rows past the end were staged as zeros)
         const int idx = tid + e2 * NTH;
         const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
-        raw[e2] = r < pos.len ? *reinterpret_cast<const uint4*>(v + ((pos.t0 + r) * H + h) * DV + c8)
-                              : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int e2 = 0; e2 < kPer; ++e2) {
-        const int idx = tid + e2 * NTH;
-        const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
-        const bf16* x = reinterpret_cast<const bf16*>(&raw[e2]);
+        const bf16* x = reinterpret_cast<const bf16*>(&vraw[e2]);
         const float br = sBeta[r];
         uint32_t pk[4];
 #pragma unroll
@@ -445,11 +476,17 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
       sA[(16 * a + (e >> 4)) * LDA + 16 * b + (e & 15)] = 0.f;
     }
-    for (int idx = tid; idx < C * LDA; idx += NTH) sX[idx] = 0.f;
     __syncthreads();
+    stage_inputs(task + gridDim.x);   // the operand area is free until the next task: stage its inputs
 
-    // 6. X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one
-    //    column per thread in registers, then X_ab = -X_aa sum_{b<=m<a} A_am X_mb.
+    // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
+    //    diagonal 16x16 blocks by forward substitution in fp32, one column per
+    //    thread in registers; then, block-row after block-row, on tensor cores,
+    //    Y_b = sum_{b<=m<a} A_am X_mb and X_ab = -X_aa Y_b.
+    for (int idx = tid; idx < C * C; idx += NTH) {   // fp16 copy of A for the products
+      const int r = idx / C, i = idx % C;
+      sAh[r * LDX + i] = __float2half_rn(sA[r * LDA + i]);
+    }
     if (tid < C) {
       const int base = (tid / kSub) * kSub, jc = tid % kSub;
       float xc[kSub];
@@ -461,50 +498,47 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         xc[r] = r < jc ? 0.f : accx;
       }
 #pragma unroll
-      for (int r = 0; r < kSub; ++r) sX[(base + r) * LDA + base + jc] = xc[r];
+      for (int r = 0; r < kSub; ++r) sXb[(base + r) * LDX + base + jc] = __float2half_rn(xc[r]);
     }
     __syncthreads();
-    {
-      const int rr = (tid >> 4) & 15, cc = tid & 15;
-      const bool act = tid < 256;
 #pragma unroll
-      for (int ab = 1; ab < C / kSub; ++ab) {
-        if (act) {
-#pragma unroll
-          for (int b = 0; b < ab; ++b) {   // Y_b = sum_{b <= m < ab} A_{ab,m} X_{m,b}
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-            for (int m = b * kSub; m < ab * kSub; m += 4) {
-              const float* arow = sA + (ab * kSub + rr) * LDA + m;
-              p0 += arow[0] * sX[(m + 0) * LDA + b * kSub + cc];
-              p1 += arow[1] * sX[(m + 1) * LDA + b * kSub + cc];
-              p2 += arow[2] * sX[(m + 2) * LDA + b * kSub + cc];
-              p3 += arow[3] * sX[(m + 3) * LDA + b * kSub + cc];
-            }
-            sY[(b * kSub + rr) * kSub + cc] = (p0 + p1) + (p2 + p3);
-          }
+    for (int ab = 1; ab < C / kSub; ++ab) {
+      if (warp < ab) {   // warp b computes X_{ab, b}
+        const int b = warp;
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        for (int m = b; m < ab; ++m) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(tc::smem_u32(sAh + (16 * ab + (lane & 15)) * LDX + 16 * m + (lane >> 4) * 8), a0, a1, a2, a3);
+          ldsm_x4_t(tc::smem_u32(sXb + (16 * m + (lane & 7) + ((lane >> 3) & 1) * 8) * LDX + 16 * b + (lane >> 4) * 8),
+                    b0, b1, b2, b3);
+          mma16816_f16(y[0], a0, a1, a2, a3, b0, b1);
+          mma16816_f16(y[1], a0, a1, a2, a3, b2, b3);
         }
-        __syncthreads();
-        if (act) {
+        f16* yb = sYh + warp * 16 * 24;
 #pragma unroll
-          for (int b = 0; b < ab; ++b) {   // X_{ab,b} = -X_{ab,ab} Y_b
-            float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-            for (int t = 0; t < kSub; t += 2) {
-              p0 += sX[(ab * kSub + rr) * LDA + ab * kSub + t] * sY[(b * kSub + t) * kSub + cc];
-              p1 += sX[(ab * kSub + rr) * LDA + ab * kSub + t + 1] * sY[(b * kSub + t + 1) * kSub + cc];
-            }
-            sX[(ab * kSub + rr) * LDA + b * kSub + cc] = -(p0 + p1);
-          }
+        for (int nt = 0; nt < 2; ++nt) {
+          *reinterpret_cast<uint32_t*>(yb + gq * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][0], y[nt][1]);
+          *reinterpret_cast<uint32_t*>(yb + (gq + 8) * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][2], y[nt][3]);
         }
-        __syncthreads();
+        __syncwarp();
+        float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(tc::smem_u32(sXb + (16 * ab + (lane & 15)) * LDX + 16 * ab + (lane >> 4) * 8), a0, a1, a2, a3);
+          ldsm_x4_t(tc::smem_u32(yb + ((lane & 7) + ((lane >> 3) & 1) * 8) * 24 + (lane >> 4) * 8), b0, b1, b2, b3);
+          mma16816_f16(x[0], a0, a1, a2, a3, b0, b1);
+          mma16816_f16(x[1], a0, a1, a2, a3, b2, b3);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          *reinterpret_cast<uint32_t*>(sXb + (16 * ab + gq) * LDX + 16 * b + 8 * nt + 2 * tq) =
+              pack_f16x2(-x[nt][0], -x[nt][1]);
+          *reinterpret_cast<uint32_t*>(sXb + (16 * ab + gq + 8) * LDX + 16 * b + 8 * nt + 2 * tq) =
+              pack_f16x2(-x[nt][2], -x[nt][3]);
+        }
       }
+      __syncthreads();
     }
-    for (int idx = tid; idx < C * C; idx += NTH) {
-      const int r = idx / C, i = idx % C;
-      sXb[r * LDX + i] = __float2half_rn(sX[r * LDA + i]);
-    }
-    __syncthreads();
 
     // 7. [w | u] = X [beta k e^G | beta V]: warp -> 16 rows (mt) x a quarter of the columns
     {
@@ -546,6 +580,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     }
     __syncthreads();   // shared memory is reused by the next task
   }
+  cp_async_wait_all();
 }
 
 // -------------------------------------------------------------- chain kernel
