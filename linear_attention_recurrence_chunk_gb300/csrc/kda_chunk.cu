@@ -31,7 +31,7 @@ namespace kda {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restrict__ cu, int32_t num_seqs,
                                                          int64_t T_seq, int64_t total, int32_t* seq_chunk0,
-                                                         int32_t* chunk_seq, int32_t max_chunks,
+                                                         int4* chunk_info, int32_t max_chunks,
                                                          int32_t* dev_err) {
   __shared__ int32_t s_scan[1024];
   __shared__ int32_t s_carry;
@@ -69,15 +69,29 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restri
       __syncthreads();
     }
     const int32_t start = s_carry + s_scan[tid] - n;
-    if (s < num_seqs) {
-      seq_chunk0[s] = start;
-      for (int32_t c = 0; c < n && start + c < max_chunks; ++c) chunk_seq[start + c] = s;
-    }
+    if (s < num_seqs) seq_chunk0[s] = start;
     __syncthreads();
     if (tid == blockDim.x - 1) s_carry += s_scan[tid];
     __syncthreads();
   }
-  if (tid == 0) seq_chunk0[num_seqs] = min(s_carry, max_chunks);
+  const int32_t n_chunks = min(s_carry, max_chunks);
+  if (tid == 0) seq_chunk0[num_seqs] = n_chunks;
+  __syncthreads();
+  // Per chunk: its sequence (the last s with seq_chunk0[s] <= j, which skips
+  // empty sequences), row count and first token.
+  for (int32_t j = tid; j < n_chunks; j += blockDim.x) {
+    int32_t lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (seq_chunk0[mid] <= j) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t start = cu ? (int64_t)cu[lo] : (int64_t)lo * T_seq;
+    const int64_t end = cu ? (int64_t)cu[lo + 1] : start + T_seq;
+    const int64_t t0 = start + (int64_t)(j - seq_chunk0[lo]) * kChunk;
+    chunk_info[j] = make_int4(lo, (int32_t)min((int64_t)kChunk, end - t0), (int32_t)(uint32_t)(uint64_t)t0,
+                              (int32_t)(uint32_t)((uint64_t)t0 >> 32));
+  }
 }
 
 // Intermediate record of one (chunk, head) in the workspace (fp32 SIMT path).
@@ -402,8 +416,8 @@ Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t
   w.tc = tc_path_supported(d_k, d_v, dt);
   w.inter_bytes_per_chunk_head = w.tc ? tc_record_bytes(d_k, d_v) : sizeof(float) * inter_floats(d_k, d_v);
   w.off_seq_chunk0 = 0;
-  w.off_chunk_seq = align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
-  w.off_inter = w.off_chunk_seq + align256(sizeof(int32_t) * (size_t)std::max<int64_t>(max_chunks, 1));
+  w.off_chunk_info = align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
+  w.off_inter = w.off_chunk_info + align256(sizeof(int4) * (size_t)std::max<int64_t>(max_chunks, 1));
   const size_t R = (size_t)max_chunks * (size_t)H;
   if (w.tc) {
     w.off_wq = w.off_inter;
@@ -457,13 +471,13 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& p, const Workspace& ws, void* w
   char* base = static_cast<char*>(workspace);
   ChunkMap map;
   map.seq_chunk0 = reinterpret_cast<int32_t*>(base + ws.off_seq_chunk0);
-  map.chunk_seq = reinterpret_cast<int32_t*>(base + ws.off_chunk_seq);
+  map.chunk_info = reinterpret_cast<int4*>(base + ws.off_chunk_info);
   map.max_chunks = ws.max_chunks;
   float* inter = reinterpret_cast<float*>(base + ws.off_inter);
 
   prof_begin(stream, "chunk_map");
   chunk_map_kernel<<<1, 1024, 0, stream>>>(p.cu, p.num_seqs, p.T_seq, p.total_tokens, map.seq_chunk0,
-                                           map.chunk_seq, map.max_chunks, p.dev_err);
+                                           map.chunk_info, map.max_chunks, p.dev_err);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

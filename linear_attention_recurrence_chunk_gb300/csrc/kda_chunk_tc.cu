@@ -93,16 +93,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
 // (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
-__device__ __forceinline__ float fast_log_decay(float x) { return -5.f * __frcp_rn(1.f + __expf(-x)); }
+__device__ __forceinline__ float fast_log_decay(float x) { return __fdividef(-5.f, 1.f + __expf(-x)); }
 
 // bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -126,42 +125,47 @@ struct PrepTcSmem {
   static constexpr int LDB = DK + 8;          // 16-bit row stride of the 128-wide operands (272 B)
   static constexpr int LDKV = DK + DV + 8;    // fp16 row stride of [beta k e^G | beta V]
   static constexpr int LDX = C + 8;           // fp16 row stride of X
-  static constexpr int LDA = C + 1;           // fp32 row stride of A and X
+  static constexpr int LDA = C + 1;           // fp32 row stride of A's diagonal blocks
   static constexpr int kCopRows = 16 + 32 + 48 + 64;
-  static constexpr size_t oG = 0;                                    // fp32 [64][128]  cumulative log-decay
-  static constexpr size_t oKE = oG + (size_t)C * DK * 4;             // bf16 [64][LDB]  k e^{G - G_s}
+  // raw input rows of the next task (TMA, bf16 [64][d]), staged during this one
+  static constexpr size_t oRawG = 0;
+  static constexpr size_t oRawK = oRawG + (size_t)C * DK * 2;
+  static constexpr size_t oRawQ = oRawK + (size_t)C * DK * 2;
+  static constexpr size_t oRawV = oRawQ + (size_t)C * DK * 2;
+  static constexpr size_t oKE = (oRawV + (size_t)C * DV * 2 + 1023) / 1024 * 1024;  // bf16 [64][LDB] k e^{G - G_s}
   static constexpr size_t oQE = oKE + (size_t)C * LDB * 2;           // bf16 [64][LDB]  q e^{G - G_s}, high part
   static constexpr size_t oQEl = oQE + (size_t)C * LDB * 2;          // bf16 [64][LDB]  low part
   static constexpr size_t oCop = oQEl + (size_t)C * LDB * 2;         // bf16 [160][LDB] column operands, high part
-  static constexpr size_t oCopl = oCop + (size_t)kCopRows * LDB * 2; // bf16 [160][LDB] low part
-  static constexpr size_t oKV = oCopl + (size_t)kCopRows * LDB * 2;  // fp16 [64][LDKV]
-  static constexpr size_t oFac = oKV + (size_t)C * LDKV * 2;         // fp32 factors
-  static constexpr size_t oBeta = oFac + (size_t)(4 + 4 + 4 + 16) * DK * 4;
-  static constexpr size_t kBytes = oBeta + (size_t)C * 4;
+  static constexpr size_t oCopl = oCop + (size_t)kCopRows * LDB * 2; // bf16 [64][LDB] low part, diagonal blocks
+  static constexpr size_t oKV = oCopl + (size_t)C * LDB * 2;         // fp16 [64][LDKV]
+  static constexpr size_t oTot = oKV + (size_t)C * LDKV * 2;         // fp32 [8][DK] group sums; later P partials
+  static constexpr size_t oBeta = oTot + (size_t)8 * DK * 4;         // fp32 [64]
+  static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarrier of the raw rows
+  static constexpr size_t kBytes = oBar + 8;
+  static constexpr size_t kAlloc = kBytes + 1024;                    // slack to align the base to 1 KB
   // reused once A and P are in registers
-  static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]
+  static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]  A, diagonal blocks
   static constexpr size_t oXb = oA + (size_t)C * LDA * 4;             // fp16 [64][LDX]  X
-  static constexpr size_t oAh = oXb + (size_t)C * LDX * 2;           // fp16 [64][LDX] copy of A
+  static constexpr size_t oAh = oXb + (size_t)C * LDX * 2;           // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
-  // the next task's raw inputs (bf16 [64][d]: g, k, q, v), staged while this task finishes
-  static constexpr size_t oRaw = (oYh + 3 * 16 * 24 * 2 + 1023) / 1024 * 1024;
-  static constexpr size_t oRawK = oRaw + (size_t)C * DK * 2, oRawQ = oRawK + (size_t)C * DK * 2,
-                          oRawV = oRawQ + (size_t)C * DK * 2;
-  static_assert(oRawV + (size_t)C * DV * 2 <= oKV, "aliases fit in the operand area");
+  static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
   static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
-                    (oXb % 16) == 0,
-                "ldmatrix alignment");
-  static_assert(kBytes <= 232448, "fits the 227 KB shared-memory limit");
+                    (oXb % 16) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
+                "ldmatrix, mbarrier and TMA alignment");
+  static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
 };
 
-// A/P jobs per warp (16 warps): (kind, row block a, column block b), kind 1 = A,
-// 2 = P, 0 = none.  Warps 0-9 take one P block each (three MMAs per K step),
-// warps 10-15 share the ten A blocks (one MMA per K step).
+// A/P jobs per warp (16 warps): (kind, row block a, column block b).  Kinds:
+// 1 = A block (k e^{G-G_s} x column operand), 2 = P block below the diagonal
+// (q e^{G-G_s} x column operand, high parts), 3 = P diagonal block, high row
+// part x (high + low) column parts, 4 = the low row part x high column part of
+// the same diagonal block, handed to the kind-3 warp through shared memory;
+// 0 = none.  Every warp carries at most 32 MMAs.
 __constant__ int8_t kApJobs[16][2][3] = {
-    {{2, 3, 3}, {0, 0, 0}}, {{2, 3, 2}, {0, 0, 0}}, {{2, 3, 1}, {0, 0, 0}}, {{2, 3, 0}, {0, 0, 0}},
-    {{2, 2, 2}, {0, 0, 0}}, {{2, 2, 1}, {0, 0, 0}}, {{2, 2, 0}, {0, 0, 0}}, {{2, 1, 1}, {0, 0, 0}},
-    {{2, 1, 0}, {0, 0, 0}}, {{2, 0, 0}, {0, 0, 0}}, {{1, 3, 3}, {1, 3, 2}}, {{1, 3, 1}, {1, 3, 0}},
-    {{1, 2, 2}, {1, 2, 1}}, {{1, 2, 0}, {1, 1, 1}}, {{1, 1, 0}, {0, 0, 0}}, {{1, 0, 0}, {0, 0, 0}}};
+    {{3, 0, 0}, {0, 0, 0}}, {{3, 1, 1}, {0, 0, 0}}, {{3, 2, 2}, {0, 0, 0}}, {{3, 3, 3}, {0, 0, 0}},
+    {{4, 0, 0}, {1, 3, 3}}, {{4, 1, 1}, {1, 3, 2}}, {{4, 2, 2}, {1, 3, 1}}, {{4, 3, 3}, {1, 3, 0}},
+    {{2, 3, 2}, {1, 2, 2}}, {{2, 3, 1}, {1, 2, 1}}, {{2, 3, 0}, {1, 2, 0}}, {{2, 2, 1}, {1, 1, 1}},
+    {{2, 2, 0}, {0, 0, 0}}, {{2, 1, 0}, {0, 0, 0}}, {{1, 1, 0}, {0, 0, 0}}, {{1, 0, 0}, {0, 0, 0}}};
 
 // First row (in the column-operand area) of block-row a's column operand.
 __device__ __forceinline__ int cop_row0(int a) { return a == 0 ? 0 : (a == 1 ? 16 : (a == 2 ? 48 : 96)); }
@@ -169,78 +173,91 @@ __device__ __forceinline__ int cop_row0(int a) { return a == 0 ? 0 : (a == 1 ? 1
 
 template <int DV>
 __global__ void __launch_bounds__(kPrepTcThreads, 1)
-    chunk_prep_tc(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
-                  const bf16* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu,
-                  int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map, TcRecords out, int64_t n_tasks) {
+    chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+                  const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
+                  int64_t n_tasks, int32_t* __restrict__ dev_err) {
   using L = PrepTcSmem<DV>;
   constexpr int LDB = L::LDB, LDKV = L::LDKV, LDX = L::LDX, LDA = L::LDA;
   constexpr int NTH = kPrepTcThreads;
-  extern __shared__ __align__(16) uint8_t smem[];
-  float* sG = reinterpret_cast<float*>(smem + L::oG);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   bf16* sKE = reinterpret_cast<bf16*>(smem + L::oKE);
   bf16* sQE = reinterpret_cast<bf16*>(smem + L::oQE);
   bf16* sQEl = reinterpret_cast<bf16*>(smem + L::oQEl);
   bf16* sCop = reinterpret_cast<bf16*>(smem + L::oCop);
   bf16* sCopl = reinterpret_cast<bf16*>(smem + L::oCopl);
   f16* sKV = reinterpret_cast<f16*>(smem + L::oKV);
-  float* fGs = reinterpret_cast<float*>(smem + L::oFac);   // [4][DK] cumulative decay before block a
-  float* fLam = fGs + 4 * DK;                                // [4][DK] e^{G_s(a)}
-  float* fPsi = fLam + 4 * DK;                               // [4][DK] e^{G_last - G_s(a)}
-  float* fOm = fPsi + 4 * DK;                                // [4][4][DK] e^{G_s(a) - G_s(b)}, b <= a
+  float* sTot = reinterpret_cast<float*>(smem + L::oTot);
   float* sBeta = reinterpret_cast<float*>(smem + L::oBeta);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::oBar);
   float* sA = reinterpret_cast<float*>(smem + L::oA);
   f16* sXb = reinterpret_cast<f16*>(smem + L::oXb);
   f16* sAh = reinterpret_cast<f16*>(smem + L::oAh);
   f16* sYh = reinterpret_cast<f16*>(smem + L::oYh);
-  const bf16* rawG = reinterpret_cast<const bf16*>(smem + L::oRaw);
+  const bf16* rawG = reinterpret_cast<const bf16*>(smem + L::oRawG);
   const bf16* rawK = reinterpret_cast<const bf16*>(smem + L::oRawK);
   const bf16* rawQ = reinterpret_cast<const bf16*>(smem + L::oRawQ);
   const bf16* rawV = reinterpret_cast<const bf16*>(smem + L::oRawV);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
-  // Start copying a task's raw g, k, q, v rows into the staging area (rows past
-  // the sequence end are zero-filled).  Uniform across the CTA.
-  auto stage_inputs = [&](int64_t t) {
-    ChunkPos np;
-    if (t >= n_tasks || !locate_chunk(map, cu, num_seqs, T_seq, (int32_t)(t / H), np)) return;
-    const int hn = (int)(t % H);
-    constexpr int kRow = DK / 8, kRowV = DV / 8;   // 16-byte chunks per row
-    for (int idx = tid; idx < 3 * C * kRow + C * kRowV; idx += NTH) {
-      const bf16* base;
-      int r, c8, d;
-      size_t dst;
-      if (idx < 3 * C * kRow) {
-        const int tsel = idx / (C * kRow), x = idx % (C * kRow);
-        r = x / kRow;
-        c8 = (x % kRow) * 8;
-        d = DK;
-        base = tsel == 0 ? g : (tsel == 1 ? k : q);
-        dst = L::oRaw + (size_t)tsel * C * DK * 2 + (size_t)(r * DK + c8) * 2;
-      } else {
-        const int x = idx - 3 * C * kRow;
-        r = x / kRowV;
-        c8 = (x % kRowV) * 8;
-        d = DV;
-        base = v;
-        dst = L::oRawV + (size_t)(r * DV + c8) * 2;
-      }
-      const bool ok = r < np.len;
-      cp_async16(smem + dst, ok ? base + ((np.t0 + r) * H + hn) * d + c8 : base, ok ? 16u : 0u);
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&tmG);
+    tc::tma_prefetch_desc(&tmK);
+    tc::tma_prefetch_desc(&tmQ);
+    tc::tma_prefetch_desc(&tmV);
+  }
+  __syncthreads();
+
+  // Chunk records of this CTA's tasks: one 16-byte load, fetched a task ahead.
+  const int32_t n_chunks = map.seq_chunk0[num_seqs];   // negative after malformed cu_seqlens
+  auto fetch = [&](int64_t t) -> int4 {
+    return (t < n_tasks && t / H < n_chunks) ? map.chunk_info[t / H] : make_int4(0, 0, 0, 0);
+  };
+  // Staging of a task's raw rows: 64 tokens of one head of g, k, q, v by TMA
+  // (zero-filled past the token array; rows past the sequence end are masked
+  // by the gate and by beta = 0) and beta by cp.async.  The barrier is armed
+  // by thread 0 before the CTA barrier that precedes the four copies, which
+  // lanes 0 of warps 12-15 issue.
+  auto arm = [&](int4 ci) {
+    if (ci.y > 0 && tid == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)C * (3 * DK + DV) * 2);
+  };
+  auto issue = [&](int64_t t, int4 ci) {
+    if (ci.y <= 0 || warp < 12 || lane != 0) return;
+    const int which = warp - 12;
+    const CUtensorMap* m = which == 0 ? &tmG : (which == 1 ? &tmK : (which == 2 ? &tmQ : &tmV));
+    tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, (int32_t)(t % H), ci.z, bar);
+  };
+  auto stage_beta = [&](int64_t t, int4 ci) {
+    if (ci.y <= 0) return;
+    if (tid < C) {
+      const bool ok = tid < ci.y;
+      cp_async4(sBeta + tid, ok ? beta + ((int64_t)ci.z + tid) * H + t % H : beta, ok ? 4u : 0u);
     }
     cp_async_commit();
   };
-  stage_inputs(blockIdx.x);
+  int4 ci_next = fetch(blockIdx.x);
+  arm(ci_next);
+  __syncthreads();
+  issue(blockIdx.x, ci_next);
+  stage_beta(blockIdx.x, ci_next);
+  uint32_t parity = 0;
 
   // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
-    const int32_t j = (int32_t)(task / H);
-    const int h = (int)(task % H);
-    ChunkPos pos;
-    if (!locate_chunk(map, cu, num_seqs, T_seq, j, pos)) {
-      stage_inputs(task + gridDim.x);
+    const int4 ci = ci_next;
+    ci_next = fetch(task + gridDim.x);
+    if (ci.y <= 0) {
+      arm(ci_next);
+      __syncthreads();
+      issue(task + gridDim.x, ci_next);
+      stage_beta(task + gridDim.x, ci_next);
       continue;
     }
+    const int len = ci.y;
     const int64_t rec = task;   // == j * H + h
     f16* o_wq = out.wq + rec * 128 * DK;
     f16* o_p = out.p + rec * C * C;
@@ -248,108 +265,89 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     f16* o_u = out.u + rec * C * DV;
     float* o_gam = out.gam + rec * DK;
 
-    // 1. log-decay of every (row, channel); rows past the sequence end decay by 0
-    cp_async_wait_all();   // this task's raw rows, staged during the previous task
-    __syncthreads();
-    {
-      constexpr int kPer = C * (DK / 8) / NTH;   // 2
-      uint4 raw[kPer];
-#pragma unroll
-      for (int e2 = 0; e2 < kPer; ++e2) {
-        const int idx = tid + e2 * NTH;
-        const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-        raw[e2] = *reinterpret_cast<const uint4*>(rawG + r * DK + c8);
-      }
-#pragma unroll
-      for (int e2 = 0; e2 < kPer; ++e2) {
-        const int idx = tid + e2 * NTH;
-        const int r = idx / (DK / 8), c8 = (idx % (DK / 8)) * 8;
-        const bf16* x = reinterpret_cast<const bf16*>(&raw[e2]);
-        float lg[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) lg[e] = r < pos.len ? fast_log_decay(__bfloat162float(x[e])) : 0.f;
-        float4* dst = reinterpret_cast<float4*>(sG + r * DK + c8);
-        dst[0] = make_float4(lg[0], lg[1], lg[2], lg[3]);
-        dst[1] = make_float4(lg[4], lg[5], lg[6], lg[7]);
-      }
+    // 1. Thread -> channel pair (c, c+1) and the 8 rows r0..r0+7 of sub-tile a.
+    //    Gate and inclusive cumulative sum over the thread's rows, in registers;
+    //    the raw k, q, v of the thread are read before the area is reused.
+    const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2, r0 = 8 * rg;
+    cp_async_wait_all();   // beta
+    const bool ok = tc::mbar_wait(bar, parity, kWaitLimit);
+    if (__syncthreads_or(!ok)) {   // a staging copy never landed: report, drain, stop
+      if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      tc::mbar_wait(bar, parity, kWaitLimit);
+      return;
     }
-    if (tid < C) sBeta[tid] = tid < pos.len ? beta[(pos.t0 + tid) * H + h] : 0.f;
-    __syncthreads();
-
-    // 2. inclusive cumulative sum over the chunk's rows: four 16-row scans, then the fix-up
+    parity ^= 1u;
+    float2 G[8];
     {
-      const int c = tid & (DK - 1), qt = tid >> 7;
-      float run = 0.f;
-#pragma unroll
-      for (int r = 16 * qt; r < 16 * qt + 16; ++r) {
-        run += sG[r * DK + c];
-        sG[r * DK + c] = run;
-      }
-      __syncthreads();
-      float add = 0.f;
-      for (int q2 = 0; q2 < qt; ++q2) add += sG[(16 * q2 + 15) * DK + c];
-      __syncthreads();
-      if (qt > 0) {
-#pragma unroll
-        for (int r = 16 * qt; r < 16 * qt + 16; ++r) sG[r * DK + c] += add;
-      }
-    }
-    __syncthreads();
-
-    // 3. per (16-row block, channel) factors
-    if (tid < DK) {
-      const int c = tid;
-      const float gl = sG[(C - 1) * DK + c];
-      float gs[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        gs[a] = a ? sG[(16 * a - 1) * DK + c] : 0.f;
-        fGs[a * DK + c] = gs[a];
-        fLam[a * DK + c] = expf(gs[a]);
-        fPsi[a * DK + c] = expf(gl - gs[a]);
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b <= a; ++b) fOm[(a * 4 + b) * DK + c] = a == b ? 1.f : expf(gs[a] - gs[b]);
-      o_gam[c] = expf(gl);
-    }
-    __syncthreads();
-
-    // 4. elementwise operands.  Thread -> channel pair (c, c+1) and 8 rows of
-    //    block a; every 16-bit operand is stored as a 32-bit pair.
-    {
-      const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2;
-      const int r0 = 16 * a + 8 * (rg & 1);
-      const float2 gs = make_float2(fGs[a * DK + c], fGs[a * DK + c + 1]);
-      const float2 lam = make_float2(fLam[a * DK + c], fLam[a * DK + c + 1]);
-      const float2 psi = make_float2(fPsi[a * DK + c], fPsi[a * DK + c + 1]);
-      float2 om[4];
-#pragma unroll
-      for (int a2 = 0; a2 < 4; ++a2)
-        om[a2] = a2 >= a ? make_float2(fOm[(a2 * 4 + a) * DK + c], fOm[(a2 * 4 + a) * DK + c + 1]) : make_float2(0.f, 0.f);
-      __nv_bfloat162 kq[8], qq[8];
+      float2 run = make_float2(0.f, 0.f);
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
-        kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawK + (r0 + rr) * DK + c);
-        qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawQ + (r0 + rr) * DK + c);
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
+        if (r0 + rr < len) {
+          run.x += fast_log_decay(__low2float(x));
+          run.y += fast_log_decay(__high2float(x));
+        }
+        G[rr] = run;
       }
-      // the staged raw v rows of this thread, before any operand write reuses the area
-      constexpr int kPerV = C * (DV / 8) / NTH;   // 2 or 1
-      uint4 vraw[kPerV];
+      *reinterpret_cast<float2*>(sTot + rg * DK + c) = run;
+    }
+    __nv_bfloat162 kq[8], qq[8];
 #pragma unroll
-      for (int e2 = 0; e2 < kPerV; ++e2) {
-        const int idx = tid + e2 * NTH;
-        vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
+    for (int rr = 0; rr < 8; ++rr) {
+      kq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawK + (r0 + rr) * DK + c);
+      qq[rr] = *reinterpret_cast<const __nv_bfloat162*>(rawQ + (r0 + rr) * DK + c);
+    }
+    constexpr int kPerV = C * (DV / 8) / NTH;   // 2 or 1
+    uint4 vraw[kPerV];
+#pragma unroll
+    for (int e2 = 0; e2 < kPerV; ++e2) {
+      const int idx = tid + e2 * NTH;
+      vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
+    }
+    arm(ci_next);
+    __syncthreads();   // every raw read is done; the group sums are visible
+    issue(task + gridDim.x, ci_next);
+
+    // 2. Offsets from the group sums: G_s(a') = cumulative decay before sub-tile
+    //    a', G_last; then per-thread factors e^{G_s(a)}, e^{G_last - G_s(a)},
+    //    e^{G_s(a') - G_s(a)} for a' >= a.
+    float2 gsA[4], gl;
+    {
+      float2 acc = make_float2(0.f, 0.f), excl = acc;
+#pragma unroll
+      for (int r2 = 0; r2 < 8; ++r2) {
+        if ((r2 & 1) == 0) gsA[r2 >> 1] = acc;
+        if (r2 == rg) excl = acc;
+        const float2 t2 = *reinterpret_cast<const float2*>(sTot + r2 * DK + c);
+        acc.x += t2.x;
+        acc.y += t2.y;
       }
-      __syncthreads();
+      gl = acc;
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        G[rr].x += excl.x;
+        G[rr].y += excl.y;
+      }
+    }
+    const float2 gs = gsA[a];
+    const float2 lam = make_float2(__expf(gs.x), __expf(gs.y));
+    const float2 psi = make_float2(__expf(gl.x - gs.x), __expf(gl.y - gs.y));
+    float2 om[4];
+#pragma unroll
+    for (int a2 = 0; a2 < 4; ++a2)
+      om[a2] = a2 > a ? make_float2(__expf(gsA[a2].x - gs.x), __expf(gsA[a2].y - gs.y))
+                      : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
+    if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(__expf(gl.x), __expf(gl.y));
+
+    // 3. Elementwise operands; every 16-bit operand is stored as a 32-bit pair.
+    {
       uint32_t kt0[4], kt1[4];   // K~^T rows c and c+1, tokens r0..r0+7, fp16 pairs
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = r0 + rr;
-        const float2 gr = *reinterpret_cast<const float2*>(sG + r * DK + c);
+        const float2 gr = G[rr];
         const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
-        const float f0 = __frcp_rn(e0), f1 = __frcp_rn(e1);                 // e^{G_s - G_r} in [1, e^80)
+        const float f0 = __expf(gs.x - gr.x), f1 = __expf(gs.y - gr.y);   // e^{G_s - G_r} in [1, e^80)
         const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
         const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
         const float br = sBeta[r];
@@ -359,13 +357,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         *reinterpret_cast<uint32_t*>(sQE + r * LDB + c) = hi;
         *reinterpret_cast<uint32_t*>(sQEl + r * LDB + c) = lo;
         const float kf0 = k0 * f0, kf1 = k1 * f1;
+        split_bf16x2(kf0, kf1, hi, lo);   // own sub-tile: high and low parts
+        *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a) + r) * LDB + c) = hi;
+        *reinterpret_cast<uint32_t*>(sCopl + r * LDB + c) = lo;
 #pragma unroll
-        for (int a2 = 0; a2 < 4; ++a2) {
-          if (a2 >= a) {
-            split_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y, hi, lo);
-            *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = hi;
-            *reinterpret_cast<uint32_t*>(sCopl + (cop_row0(a2) + r) * LDB + c) = lo;
-          }
+        for (int a2 = 1; a2 < 4; ++a2) {   // later sub-tiles: factors <= 1, high part only
+          if (a2 > a)
+            *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
         }
         *reinterpret_cast<uint32_t*>(sKV + r * LDKV + c) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
         *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
@@ -382,7 +380,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       *reinterpret_cast<uint4*>(o_kt + c * C + r0) = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
       *reinterpret_cast<uint4*>(o_kt + (c + 1) * C + r0) = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
 #pragma unroll
-      for (int e2 = 0; e2 < kPerV; ++e2) {   // beta V (rows past the end were staged as zeros)
+      for (int e2 = 0; e2 < kPerV; ++e2) {   // beta V (beta is 0 on rows past the sequence end)
         const int idx = tid + e2 * NTH;
         const int r = idx / (DV / 8), c8 = (idx % (DV / 8)) * 8;
         const bf16* x = reinterpret_cast<const bf16*>(&vraw[e2]);
@@ -395,8 +393,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     }
     __syncthreads();
 
-    // 5. A and P, one 16x16 block (row block a, column block b <= a) per job;
-    //    a P block (split operands) costs three MMAs per K step, an A block one.
+    // 5. A and P, one 16x16 block (row block a, column block b <= a) per job.
     float acc[2][2][4];
 #pragma unroll
     for (int jb = 0; jb < 2; ++jb)
@@ -406,11 +403,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     for (int jb = 0; jb < 2; ++jb) {
       const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
       if (kind == 0) continue;
-      const bool isP = kind == 2;
-      const bf16* rowop = (isP ? sQE : sKE) + (16 * a) * LDB;
-      const bf16* rowlo = sQEl + (16 * a) * LDB;
+      const bf16* rowop = (kind == 1 ? sKE : (kind == 4 ? sQEl : sQE)) + (16 * a) * LDB;
       const bf16* colop = sCop + (cop_row0(a) + 16 * b) * LDB;
-      const bf16* collo = sCopl + (cop_row0(a) + 16 * b) * LDB;
+      const bf16* collo = sCopl + (16 * a) * LDB;
 #pragma unroll
       for (int ks = 0; ks < DK / 16; ++ks) {
         const int aoff = (lane & 15) * LDB + ks * 16 + (lane >> 4) * 8;
@@ -420,20 +415,23 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
         mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
         mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
-        if (isP) {
-          uint32_t l0, l1, l2, l3;
-          ldsm_x4(tc::smem_u32(rowlo + aoff), l0, l1, l2, l3);
-          mma16816(acc[jb][0], l0, l1, l2, l3, b0, b1);
-          mma16816(acc[jb][1], l0, l1, l2, l3, b2, b3);
+        if (kind == 3) {
           ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
           mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
           mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
+    float* sPart = sTot;   // [4][2][4][32] low-part partials of the diagonal P blocks
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {   // P blocks straight to the record (inclusive lower triangle)
+    for (int jb = 0; jb < 2; ++jb) {   // P blocks below the diagonal to the record; diagonal partials to SMEM
       const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
+      if (kind == 4) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sPart[((a * 2 + nt) * 4 + e) * 32 + lane] = acc[jb][nt][e];
+      }
       if (kind != 2) continue;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -441,9 +439,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = 16 * a + gq + 8 * hr;
-          const float v0 = i0 <= r ? acc[jb][nt][2 * hr] : 0.f;
-          const float v1 = i0 + 1 <= r ? acc[jb][nt][2 * hr + 1] : 0.f;
-          *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(v0, v1);
+          *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(acc[jb][nt][2 * hr], acc[jb][nt][2 * hr + 1]);
         }
       }
     }
@@ -455,38 +451,47 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     }
     __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {   // A = beta_r * (strictly lower part)
+    for (int jb = 0; jb < 2; ++jb) {
       const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
+      if (kind == 3) {   // diagonal P block: add the low-part partial, keep the inclusive lower triangle
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int i0 = 16 * b + 8 * nt + 2 * tq;
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = 16 * a + gq + 8 * hr;
+            const float v0 = acc[jb][nt][2 * hr] + sPart[((a * 2 + nt) * 4 + 2 * hr) * 32 + lane];
+            const float v1 = acc[jb][nt][2 * hr + 1] + sPart[((a * 2 + nt) * 4 + 2 * hr + 1) * 32 + lane];
+            *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
+          }
+        }
+      }
       if (kind != 1) continue;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {   // A = beta_r * (strictly lower part): diagonal blocks fp32, the rest fp16
         const int i0 = 16 * b + 8 * nt + 2 * tq;
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = 16 * a + gq + 8 * hr;
           const float br = sBeta[r];
-          sA[r * LDA + i0] = i0 < r ? br * acc[jb][nt][2 * hr] : 0.f;
-          sA[r * LDA + i0 + 1] = i0 + 1 < r ? br * acc[jb][nt][2 * hr + 1] : 0.f;
+          if (a == b) {
+            sA[r * LDA + i0] = br * acc[jb][nt][2 * hr];
+            sA[r * LDA + i0 + 1] = br * acc[jb][nt][2 * hr + 1];
+          } else {
+            *reinterpret_cast<uint32_t*>(sAh + r * LDX + i0) =
+                pack_f16x2(br * acc[jb][nt][2 * hr], br * acc[jb][nt][2 * hr + 1]);
+          }
         }
       }
     }
-    for (int idx = tid; idx < 6 * 256; idx += NTH) {   // zeros above the block diagonal of A
-      const int blk = idx >> 8, e = idx & 255;
-      const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      sA[(16 * a + (e >> 4)) * LDA + 16 * b + (e & 15)] = 0.f;
-    }
     __syncthreads();
-    stage_inputs(task + gridDim.x);   // the operand area is free until the next task: stage its inputs
+    stage_beta(task + gridDim.x, ci_next);   // beta is no longer read by this task
 
     // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
-    //    diagonal 16x16 blocks by forward substitution in fp32, one column per
-    //    thread in registers; then, block-row after block-row, on tensor cores,
+    //    diagonal 16x16 blocks (only their strictly lower parts are read) by
+    //    forward substitution in fp32, one column per thread in registers;
+    //    then, block-row after block-row, on tensor cores,
     //    Y_b = sum_{b<=m<a} A_am X_mb and X_ab = -X_aa Y_b.
-    for (int idx = tid; idx < C * C; idx += NTH) {   // fp16 copy of A for the products
-      const int r = idx / C, i = idx % C;
-      sAh[r * LDX + i] = __float2half_rn(sA[r * LDA + i]);
-    }
     if (tid < C) {
       const int base = (tid / kSub) * kSub, jc = tid % kSub;
       float xc[kSub];
@@ -846,6 +851,20 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, void* base, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D tensor map over a token-major [tokens][H][inner] bf16 input, one box =
+// 64 tokens of one head.
+bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H, uint64_t tokens) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, H, tokens};
+  const cuuint64_t strides[2] = {inner * 2, H * inner * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)C};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DV>
 cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap& map, char* base,
                       cudaStream_t stream) {
@@ -858,7 +877,12 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   const uint64_t R = (uint64_t)ws.max_chunks * (uint64_t)p.H;
   cudaError_t e;
   if (ws.max_chunks > 0 && p.total_tokens > 0) {
-    const size_t smem = PrepTcSmem<DV>::kBytes;
+    CUtensorMap mG, mK, mQ, mV;
+    const uint64_t tok = (uint64_t)p.total_tokens;
+    if (!make_input_map(&mG, p.g, DK, p.H, tok) || !make_input_map(&mK, p.k, DK, p.H, tok) ||
+        !make_input_map(&mQ, p.q, DK, p.H, tok) || !make_input_map(&mV, p.v, DV, p.H, tok))
+      return cudaErrorInvalidValue;
+    const size_t smem = PrepTcSmem<DV>::kAlloc;
     e = cudaFuncSetAttribute(chunk_prep_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -867,9 +891,8 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
     const int grid = (int)std::min<int64_t>(n_tasks, sms);
     prof_begin(stream, "chunk_prep_tc");
-    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(
-        static_cast<const bf16*>(p.q), static_cast<const bf16*>(p.k), static_cast<const bf16*>(p.v),
-        static_cast<const bf16*>(p.g), p.beta, p.cu, p.num_seqs, p.T_seq, p.H, map, rec, n_tasks);
+    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, p.beta, p.num_seqs, p.H, map, rec,
+                                                              n_tasks, p.dev_err);
     prof_end(stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

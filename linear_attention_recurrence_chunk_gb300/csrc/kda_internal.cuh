@@ -43,7 +43,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { retu
 // Sequence -> chunk map built on the device from cu_seqlens (or from B, T).
 struct ChunkMap {
   int32_t* seq_chunk0;   // [num_seqs + 1] first global chunk of each sequence (exclusive scan)
-  int32_t* chunk_seq;    // [max_chunks] sequence of each global chunk
+  int4* chunk_info;      // [max_chunks] per global chunk: (sequence, rows, first token low, high word)
   int32_t max_chunks;    // upper bound used to size the grid
 };
 
@@ -56,14 +56,13 @@ struct ChunkPos {
 
 __device__ __forceinline__ bool locate_chunk(const ChunkMap& m, const int32_t* cu, int32_t num_seqs, int64_t T_seq,
                                              int32_t j, ChunkPos& p) {
+  (void)cu;
+  (void)T_seq;
   if (j >= m.seq_chunk0[num_seqs]) return false;
-  const int32_t s = m.chunk_seq[j];
-  const int32_t local = j - m.seq_chunk0[s];
-  const int64_t start = cu ? (int64_t)cu[s] : (int64_t)s * T_seq;
-  const int64_t end = cu ? (int64_t)cu[s + 1] : start + T_seq;
-  p.seq = s;
-  p.t0 = start + (int64_t)local * kChunk;
-  p.len = (int32_t)min((int64_t)kChunk, end - p.t0);
+  const int4 ci = m.chunk_info[j];
+  p.seq = ci.x;
+  p.len = ci.y;
+  p.t0 = (int64_t)(((uint64_t)(uint32_t)ci.w << 32) | (uint32_t)ci.z);
   return p.len > 0;
 }
 
@@ -91,7 +90,7 @@ struct ChunkProblem {
 // separate arrays so that each can be read with 2D TMA tiles.
 struct Workspace {
   size_t bytes;
-  size_t off_seq_chunk0, off_chunk_seq, off_inter;
+  size_t off_seq_chunk0, off_chunk_info, off_inter;
   int32_t max_chunks;
   size_t inter_bytes_per_chunk_head;
   bool tc;
