@@ -589,7 +589,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 }
 
 // -------------------------------------------------------------- chain kernel
-constexpr int kChainTcThreads = 160;          // 4 consumer warps (TMEM lanes 0-127) + 1 TMA producer warp
+// Warp roles: 8 consumer warps (warp w reads TMEM lanes 32(w%4)..+31 and the
+// value columns 16(w/4)..+15 of the CTA's block), one TMA producer warp and
+// one MMA-issuing warp.
+constexpr int kChainConsumerWarps = 8;
+constexpr int kChainTmaWarp = 8, kChainMmaWarp = 9;
+constexpr int kChainTcThreads = 32 * (kChainConsumerWarps + 2);
 // K-major A (TMA-staged tiles), MN-major B (the state block / V_new written by the threads), fp16,
 // M = 128, N = 32.
 constexpr uint32_t kIdescMN = tc::idesc_f16_f32(128, BV) | (1u << 16);
@@ -608,21 +613,38 @@ struct ChainTcSmem {
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
   static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
   static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
-  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain
-  static constexpr uint32_t oTmem = oBar + 7 * 8;
+  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready
+  static constexpr uint32_t oTmem = oBar + 9 * 8;
   static constexpr uint32_t kBytes = oTmem + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
 
-// 32 fp32 values of K row `k` of an MN-major SW64 operand, as fp16, in four 16-byte stores.
-__device__ __forceinline__ void store_mn_row(uint8_t* tile, int k, const float (&x)[32]) {
+// 16 fp32 values (value columns 16 hf .. 16 hf + 15) of K row `k` of an MN-major
+// SW64 operand, as fp16, in two 16-byte stores.
+__device__ __forceinline__ void store_mn_half(uint8_t* tile, int k, int hf, const float (&x)[16]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    *reinterpret_cast<uint4*>(tile + tc::sw64_chunk_offset(k, j)) =
+  for (int j = 0; j < 2; ++j)
+    *reinterpret_cast<uint4*>(tile + tc::sw64_chunk_offset(k, 2 * hf + j)) =
         make_uint4(pack_f16x2(x[8 * j + 0], x[8 * j + 1]), pack_f16x2(x[8 * j + 2], x[8 * j + 3]),
                    pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
 }
 
+// 16 fp32 values as bf16 to global memory (two 16-byte stores).
+__device__ __forceinline__ void store_bf16x16(bf16* dst, const float (&x)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    d[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                      pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+}
+
+// Inter-chunk pass of one (sequence, head, 32-column value block): the state
+// lives in fp32 registers of the consumer threads (key channel = TMEM lane),
+// its fp16 copy is the B operand of both MMA rounds of the next chunk.
+//   round 1: D12 = [w; q e^G] S                       (rows 0-63: w S, 64-127: q e^G S)
+//   V_new  = u - (w S)                                 (consumers, to SMEM)
+//   round 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
+//   S      = e^{G_last} S + D3                          (consumers)
 template <int DV>
 __global__ void __launch_bounds__(kChainTcThreads, 1)
     chunk_chain_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
@@ -639,6 +661,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* mma1 = full + 4;
   uint64_t* mma2 = full + 5;
   uint64_t* drain = full + 6;
+  uint64_t* vn_ready = full + 7;   // the 128 V_new threads have stored their rows
+  uint64_t* s_ready = full + 8;    // the 256 consumer threads have stored the state and read TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
@@ -652,6 +676,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
+    tc::mbar_init(vn_ready, 128);
+    tc::mbar_init(s_ready, 32 * kChainConsumerWarps);
     tc::fence_mbar_init();
   }
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
@@ -669,7 +695,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  if (warp == 4) {
+  if (warp == kChainTmaWarp) {
     // ---------------- TMA producer
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmWQ);
@@ -698,125 +724,128 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       // never leave loads in flight: wait (bounded) until the last ones landed
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) tc::mbar_wait(full + (i & 1), (i >> 1) & 1, kWaitLimit);
     }
-  } else {
-    // ---------------- consumers: thread t <-> TMEM lane t
-    const int c = tid;   // key channel of this thread's state row
-    float S[BV];
-    {
-      const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + n0;
+  } else if (warp == kChainMmaWarp) {
+    // ---------------- MMA issue (one thread).  Descriptors: the B tiles never
+    // move; A tiles differ per stage only by the stage offset, K slices by
+    // constant offsets added to the start-address field.
+    if (lane == 0) {
+      const uint64_t dS0 = tc::desc_mnmajor_sw64(tc::smem_u32(sS));
+      const uint64_t dV0 = tc::desc_mnmajor_sw64(tc::smem_u32(sVN));
+      const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));   // stage 0 base
+      bool ok = true, issued = false;
+      for (int i = 0; i < nch && ok; ++i) {
+        const int st = i & 1;
+        ok = tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit) && tc::mbar_wait(s_ready, i & 1, kWaitLimit);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
+        const uint32_t d12 = tmem + kTmemD12 + (uint32_t)st * 32;
+        tc::mma_16bit_first(d12, dA, dS0, kIdescMN);   // round 1
 #pragma unroll
-      for (int n = 0; n < BV; n += 4) {
+        for (int kk = 1; kk < DK / 16; ++kk)
+          tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN);
+        tc::mma_commit(mma1);
+        issued = true;
+        ok = tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
+        if (!ok) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)   // round 2
+          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
+        tc::mma_16bit_first(tmem + kTmemD3, dA + (L::oKT >> 4), dV0, kIdescMN);
+#pragma unroll
+        for (int kk = 1; kk < C / 16; ++kk)
+          tc::mma_16bit_acc(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
+        tc::mma_commit(mma2);
+        tc::mma_commit(empty + st);
+      }
+      if (!ok) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      if (issued) {   // no MMA may still be writing TMEM when it is freed
+        tc::mma_commit(drain);
+        tc::mbar_wait(drain, 0, kWaitLimit);
+      }
+    }
+  } else {
+    // ---------------- consumers: TMEM lane quarter q, value columns 16 hf .. 16 hf + 15
+    const int q = warp & 3, hf = warp >> 2;
+    const int c = 32 * q + lane;   // key channel of this thread's state row; token row for V_new / o
+    const uint32_t tl = (uint32_t)(32 * q);
+    float S[16];
+    {
+      const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + n0 + 16 * hf;
+#pragma unroll
+      for (int n = 0; n < 16; n += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s0) x = *reinterpret_cast<const float4*>(s0 + off + n);
         S[n] = x.x; S[n + 1] = x.y; S[n + 2] = x.z; S[n + 3] = x.w;
       }
     }
-    store_mn_row(sS, c, S);
-    // Operand descriptors: B tiles never move; A tiles differ per stage only by
-    // the stage offset, and K slices by constant offsets added to the start field.
-    const uint64_t dS0 = tc::desc_mnmajor_sw64(tc::smem_u32(sS));
-    const uint64_t dV0 = tc::desc_mnmajor_sw64(tc::smem_u32(sVN));
-    const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));   // stage 0 base
+    store_mn_half(sS, c, hf, S);
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(s_ready);
     bool bad = false;
-    bool issued = false;   // thread 0: some MMA was issued
     int i = 0;
     int64_t prev_t0 = 0;
     int64_t prev_len = 0;
     for (; i < nch; ++i) {
       const int st = i & 1;
-      uint8_t* stg = sm + st * L::kStage;
-      const uint32_t d12 = tmem + kTmemD12 + (uint32_t)st * 32;
+      const uint8_t* stg = sm + st * L::kStage;
       bad |= !tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit);
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      if (tc::bar_sync_or(1, 128, bad)) break;
-      tc::tc_fence_after();
-      const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
-      if (tid == 0) {   // round 1: D12 = [w; q e^G] . S
-#pragma unroll
-        for (int kk = 0; kk < DK / 16; ++kk)
-          tc::mma_16bit(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN,
-                        kk > 0);
-        tc::mma_commit(mma1);
-        issued = true;
-      }
-      if (i > 0 && warp >= 2 && !bad) {   // previous chunk's o rows (tokens) = lanes 64-127 of the other buffer
-        const int r = tid - 64;
-        float ov[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)(st ^ 1) * 32), ov);
-        if (r < prev_len) {
-          uint4* dst = reinterpret_cast<uint4*>(o + ((prev_t0 + r) * H + h) * DV + n0);
-#pragma unroll
-          for (int q4 = 0; q4 < BV / 8; ++q4)
-            dst[q4] = make_uint4(pack_bf16x2(ov[8 * q4 + 0], ov[8 * q4 + 1]), pack_bf16x2(ov[8 * q4 + 2], ov[8 * q4 + 3]),
-                                 pack_bf16x2(ov[8 * q4 + 4], ov[8 * q4 + 5]), pack_bf16x2(ov[8 * q4 + 6], ov[8 * q4 + 7]));
-        }
-      }
+      if (bad) break;
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
+      if (i > 0 && q >= 2) {   // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer
+        const int r = c - 64;
+        float ov[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
+        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+      }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
+      if (bad) break;
       tc::tc_fence_after();
-      if (!bad && warp < 2) {   // V_new rows (tokens) 0-63: u - w S
-        float d[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)st * 32), d);
-        const int r = tid;
-        const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + r * BV * 2);
+      if (q < 2) {   // V_new rows (tokens) 0-63: u - w S
+        float d[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)st * 32 + 16 * hf), d);
+        const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + c * BV * 2 + hf * 32);
 #pragma unroll
-        for (int q4 = 0; q4 < BV / 8; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
           const uint4 raw = urow[q4];
           const f16* uv = reinterpret_cast<const f16*>(&raw);
 #pragma unroll
           for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
         }
-        store_mn_row(sVN, r, d);
-      }
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_before();
-      if (tc::bar_sync_or(1, 128, bad)) break;
-      tc::tc_fence_after();
-      if (tid == 0) {   // round 2: D12 += [0; P] . V_new ; D3 = K~^T . V_new
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          tc::mma_16bit(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, 1);
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          tc::mma_16bit(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, kk > 0);
-        tc::mma_commit(mma2);
-        tc::mma_commit(empty + st);
+        store_mn_half(sVN, c, hf, d);
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(vn_ready);
       }
       bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
+      if (bad) break;
       tc::tc_fence_after();
-      if (!bad) {
-        float d[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD3), d);
+      {
+        float d[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD3 + 16 * hf), d);
 #pragma unroll
-        for (int n = 0; n < BV; ++n) S[n] = gam * S[n] + d[n];
-        store_mn_row(sS, c, S);
+        for (int n = 0; n < 16; ++n) S[n] = gam * S[n] + d[n];
+        store_mn_half(sS, c, hf, S);
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(s_ready);
       }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
-    if (i == nch && !bad && nch > 0 && warp >= 2) {   // the last chunk's o
-      const int r = tid - 64;
-      float ov[32];
-      tc::tmem_ld32(tc::tmem_addr(tmem, 32 * warp, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32), ov);
-      if (r < prev_len) {
-        uint4* dst = reinterpret_cast<uint4*>(o + ((prev_t0 + r) * H + h) * DV + n0);
-#pragma unroll
-        for (int q4 = 0; q4 < BV / 8; ++q4)
-          dst[q4] = make_uint4(pack_bf16x2(ov[8 * q4 + 0], ov[8 * q4 + 1]), pack_bf16x2(ov[8 * q4 + 2], ov[8 * q4 + 3]),
-                               pack_bf16x2(ov[8 * q4 + 4], ov[8 * q4 + 5]), pack_bf16x2(ov[8 * q4 + 6], ov[8 * q4 + 7]));
-      }
+    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
+      const int r = c - 64;
+      float ov[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
+      if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
     }
     if (i < nch || bad) {
-      if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      atomicExch(dev_err, (int32_t)kDevErrTimeout);
     } else if (s_final) {
-      float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + n0;
+      float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + n0 + 16 * hf;
 #pragma unroll
-      for (int n = 0; n < BV; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
-    }
-    if (tid == 0 && issued) {   // no MMA may still be writing TMEM when it is freed
-      tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0, kWaitLimit);
+      for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
     }
   }
   tc::tc_fence_before();
