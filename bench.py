@@ -56,8 +56,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=100)
-    ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD], default=WORKLOAD,
-                    help="the headline workload, or a T=8192 cut of it for profiler captures")
+    ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD, "prefill_b8_h96_t8192_d128",
+                                           "varlen_12seq_1m_h32_d128"], default=WORKLOAD,
+                    help="the headline workload (default), a T=8192 cut of it for profiler captures, "
+                         "or one of the other prefill workloads")
     return ap.parse_args()
 
 
@@ -252,8 +254,8 @@ def bench_prefill(args, ws_size, local):
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
 
     def step():
-        kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["s0"], o=o, final_state=sf,
-                          workspace=wsp, stream=stream)
+        kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["s0"], cu_seqlens=t["cu"],
+                          o=o, final_state=sf, workspace=wsp, stream=stream)
 
     for _ in range(args.warmup):
         step()

@@ -42,6 +42,8 @@
 #include <mutex>
 
 #include "kda_internal.cuh"
+
+#include <cstdlib>
 #include "tc_ptx.cuh"
 
 namespace kda {
@@ -853,6 +855,260 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------- wide chain kernel
+// The same inter-chunk pass with all DV value columns in one CTA (one CTA per
+// (sequence, head)): the per-chunk A tiles are read and the MMAs issued once
+// per head instead of once per 32-column block.  Used when the 32-column grid
+// would exceed one wave of the GPU.  Consumer warp w reads TMEM lanes
+// 32(w%4)..+31 and value columns 32(w/4)..+31; the state block and V_new are
+// MN-major B operands of DV/32 atoms of 32 columns.
+template <int DV>
+struct ChainWideSmem {
+  static constexpr int kConsumerWarps = 4 * (DV / 32);
+  static constexpr int kThreads = 32 * (kConsumerWarps + 2);
+  static constexpr int kTmaWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
+  static constexpr uint32_t kTmemCols = DV == 128 ? 512 : 256;   // D12 x 2 + D3, DV columns each
+  static constexpr uint32_t oWQ = 0;           // [w; q e^G] 128 x 128: two 64-column atoms of 16 KB
+  static constexpr uint32_t oPZ = 32768;       // [0; P] 128 x 64 (rows 0-63 stay zero)
+  static constexpr uint32_t oKT = 49152;       // (k e^{G_last-G})^T 128 x 64
+  static constexpr uint32_t oU = 65536;        // u 64 x DV, plain row-major
+  static constexpr uint32_t oGam = oU + 64 * DV * 2;   // e^{G_last}, 128 fp32
+  static constexpr uint32_t kStage = (oGam + DK * 4 + 1023) / 1024 * 1024;
+  static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * DV * 2 + DK * 4;
+  static constexpr uint32_t kSAtom = DK * 64, kVAtom = C * 64;   // MN atom strides
+  static constexpr uint32_t oS = 2 * kStage;                      // state block, DV/32 atoms
+  static constexpr uint32_t oVN = oS + (DV / 32) * kSAtom;        // V_new, DV/32 atoms
+  static constexpr uint32_t oBar = oVN + (DV / 32) * kVAtom;      // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready
+  static constexpr uint32_t oTmem = oBar + 9 * 8;
+  static constexpr uint32_t kBytes = oTmem + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
+};
+
+// 32 fp32 values of K row `k` of one 32-column MN-major SW64 atom, as fp16.
+__device__ __forceinline__ void store_mn_atom_row(uint8_t* atom, int k, const float (&x)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(atom + tc::sw64_chunk_offset(k, j)) =
+        make_uint4(pack_f16x2(x[8 * j + 0], x[8 * j + 1]), pack_f16x2(x[8 * j + 2], x[8 * j + 3]),
+                   pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
+}
+
+template <int DV>
+__global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
+    chunk_chain_wide_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
+                        const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
+                        const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu,
+                        int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0,
+                        float* __restrict__ s_final, bf16* __restrict__ o, int32_t* dev_err) {
+  using L = ChainWideSmem<DV>;
+  constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, DV) | (1u << 16);
+  constexpr uint32_t kD3 = 2 * DV;
+  if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::oBar);
+  uint64_t* empty = full + 2;
+  uint64_t* mma1 = full + 4;
+  uint64_t* mma2 = full + 5;
+  uint64_t* drain = full + 6;
+  uint64_t* vn_ready = full + 7;
+  uint64_t* s_ready = full + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
+  uint8_t* sS = sm + L::oS;
+  uint8_t* sVN = sm + L::oVN;
+
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int32_t j0 = map.seq_chunk0[s];
+  const int32_t nch = map.seq_chunk0[s + 1] - j0;
+  const int64_t seq_start = cu ? (int64_t)cu[s] : (int64_t)s * T_seq;
+  const int64_t seq_end = cu ? (int64_t)cu[s + 1] : seq_start + T_seq;
+
+  if (tid == 0) {
+    for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
+    tc::mbar_init(vn_ready, 32 * (L::kConsumerWarps / 2));
+    tc::mbar_init(s_ready, 32 * L::kConsumerWarps);
+    tc::fence_mbar_init();
+  }
+  for (int i = tid; i < 2 * 512; i += L::kThreads) {   // rows 0-63 of both [0; P] tiles stay zero
+    const int st = i >> 9, off = (i & 511) * 16;
+    *reinterpret_cast<uint4*>(sm + st * L::kStage + L::oPZ + off) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, L::kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == L::kTmaWarp) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmWQ);
+      tc::tma_prefetch_desc(&tmP);
+      tc::tma_prefetch_desc(&tmKT);
+      tc::tma_prefetch_desc(&tmU);
+      tc::tma_prefetch_desc(&tmGam);
+      int issued = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !tc::mbar_wait(empty + st, ((i >> 1) - 1) & 1, kWaitLimit)) {
+          atomicExch(dev_err, (int32_t)kDevErrTimeout);
+          break;
+        }
+        const int64_t rec = (int64_t)(j0 + i) * H + h;
+        uint8_t* stg = sm + st * L::kStage;
+        tc::mbar_arrive_expect_tx(full + st, L::kTxBytes);
+        tc::tma_load_2d(stg + L::oWQ, &tmWQ, 0, (int32_t)(rec * 128), full + st);
+        tc::tma_load_2d(stg + L::oWQ + 16384, &tmWQ, 64, (int32_t)(rec * 128), full + st);
+        tc::tma_load_2d(stg + L::oPZ + 8192, &tmP, 0, (int32_t)(rec * C), full + st);
+        tc::tma_load_2d(stg + L::oKT, &tmKT, 0, (int32_t)(rec * DK), full + st);
+        tc::tma_load_2d(stg + L::oU, &tmU, 0, (int32_t)(rec * C), full + st);
+        tc::tma_load_2d(stg + L::oGam, &tmGam, 0, (int32_t)rec, full + st);
+        ++issued;
+      }
+      for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) tc::mbar_wait(full + (i & 1), (i >> 1) & 1, kWaitLimit);
+    }
+  } else if (warp == L::kMmaWarp) {
+    if (lane == 0) {
+      const uint64_t dS0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sS), L::kSAtom);
+      const uint64_t dV0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sVN), L::kVAtom);
+      const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));
+      bool ok = true, issued = false;
+      for (int i = 0; i < nch && ok; ++i) {
+        const int st = i & 1;
+        ok = tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit) && tc::mbar_wait(s_ready, i & 1, kWaitLimit);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
+        const uint32_t d12 = tmem + (uint32_t)st * DV;
+        tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // round 1
+#pragma unroll
+        for (int kk = 1; kk < DK / 16; ++kk)
+          tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdesc);
+        tc::mma_commit(mma1);
+        issued = true;
+        ok = tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
+        if (!ok) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)   // round 2
+          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc);
+        tc::mma_16bit_first(tmem + kD3, dA + (L::oKT >> 4), dV0, kIdesc);
+#pragma unroll
+        for (int kk = 1; kk < C / 16; ++kk)
+          tc::mma_16bit_acc(tmem + kD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc);
+        tc::mma_commit(mma2);
+        tc::mma_commit(empty + st);
+      }
+      if (!ok) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      if (issued) {
+        tc::mma_commit(drain);
+        tc::mbar_wait(drain, 0, kWaitLimit);
+      }
+    }
+  } else {
+    const int q = warp & 3, cg = warp >> 2;   // TMEM lane quarter, 32-column group
+    const int c = 32 * q + lane;
+    const uint32_t tl = (uint32_t)(32 * q);
+    float S[32];
+    {
+      const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + 32 * cg;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0) x = *reinterpret_cast<const float4*>(s0 + off + n);
+        S[n] = x.x; S[n + 1] = x.y; S[n + 2] = x.z; S[n + 3] = x.w;
+      }
+    }
+    store_mn_atom_row(sS + cg * L::kSAtom, c, S);
+    tc::fence_proxy_async_smem();
+    tc::mbar_arrive(s_ready);
+    bool bad = false;
+    int i = 0;
+    int64_t prev_t0 = 0;
+    int64_t prev_len = 0;
+    for (; i < nch; ++i) {
+      const int st = i & 1;
+      const uint8_t* stg = sm + st * L::kStage;
+      bad |= !tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit);
+      if (bad) break;
+      const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
+      if (i > 0 && q >= 2) {   // previous chunk's o rows from the other buffer
+        const int r = c - 64;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float ov[16];
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)(st ^ 1) * DV + 32 * cg + 16 * hf), ov);
+          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + 32 * cg + 16 * hf, ov);
+        }
+      }
+      bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
+      if (bad) break;
+      tc::tc_fence_after();
+      if (q < 2) {   // V_new rows (tokens) 0-63: u - w S, in two 16-column halves
+        const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + (c * DV + 32 * cg) * 2);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float d[16];
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)st * DV + 32 * cg + 16 * hf), d);
+#pragma unroll
+          for (int q4 = 0; q4 < 2; ++q4) {
+            const uint4 raw = urow[2 * hf + q4];
+            const f16* uv = reinterpret_cast<const f16*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
+          }
+          store_mn_half(sVN + cg * L::kVAtom, c, hf, d);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(vn_ready);
+      }
+      bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
+      if (bad) break;
+      tc::tc_fence_after();
+      {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float d[16];
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, kD3 + 32 * cg + 16 * hf), d);
+#pragma unroll
+          for (int n = 0; n < 16; ++n) S[16 * hf + n] = gam * S[16 * hf + n] + d[n];
+        }
+        store_mn_atom_row(sS + cg * L::kSAtom, c, S);
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(s_ready);
+      }
+      prev_t0 = seq_start + (int64_t)i * C;
+      prev_len = min((int64_t)C, seq_end - prev_t0);
+    }
+    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
+      const int r = c - 64;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float ov[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)((nch - 1) & 1) * DV + 32 * cg + 16 * hf), ov);
+        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + 32 * cg + 16 * hf, ov);
+      }
+    }
+    if (i < nch || bad) {
+      atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    } else if (s_final) {
+      float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + 32 * cg;
+#pragma unroll
+      for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
+}
+
 // --------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -925,14 +1181,39 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     prof_end(stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // Chain variant: 32 value columns per CTA (the most CTAs, for few long
+  // chains) unless that grid exceeds one wave of the GPU; then one CTA per
+  // (sequence, head) with all DV columns, which reads the per-chunk tiles and
+  // issues the MMAs once per head.  KDA_CHAIN_COLUMNS=32 or =DV forces one.
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  bool wide = (int64_t)p.num_seqs * p.H * (DV / BV) > sms;
+  if (const char* env = std::getenv("KDA_CHAIN_COLUMNS")) {
+    const int cols = std::atoi(env);
+    if (cols == BV) wide = false;
+    else if (cols == DV) wide = true;
+  }
   CUtensorMap mWQ, mP, mKT, mU, mGam;
   const uint64_t Rr = R > 0 ? R : 1;
   if (!make_map(&mWQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, Rr * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mP, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, Rr * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mKT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.kt, C, Rr * DK, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, BV, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, wide ? DV : BV, 64,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  if (wide) {
+    using W = ChainWideSmem<DV>;
+    e = cudaFuncSetAttribute(chunk_chain_wide_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
+    if (e != cudaSuccess) return e;
+    prof_begin(stream, "chunk_chain_wide_tc");
+    chunk_chain_wide_tc<DV><<<dim3(p.num_seqs, p.H), W::kThreads, W::kAlloc, stream>>>(
+        mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
+        p.dev_err);
+    prof_end(stream);
+    return cudaGetLastError();
+  }
   e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_tc");

@@ -182,6 +182,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw64(uint32_t addr) {
   return d;
 }
 
+// The same layout for an MN extent of several 32-element atoms, each a
+// separate [K rows][64 B] block `atom_stride` bytes after the previous one
+// (the leading byte offset of MN-major swizzled layouts is the atom stride).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw64_atoms(uint32_t addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);               // start address >> 4
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: MN atom stride
+  d |= (uint64_t)(512u >> 4) << 32;                     // stride byte offset: 8 K rows x 64 B
+  d |= (uint64_t)1u << 46;                              // descriptor version 1
+  d |= (uint64_t)4u << 61;                              // 64-byte swizzle
+  return d;
+}
+
 // Byte offset of the 16-byte chunk j (MN elements 8j..8j+7) of K row k in that layout.
 __host__ __device__ __forceinline__ uint32_t sw64_chunk_offset(uint32_t k, uint32_t j) {
   return k * 64u + (((j ^ (k >> 1)) & 3u) << 4);

@@ -61,6 +61,24 @@ def test_prefill_small_all_outputs(dtype, d_k, d_v, B, T, s0_std):
     _check_all_chains(w, o, sf)
 
 
+@pytest.mark.parametrize("chain_cols", ["32", "full"])
+@pytest.mark.parametrize("d_v,B,T,lens", [(128, 2, 1, None), (128, 3, 200, None), (64, 1, 191, None),
+                                          (128, 1, None, [0, 1, 63, 64, 65, 200, 0, 17])])
+def test_prefill_both_chain_widths(monkeypatch, chain_cols, d_v, B, T, lens):
+    """Both inter-chunk variants (32 value columns per CTA, and all of them) on
+    the same small cases: full tiles, ragged tails, empty sequences."""
+    monkeypatch.setenv("KDA_CHAIN_COLUMNS", "32" if chain_cols == "32" else str(d_v))
+    if lens is not None:
+        lens = np.array(lens)
+        w = ks.PrefillWorkload("widths", "bf16", 1, int(lens.sum()), 3, 128, d_v, seed=321, s0_std=0.05,
+                               seq_lens=lens)
+    else:
+        w = ks.PrefillWorkload("widths", "bf16", B, T, 3, 128, d_v, seed=123 + T, s0_std=0.05)
+    t = prefill_device_inputs(w, DEV)
+    o, sf = _run_prefill(w, t)
+    _check_all_chains(w, o, sf)
+
+
 def test_fp32_b1_h2_t256_d64_workload():
     """The fp32 workload in full (B=1, H=2, T=256, d=64, S0 = 0)."""
     w = ks.workloads()["fp32_b1_h2_t256_d64"]
