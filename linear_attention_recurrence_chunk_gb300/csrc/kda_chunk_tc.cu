@@ -609,7 +609,7 @@ struct ChainTcSmem {
   static constexpr uint32_t oWQ = 0;           // [w; q e^G] 128 x 128: two 64-column atoms of 16 KB
   static constexpr uint32_t oPZ = 32768;       // [0; P] 128 x 64 (rows 0-63 stay zero)
   static constexpr uint32_t oKT = 49152;       // (k e^{G_last-G})^T 128 x 64
-  static constexpr uint32_t oU = 65536;        // u block 64 x 32, plain row-major (64 B rows)
+  static constexpr uint32_t oU = 65536;        // u block 64 x 32, 64-byte swizzle (64 B rows)
   static constexpr uint32_t oGam = 69632;      // e^{G_last}, 128 fp32
   static constexpr uint32_t kStage = 71680;    // 70 KB, keeps the next stage 1024-aligned
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
@@ -663,8 +663,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* mma1 = full + 4;
   uint64_t* mma2 = full + 5;
   uint64_t* drain = full + 6;
-  uint64_t* vn_ready = full + 7;   // the 128 V_new threads have stored their rows
-  uint64_t* s_ready = full + 8;    // the 256 consumer threads have stored the state and read TMEM
+  uint64_t* vn_ready = full + 7;   // the 4 V_new warps have stored their rows
+  uint64_t* s_ready = full + 8;    // the 8 consumer warps have stored the state and read TMEM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
@@ -678,8 +678,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
-    tc::mbar_init(vn_ready, 128);
-    tc::mbar_init(s_ready, 32 * kChainConsumerWarps);
+    tc::mbar_init(vn_ready, 4);                      // one arrival per V_new warp
+    tc::mbar_init(s_ready, kChainConsumerWarps);     // one arrival per consumer warp
     tc::fence_mbar_init();
   }
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
@@ -784,7 +784,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     }
     store_mn_half(sS, c, hf, S);
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(s_ready);
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(s_ready);
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -793,7 +794,10 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       const int st = i & 1;
       const uint8_t* stg = sm + st * L::kStage;
       bad |= !tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
       if (i > 0 && q >= 2) {   // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer
         const int r = c - 64;
@@ -802,15 +806,17 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       tc::tc_fence_after();
       if (q < 2) {   // V_new rows (tokens) 0-63: u - w S
         float d[16];
         tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)st * 32 + 16 * hf), d);
-        const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + c * BV * 2 + hf * 32);
 #pragma unroll
         for (int q4 = 0; q4 < 2; ++q4) {
-          const uint4 raw = urow[q4];
+          const uint4 raw = *reinterpret_cast<const uint4*>(stg + L::oU + tc::sw64_chunk_offset(c, 2 * hf + q4));
           const f16* uv = reinterpret_cast<const f16*>(&raw);
 #pragma unroll
           for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
@@ -818,10 +824,14 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         store_mn_half(sVN, c, hf, d);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(vn_ready);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(vn_ready);
       }
       bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       tc::tc_fence_after();
       {
         float d[16];
@@ -831,7 +841,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         store_mn_half(sS, c, hf, S);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(s_ready);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(s_ready);
       }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
@@ -871,7 +882,7 @@ struct ChainWideSmem {
   static constexpr uint32_t oWQ = 0;           // [w; q e^G] 128 x 128: two 64-column atoms of 16 KB
   static constexpr uint32_t oPZ = 32768;       // [0; P] 128 x 64 (rows 0-63 stay zero)
   static constexpr uint32_t oKT = 49152;       // (k e^{G_last-G})^T 128 x 64
-  static constexpr uint32_t oU = 65536;        // u 64 x DV, plain row-major
+  static constexpr uint32_t oU = 65536;        // u 64 x DV: DV/64 atoms [64 rows][128 B], 128-byte swizzle
   static constexpr uint32_t oGam = oU + 64 * DV * 2;   // e^{G_last}, 128 fp32
   static constexpr uint32_t kStage = (oGam + DK * 4 + 1023) / 1024 * 1024;
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * DV * 2 + DK * 4;
@@ -927,8 +938,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
-    tc::mbar_init(vn_ready, 32 * (L::kConsumerWarps / 2));
-    tc::mbar_init(s_ready, 32 * L::kConsumerWarps);
+    tc::mbar_init(vn_ready, L::kConsumerWarps / 2);   // one arrival per V_new warp
+    tc::mbar_init(s_ready, L::kConsumerWarps);        // one arrival per consumer warp
     tc::fence_mbar_init();
   }
   for (int i = tid; i < 2 * 512; i += L::kThreads) {   // rows 0-63 of both [0; P] tiles stay zero
@@ -966,7 +977,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         tc::tma_load_2d(stg + L::oWQ + 16384, &tmWQ, 64, (int32_t)(rec * 128), full + st);
         tc::tma_load_2d(stg + L::oPZ + 8192, &tmP, 0, (int32_t)(rec * C), full + st);
         tc::tma_load_2d(stg + L::oKT, &tmKT, 0, (int32_t)(rec * DK), full + st);
-        tc::tma_load_2d(stg + L::oU, &tmU, 0, (int32_t)(rec * C), full + st);
+#pragma unroll
+        for (int a = 0; a < DV / 64; ++a) tc::tma_load_2d(stg + L::oU + a * 8192, &tmU, 64 * a, (int32_t)(rec * C), full + st);
         tc::tma_load_2d(stg + L::oGam, &tmGam, 0, (int32_t)rec, full + st);
         ++issued;
       }
@@ -1026,7 +1038,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
     }
     store_mn_atom_row(sS + cg * L::kSAtom, c, S);
     tc::fence_proxy_async_smem();
-    tc::mbar_arrive(s_ready);
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(s_ready);
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -1035,7 +1048,10 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
       const int st = i & 1;
       const uint8_t* stg = sm + st * L::kStage;
       bad |= !tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
       if (i > 0 && q >= 2) {   // previous chunk's o rows from the other buffer
         const int r = c - 64;
@@ -1047,17 +1063,21 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         }
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       tc::tc_fence_after();
       if (q < 2) {   // V_new rows (tokens) 0-63: u - w S, in two 16-column halves
-        const uint4* urow = reinterpret_cast<const uint4*>(stg + L::oU + (c * DV + 32 * cg) * 2);
+        const uint8_t* uat = stg + L::oU + (cg >> 1) * 8192;   // the 64-column atom of this column group
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float d[16];
           tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)st * DV + 32 * cg + 16 * hf), d);
 #pragma unroll
           for (int q4 = 0; q4 < 2; ++q4) {
-            const uint4 raw = urow[2 * hf + q4];
+            const uint4 raw =
+                *reinterpret_cast<const uint4*>(uat + tc::sw128_offset(c, 32 * (cg & 1) + 16 * hf + 8 * q4));
             const f16* uv = reinterpret_cast<const f16*>(&raw);
 #pragma unroll
             for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
@@ -1066,10 +1086,14 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(vn_ready);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(vn_ready);
       }
       bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
-      if (bad) break;
+      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+        bad = true;
+        break;
+      }
       tc::tc_fence_after();
       {
 #pragma unroll
@@ -1082,7 +1106,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         store_mn_atom_row(sS + cg * L::kSAtom, c, S);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(s_ready);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(s_ready);
       }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
@@ -1199,8 +1224,8 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   if (!make_map(&mWQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, Rr * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mP, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, Rr * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&mKT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.kt, C, Rr * DK, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, wide ? DV : BV, 64,
-                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, wide ? 64 : BV, 64,
+                wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (wide) {
