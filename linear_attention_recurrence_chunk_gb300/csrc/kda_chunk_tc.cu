@@ -867,14 +867,15 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 }
 
 // ------------------------------------------------------- wide chain kernel
-// The same inter-chunk pass with all DV value columns in one CTA (one CTA per
-// (sequence, head)): the per-chunk A tiles are read and the MMAs issued once
-// per head instead of once per 32-column block.  Used when the 32-column grid
-// would exceed one wave of the GPU.  Consumer warp w reads TMEM lanes
-// 32(w%4)..+31 and value columns 32(w/4)..+31; the state block and V_new are
-// MN-major B operands of DV/32 atoms of 32 columns.
-template <int DV>
+// The same inter-chunk pass with NC = 64 or 128 value columns per CTA: the
+// per-chunk A tiles are read and the MMAs issued once per NC columns instead
+// of once per 32.  Used when the 32-column grid would exceed one wave of the
+// GPU.  Consumer warp w reads TMEM lanes 32(w%4)..+31 and value columns
+// 32(w/4)..+31 of the block; the state block and V_new are MN-major B operands
+// of NC/32 atoms of 32 columns.
+template <int NC>
 struct ChainWideSmem {
+  static constexpr int DV = NC;              // value columns held by one CTA
   static constexpr int kConsumerWarps = 4 * (DV / 32);
   static constexpr int kThreads = 32 * (kConsumerWarps + 2);
   static constexpr int kTmaWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
@@ -905,16 +906,16 @@ __device__ __forceinline__ void store_mn_atom_row(uint8_t* atom, int k, const fl
                    pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
 }
 
-template <int DV>
-__global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
+template <int DV, int NC>
+__global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     chunk_chain_wide_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
                         const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu,
                         int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0,
                         float* __restrict__ s_final, bf16* __restrict__ o, int32_t* dev_err) {
-  using L = ChainWideSmem<DV>;
-  constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, DV) | (1u << 16);
-  constexpr uint32_t kD3 = 2 * DV;
+  using L = ChainWideSmem<NC>;
+  constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, NC) | (1u << 16);
+  constexpr uint32_t kD3 = 2 * NC;
   if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -929,7 +930,7 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
-  const int s = blockIdx.x, h = blockIdx.y;
+  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * NC;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t j0 = map.seq_chunk0[s];
   const int32_t nch = map.seq_chunk0[s + 1] - j0;
@@ -978,7 +979,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         tc::tma_load_2d(stg + L::oPZ + 8192, &tmP, 0, (int32_t)(rec * C), full + st);
         tc::tma_load_2d(stg + L::oKT, &tmKT, 0, (int32_t)(rec * DK), full + st);
 #pragma unroll
-        for (int a = 0; a < DV / 64; ++a) tc::tma_load_2d(stg + L::oU + a * 8192, &tmU, 64 * a, (int32_t)(rec * C), full + st);
+        for (int a = 0; a < NC / 64; ++a)
+          tc::tma_load_2d(stg + L::oU + a * 8192, &tmU, n0 + 64 * a, (int32_t)(rec * C), full + st);
         tc::tma_load_2d(stg + L::oGam, &tmGam, 0, (int32_t)rec, full + st);
         ++issued;
       }
@@ -996,7 +998,7 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
         const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
-        const uint32_t d12 = tmem + (uint32_t)st * DV;
+        const uint32_t d12 = tmem + (uint32_t)st * NC;
         tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // round 1
 #pragma unroll
         for (int kk = 1; kk < DK / 16; ++kk)
@@ -1028,7 +1030,7 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
     const uint32_t tl = (uint32_t)(32 * q);
     float S[32];
     {
-      const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + 32 * cg;
+      const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + n0 + 32 * cg;
 #pragma unroll
       for (int n = 0; n < 32; n += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1058,8 +1060,8 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float ov[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)(st ^ 1) * DV + 32 * cg + 16 * hf), ov);
-          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + 32 * cg + 16 * hf, ov);
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)(st ^ 1) * NC + 32 * cg + 16 * hf), ov);
+          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 32 * cg + 16 * hf, ov);
         }
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
@@ -1073,7 +1075,7 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float d[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)st * DV + 32 * cg + 16 * hf), d);
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)st * NC + 32 * cg + 16 * hf), d);
 #pragma unroll
           for (int q4 = 0; q4 < 2; ++q4) {
             const uint4 raw =
@@ -1117,14 +1119,14 @@ __global__ void __launch_bounds__(ChainWideSmem<DV>::kThreads, 1)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float ov[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)((nch - 1) & 1) * DV + 32 * cg + 16 * hf), ov);
-        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + 32 * cg + 16 * hf, ov);
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)((nch - 1) & 1) * NC + 32 * cg + 16 * hf), ov);
+        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 32 * cg + 16 * hf, ov);
       }
     }
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
     } else if (s_final) {
-      float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + 32 * cg;
+      float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + n0 + 32 * cg;
 #pragma unroll
       for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
     }
@@ -1175,6 +1177,30 @@ bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int DV, int NC>
+cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
+                                 const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
+                                 const ChunkMap& map, cudaStream_t stream) {
+  using W = ChainWideSmem<NC>;
+  cudaError_t e =
+      cudaFuncSetAttribute(chunk_chain_wide_tc<DV, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
+  if (e != cudaSuccess) return e;
+  prof_begin(stream, "chunk_chain_wide_tc");
+  chunk_chain_wide_tc<DV, NC><<<dim3(p.num_seqs, p.H, DV / NC), W::kThreads, W::kAlloc, stream>>>(
+      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
+      p.dev_err);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_chain_wide(int ncol, const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
+                              const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
+                              const ChunkMap& map, cudaStream_t stream) {
+  if (DV == 128 && ncol == 128) return launch_chain_wide_nc<DV, (DV == 128 ? 128 : 64)>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+  return launch_chain_wide_nc<DV, 64>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+}
+
 template <int DV>
 cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap& map, char* base,
                       cudaStream_t stream) {
@@ -1209,16 +1235,16 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   // Chain variant: 32 value columns per CTA (the most CTAs, for few long
   // chains) unless that grid exceeds one wave of the GPU; then one CTA per
   // (sequence, head) with all DV columns, which reads the per-chunk tiles and
-  // issues the MMAs once per head.  KDA_CHAIN_COLUMNS=32 or =DV forces one.
+  // issues the MMAs once per head.  KDA_CHAIN_COLUMNS=32, 64 or DV forces a width.
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  bool wide = (int64_t)p.num_seqs * p.H * (DV / BV) > sms;
+  int ncol = (int64_t)p.num_seqs * p.H * (DV / BV) > sms ? DV : BV;
   if (const char* env = std::getenv("KDA_CHAIN_COLUMNS")) {
     const int cols = std::atoi(env);
-    if (cols == BV) wide = false;
-    else if (cols == DV) wide = true;
+    if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
+  const bool wide = ncol != BV;
   CUtensorMap mWQ, mP, mKT, mU, mGam;
   const uint64_t Rr = R > 0 ? R : 1;
   if (!make_map(&mWQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, Rr * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1228,17 +1254,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
                 wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (wide) {
-    using W = ChainWideSmem<DV>;
-    e = cudaFuncSetAttribute(chunk_chain_wide_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
-    if (e != cudaSuccess) return e;
-    prof_begin(stream, "chunk_chain_wide_tc");
-    chunk_chain_wide_tc<DV><<<dim3(p.num_seqs, p.H), W::kThreads, W::kAlloc, stream>>>(
-        mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-        p.dev_err);
-    prof_end(stream);
-    return cudaGetLastError();
-  }
+  if (wide) return launch_chain_wide<DV>(ncol, mWQ, mP, mKT, mU, mGam, p, map, stream);
   e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_tc");

@@ -61,13 +61,13 @@ def test_prefill_small_all_outputs(dtype, d_k, d_v, B, T, s0_std):
     _check_all_chains(w, o, sf)
 
 
-@pytest.mark.parametrize("chain_cols", ["32", "full"])
+@pytest.mark.parametrize("chain_cols", ["32", "64", "full"])
 @pytest.mark.parametrize("d_v,B,T,lens", [(128, 2, 1, None), (128, 3, 200, None), (64, 1, 191, None),
                                           (128, 1, None, [0, 1, 63, 64, 65, 200, 0, 17])])
 def test_prefill_both_chain_widths(monkeypatch, chain_cols, d_v, B, T, lens):
-    """Both inter-chunk variants (32 value columns per CTA, and all of them) on
-    the same small cases: full tiles, ragged tails, empty sequences."""
-    monkeypatch.setenv("KDA_CHAIN_COLUMNS", "32" if chain_cols == "32" else str(d_v))
+    """Every inter-chunk variant (32, 64 or all value columns per CTA) on the
+    same small cases: full tiles, ragged tails, empty sequences."""
+    monkeypatch.setenv("KDA_CHAIN_COLUMNS", str(d_v) if chain_cols == "full" else chain_cols)
     if lens is not None:
         lens = np.array(lens)
         w = ks.PrefillWorkload("widths", "bf16", 1, int(lens.sum()), 3, 128, d_v, seed=321, s0_std=0.05,
