@@ -2,20 +2,23 @@
 //
 // Two kernels per call, after the sequence -> chunk map:
 //
-//  chunk_prep_tc   one CTA per (64-token chunk, head).  Gate, cumulative
-//                  log-decay, the exp(+-G) scalings, the beta-weighted
-//                  decayed k k^T matrix A and the intra-chunk read-out matrix
-//                  P per 16-row sub-tile (mma.sync: the sub-tiles are 16 rows
-//                  tall), X = (I + A)^{-1} by blocked forward substitution,
-//                  then w, u = X Diag(beta) [k e^G | V] (mma.sync).  Writes
-//                  fp16 records: [w; q e^G], P, (k e^{G_last - G})^T, u and
-//                  fp32 e^{G_last}.
+//  chunk_prep_tc   persistent, one 512-thread CTA per SM over (64-token chunk,
+//                  head) tasks in chunk-major order; the next task's raw rows
+//                  arrive by TMA while the current one is processed.  Gate,
+//                  cumulative log-decay, the exp(+-G) scalings, the
+//                  beta-weighted decayed k k^T matrix A and the intra-chunk
+//                  read-out matrix P per 16-row sub-tile (mma.sync: the
+//                  sub-tiles are 16 rows tall), X = (I + A)^{-1} by blocked
+//                  forward substitution, then w, u = X Diag(beta) [k e^G | V]
+//                  (mma.sync).  Writes fp16 records: [w; q e^G], P,
+//                  (k e^{G_last - G})^T, u and fp32 e^{G_last}.
 //
-//  chunk_chain_tc  one CTA per (sequence, head, 32 value columns).  Walks the
+//  chunk_chain_tc  one CTA per (sequence, head, 32 value columns); the wide
+//  (_wide_tc)      form takes 64 or all value columns per CTA.  Walks the
 //                  sequence's chunks in order with the fp32 state block in
-//                  registers, feeding tcgen05 MMAs (fp32 accumulators in TMEM)
-//                  from TMA-staged fp16 tiles (double-buffered by a producer
-//                  warp):
+//                  registers, feeding tcgen05 MMAs (fp32 accumulators in TMEM,
+//                  issued by one warp) from TMA-staged fp16 tiles
+//                  (double-buffered by a producer warp):
 //                     round 1:  D12 = [w; q e^G] . S                (M=128, K=d_k)
 //                               V_new = u - D12[0:64]
 //                     round 2:  D12 += [0; P] . V_new               (M=128, K=64)
@@ -26,9 +29,11 @@
 // factors reach e^80); everything the chain multiplies is bounded by 1 or by
 // the size of v and S, so it is stored in fp16, whose 10-bit mantissa is 4x
 // finer than bf16's.  P multiplies V_new (O(|v|)) into o, which is an order
-// of magnitude smaller than v, so P gets a two-term bf16 split on both
-// operands (hi*hi + hi*lo + lo*hi, about 16 bits).  With plain bf16 everywhere
-// the largest output error reached ~5% of rms(o); with this split it is ~0.4%.
+// of magnitude smaller than v, so P's diagonal sub-tiles get a two-term bf16
+// split on both operands (hi*hi + hi*lo + lo*hi, about 16 bits); below the
+// diagonal every factor is <= 1 and single bf16 products suffice.  With plain
+// bf16 everywhere the largest output error reached ~5% of rms(o); with this
+// split it is ~0.6%.
 //
 // The algebra (page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.3: intra-chunk
 // work as matrix products, the state passed across chunk boundaries) is
@@ -103,7 +108,21 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
 // (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
-__device__ __forceinline__ float fast_log_decay(float x) { return __fdividef(-5.f, 1.f + __expf(-x)); }
+// log2 of the decay, -5 Sigmoid(x) / ln 2: the prep kernel keeps G in base-2 units so that every
+// factor 2^{G_a - G_b} is one ex2.approx.
+__device__ __forceinline__ float fast_log2_decay(float x) {
+  return __fdividef(-5.f * 1.4426950408889634f, 1.f + __expf(-x));
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -286,8 +305,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       for (int rr = 0; rr < 8; ++rr) {
         const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
         if (r0 + rr < len) {
-          run.x += fast_log_decay(__low2float(x));
-          run.y += fast_log_decay(__high2float(x));
+          run.x += fast_log2_decay(__low2float(x));
+          run.y += fast_log2_decay(__high2float(x));
         }
         G[rr] = run;
       }
@@ -331,15 +350,18 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         G[rr].y += excl.y;
       }
     }
-    const float2 gs = gsA[a];
-    const float2 lam = make_float2(__expf(gs.x), __expf(gs.y));
-    const float2 psi = make_float2(__expf(gl.x - gs.x), __expf(gl.y - gs.y));
+    float2 gs = gsA[0];   // G_s(a), selected without a dynamic register index
+#pragma unroll
+    for (int a2 = 1; a2 < 4; ++a2)
+      if (a2 == a) gs = gsA[a2];
+    const float2 lam = make_float2(ex2_approx(gs.x), ex2_approx(gs.y));
+    const float2 psi = make_float2(ex2_approx(gl.x - gs.x), ex2_approx(gl.y - gs.y));
     float2 om[4];
 #pragma unroll
     for (int a2 = 0; a2 < 4; ++a2)
-      om[a2] = a2 > a ? make_float2(__expf(gsA[a2].x - gs.x), __expf(gsA[a2].y - gs.y))
+      om[a2] = a2 > a ? make_float2(ex2_approx(gsA[a2].x - gs.x), ex2_approx(gsA[a2].y - gs.y))
                       : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
-    if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(__expf(gl.x), __expf(gl.y));
+    if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(ex2_approx(gl.x), ex2_approx(gl.y));
 
     // 3. Elementwise operands; every 16-bit operand is stored as a 32-bit pair.
     {
@@ -348,8 +370,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       for (int rr = 0; rr < 8; ++rr) {
         const int r = r0 + rr;
         const float2 gr = G[rr];
-        const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
-        const float f0 = __expf(gs.x - gr.x), f1 = __expf(gs.y - gr.y);   // e^{G_s - G_r} in [1, e^80)
+        const float e0 = ex2_approx(gr.x - gs.x), e1 = ex2_approx(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]: normal
+        const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
         const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
         const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
         const float br = sBeta[r];
