@@ -31,7 +31,7 @@ namespace kda {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restrict__ cu, int32_t num_seqs,
                                                          int64_t T_seq, int64_t total, int32_t* seq_chunk0,
-                                                         int4* chunk_info, int32_t max_chunks,
+                                                         int4* chunk_info, int32_t* seq_order, int32_t max_chunks,
                                                          int32_t* dev_err) {
   __shared__ int32_t s_scan[1024];
   __shared__ int32_t s_carry;
@@ -91,6 +91,22 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restri
     const int64_t t0 = start + (int64_t)(j - seq_chunk0[lo]) * kChunk;
     chunk_info[j] = make_int4(lo, (int32_t)min((int64_t)kChunk, end - t0), (int32_t)(uint32_t)(uint64_t)t0,
                               (int32_t)(uint32_t)((uint64_t)t0 >> 32));
+  }
+  // Launch order of the sequential chains: longest first (ties by index), so
+  // that the longest chains start in the first wave.  Beyond kRankedSeqs
+  // sequences the order is the identity.
+  constexpr int32_t kRankedSeqs = 4096;
+  for (int32_t s = tid; s < num_seqs; s += blockDim.x) {
+    int32_t rank = s;
+    if (num_seqs <= kRankedSeqs) {
+      const int32_t n = seq_chunk0[s + 1] - seq_chunk0[s];
+      rank = 0;
+      for (int32_t t = 0; t < num_seqs; ++t) {
+        const int32_t nt = seq_chunk0[t + 1] - seq_chunk0[t];
+        rank += (nt > n || (nt == n && t < s)) ? 1 : 0;
+      }
+    }
+    seq_order[rank] = s;
   }
 }
 
@@ -417,7 +433,8 @@ Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t
   w.inter_bytes_per_chunk_head = w.tc ? tc_record_bytes(d_k, d_v) : sizeof(float) * inter_floats(d_k, d_v);
   w.off_seq_chunk0 = 0;
   w.off_chunk_info = align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
-  w.off_inter = w.off_chunk_info + align256(sizeof(int4) * (size_t)std::max<int64_t>(max_chunks, 1));
+  w.off_seq_order = w.off_chunk_info + align256(sizeof(int4) * (size_t)std::max<int64_t>(max_chunks, 1));
+  w.off_inter = w.off_seq_order + align256(sizeof(int32_t) * (size_t)std::max<int32_t>(num_seqs, 1));
   const size_t R = (size_t)max_chunks * (size_t)H;
   if (w.tc) {
     w.off_wq = w.off_inter;
@@ -472,12 +489,13 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& p, const Workspace& ws, void* w
   ChunkMap map;
   map.seq_chunk0 = reinterpret_cast<int32_t*>(base + ws.off_seq_chunk0);
   map.chunk_info = reinterpret_cast<int4*>(base + ws.off_chunk_info);
+  map.seq_order = reinterpret_cast<int32_t*>(base + ws.off_seq_order);
   map.max_chunks = ws.max_chunks;
   float* inter = reinterpret_cast<float*>(base + ws.off_inter);
 
   prof_begin(stream, "chunk_map");
   chunk_map_kernel<<<1, 1024, 0, stream>>>(p.cu, p.num_seqs, p.T_seq, p.total_tokens, map.seq_chunk0,
-                                           map.chunk_info, map.max_chunks, p.dev_err);
+                                           map.chunk_info, map.seq_order, map.max_chunks, p.dev_err);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -691,7 +691,9 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
-  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * BV;
+  // one-dimensional grid, sequence-rank major: all blocks of the longest chain first
+  const int blk = (int)(blockIdx.x % (unsigned)(H * (DV / BV)));
+  const int s = map.seq_order[blockIdx.x / (unsigned)(H * (DV / BV))], h = blk / (DV / BV), n0 = (blk % (DV / BV)) * BV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t j0 = map.seq_chunk0[s];
   const int32_t nch = map.seq_chunk0[s + 1] - j0;
@@ -952,7 +954,9 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
-  const int s = blockIdx.x, h = blockIdx.y, n0 = blockIdx.z * NC;
+  // one-dimensional grid, sequence-rank major: all blocks of the longest chain first
+  const int blk = (int)(blockIdx.x % (unsigned)(H * (DV / NC)));
+  const int s = map.seq_order[blockIdx.x / (unsigned)(H * (DV / NC))], h = blk / (DV / NC), n0 = (blk % (DV / NC)) * NC;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t j0 = map.seq_chunk0[s];
   const int32_t nch = map.seq_chunk0[s + 1] - j0;
@@ -1208,7 +1212,7 @@ cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, 
       cudaFuncSetAttribute(chunk_chain_wide_tc<DV, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_wide_tc");
-  chunk_chain_wide_tc<DV, NC><<<dim3(p.num_seqs, p.H, DV / NC), W::kThreads, W::kAlloc, stream>>>(
+  chunk_chain_wide_tc<DV, NC><<<(unsigned)p.num_seqs * p.H * (DV / NC), W::kThreads, W::kAlloc, stream>>>(
       mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
       p.dev_err);
   prof_end(stream);
@@ -1280,7 +1284,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_tc");
-  chunk_chain_tc<DV><<<dim3(p.num_seqs, p.H, DV / BV), kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
+  chunk_chain_tc<DV><<<(unsigned)p.num_seqs * p.H * (DV / BV), kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
       mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
       p.dev_err);
   prof_end(stream);

@@ -44,6 +44,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { retu
 struct ChunkMap {
   int32_t* seq_chunk0;   // [num_seqs + 1] first global chunk of each sequence (exclusive scan)
   int4* chunk_info;      // [max_chunks] per global chunk: (sequence, rows, first token low, high word)
+  int32_t* seq_order;    // [num_seqs] sequences by decreasing chunk count (the chain's launch order)
   int32_t max_chunks;    // upper bound used to size the grid
 };
 
@@ -90,7 +91,7 @@ struct ChunkProblem {
 // separate arrays so that each can be read with 2D TMA tiles.
 struct Workspace {
   size_t bytes;
-  size_t off_seq_chunk0, off_chunk_info, off_inter;
+  size_t off_seq_chunk0, off_chunk_info, off_seq_order, off_inter;
   int32_t max_chunks;
   size_t inter_bytes_per_chunk_head;
   bool tc;
