@@ -138,14 +138,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Byte offset of element (row, col) of a [rows][64] fp16 tile, K-major, 128-byte swizzle.
+__device__ __forceinline__ uint32_t xs_off(int row, int col) { return tc::sw128_offset(row, col); }
+// Byte offset of element (k, n) of the [beta k e^G | beta V] operand: MN-major (n contiguous),
+// 128-byte swizzle, 64-column atoms [64 k][128 B].
+__device__ __forceinline__ uint32_t kv_off(int k, int n) {
+  return (uint32_t)(n >> 6) * 8192u + (uint32_t)k * 128u + (((((uint32_t)n & 63u) >> 3) ^ ((uint32_t)k & 7u)) << 4) +
+         ((uint32_t)n & 7u) * 2u;
+}
+
 // --------------------------------------------------------------- prep kernel
 constexpr int kPrepTcThreads = 512;
 
 template <int DV>
 struct PrepTcSmem {
   static constexpr int LDB = DK + 8;          // 16-bit row stride of the 128-wide operands (272 B)
-  static constexpr int LDKV = DK + DV + 8;    // fp16 row stride of [beta k e^G | beta V]
-  static constexpr int LDX = C + 8;           // fp16 row stride of X
+  static constexpr int LDX = C + 8;           // fp16 row stride of A's off-diagonal blocks
+  static constexpr int kWuN = DK + DV;        // columns of [w | u]
   static constexpr int LDA = C + 1;           // fp32 row stride of A's diagonal blocks
   static constexpr int kCopRows = 16 + 32 + 48 + 64;
   // raw input rows of the next task (TMA, bf16 [64][d]), staged during this one
@@ -158,20 +167,24 @@ struct PrepTcSmem {
   static constexpr size_t oQEl = oQE + (size_t)C * LDB * 2;          // bf16 [64][LDB]  low part
   static constexpr size_t oCop = oQEl + (size_t)C * LDB * 2;         // bf16 [160][LDB] column operands, high part
   static constexpr size_t oCopl = oCop + (size_t)kCopRows * LDB * 2; // bf16 [64][LDB] low part, diagonal blocks
-  static constexpr size_t oKV = oCopl + (size_t)C * LDB * 2;         // fp16 [64][LDKV]
-  static constexpr size_t oTot = oKV + (size_t)C * LDKV * 2;         // fp32 [8][DK] group sums; later P partials
+  // [beta k e^G | beta V], fp16, the B operand of [w | u] = X (...): MN-major,
+  // 128-byte swizzle, 64-column atoms [64 tokens][128 B] of 8 KB
+  static constexpr size_t oKV = (oCopl + (size_t)C * LDB * 2 + 1023) / 1024 * 1024;
+  static constexpr size_t oTot = oKV + (size_t)(kWuN / 64) * 8192;   // fp32 [8][DK] group sums; later P partials
   static constexpr size_t oBeta = oTot + (size_t)8 * DK * 4;         // fp32 [64]
-  static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarrier of the raw rows
-  static constexpr size_t kBytes = oBar + 8;
+  static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarriers: raw rows, [w | u] products
+  static constexpr size_t oTmem = oBar + 16;                          // TMEM base address
+  static constexpr size_t kBytes = oTmem + 8;
   static constexpr size_t kAlloc = kBytes + 1024;                    // slack to align the base to 1 KB
   // reused once A and P are in registers
   static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]  A, diagonal blocks
-  static constexpr size_t oXb = oA + (size_t)C * LDA * 4;             // fp16 [64][LDX]  X
-  static constexpr size_t oAh = oXb + (size_t)C * LDX * 2;           // fp16 [64][LDX]  A, blocks below them
+  // X, fp16 [64][64], K-major with 128-byte swizzle (the A operand of [w | u])
+  static constexpr size_t oXb = (oA + (size_t)C * LDA * 4 + 1023) / 1024 * 1024;
+  static constexpr size_t oAh = oXb + (size_t)C * C * 2;             // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
   static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
   static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
-                    (oXb % 16) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
+                    (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
                 "ldmatrix, mbarrier and TMA alignment");
   static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
 };
@@ -199,8 +212,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
   using L = PrepTcSmem<DV>;
-  constexpr int LDB = L::LDB, LDKV = L::LDKV, LDX = L::LDX, LDA = L::LDA;
+  constexpr int LDB = L::LDB, LDX = L::LDX, LDA = L::LDA;
   constexpr int NTH = kPrepTcThreads;
+  constexpr uint32_t kTmemCols = 256;   // the [w | u] accumulator, M = 64 rows in lanes 32q..32q+15
+  constexpr uint32_t kIdescWU = tc::idesc_f16_f32(64, L::kWuN) | (1u << 16);   // B (KV) MN-major
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   bf16* sKE = reinterpret_cast<bf16*>(smem + L::oKE);
@@ -208,12 +223,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   bf16* sQEl = reinterpret_cast<bf16*>(smem + L::oQEl);
   bf16* sCop = reinterpret_cast<bf16*>(smem + L::oCop);
   bf16* sCopl = reinterpret_cast<bf16*>(smem + L::oCopl);
-  f16* sKV = reinterpret_cast<f16*>(smem + L::oKV);
+  uint8_t* sKV = smem + L::oKV;
   float* sTot = reinterpret_cast<float*>(smem + L::oTot);
   float* sBeta = reinterpret_cast<float*>(smem + L::oBeta);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::oBar);
   float* sA = reinterpret_cast<float*>(smem + L::oA);
-  f16* sXb = reinterpret_cast<f16*>(smem + L::oXb);
+  uint8_t* sX = smem + L::oXb;
   f16* sAh = reinterpret_cast<f16*>(smem + L::oAh);
   f16* sYh = reinterpret_cast<f16*>(smem + L::oYh);
   const bf16* rawG = reinterpret_cast<const bf16*>(smem + L::oRawG);
@@ -224,14 +239,57 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   const int gq = lane >> 2, tq = lane & 3;
 
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(bar, 1);       // raw rows staged
+    tc::mbar_init(bar + 1, 1);   // [w | u] products done
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmG);
     tc::tma_prefetch_desc(&tmK);
     tc::tma_prefetch_desc(&tmQ);
     tc::tma_prefetch_desc(&tmV);
   }
+  if (warp == 0) {
+    tc::tmem_alloc(reinterpret_cast<uint32_t*>(smem + L::oTmem), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
   __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<const uint32_t*>(smem + L::oTmem);
+
+  // [w | u] of a task is multiplied on the tensor cores after its inverse and
+  // read out of TMEM at the start of the next task (or after the last one):
+  // warp w reads rows 16(w%4)..+15 (lanes 32(w%4)..+15) and columns
+  // 64(w/4)..+63, and writes them to the record as fp16.
+  bool wu_pending = false;
+  uint32_t wu_parity = 0;
+  f16* wu_wq = nullptr;
+  f16* wu_u = nullptr;
+  auto wu_drain = [&]() -> bool {
+    if (!wu_pending) return true;
+    const bool okw = tc::mbar_wait(bar + 1, wu_parity, kWaitLimit);
+    wu_parity ^= 1u;
+    wu_pending = false;
+    tc::tc_fence_after();
+    const int qw = warp & 3, cg = warp >> 2;
+    if (64 * cg < L::kWuN) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[32];
+        tc::tmem_ld32(tc::tmem_addr(tmem, (uint32_t)(32 * qw), (uint32_t)(64 * cg + 32 * hf)), v);
+        if (lane < 16 && okw) {
+          const int r = 16 * qw + lane, n = 64 * cg + 32 * hf;
+          f16* dst = n < DK ? wu_wq + r * DK + n : wu_u + r * DV + (n - DK);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4*>(dst)[j] =
+                make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                           pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+      }
+    }
+    tc::tc_fence_before();
+    return okw;
+  };
 
   // Chunk records of this CTA's tasks: one 16-byte load, fetched a task ahead.
   const int32_t n_chunks = map.seq_chunk0[num_seqs];   // negative after malformed cu_seqlens
@@ -247,7 +305,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     if (ci.y > 0 && tid == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)C * (3 * DK + DV) * 2);
   };
   auto issue = [&](int64_t t, int4 ci) {
-    if (ci.y <= 0 || warp < 12 || lane != 0) return;
+    if (ci.y <= 0 || warp < 12 || warp >= 16 || lane != 0) return;
     const int which = warp - 12;
     const CUtensorMap* m = which == 0 ? &tmG : (which == 1 ? &tmK : (which == 2 ? &tmQ : &tmV));
     tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, (int32_t)(t % H), ci.z, bar);
@@ -267,6 +325,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   stage_beta(blockIdx.x, ci_next);
   uint32_t parity = 0;
 
+  bool failed = false;
   // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
     const int4 ci = ci_next;
@@ -295,9 +354,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     if (__syncthreads_or(!ok)) {   // a staging copy never landed: report, drain, stop
       if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
       tc::mbar_wait(bar, parity, kWaitLimit);
-      return;
+      failed = true;
+      break;
     }
     parity ^= 1u;
+    if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the previous task's [w | u]
     float2 G[8];
     {
       float2 run = make_float2(0.f, 0.f);
@@ -389,7 +450,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
           if (a2 > a)
             *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
         }
-        *reinterpret_cast<uint32_t*>(sKV + r * LDKV + c) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
+        *reinterpret_cast<uint32_t*>(sKV + kv_off(r, c)) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
         *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
         const __half2 kt = __floats2half2_rn(kf0 * psi.x, kf1 * psi.y);
         const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
@@ -412,7 +473,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) pk[e] = pack_f16x2(br * __bfloat162float(x[2 * e]), br * __bfloat162float(x[2 * e + 1]));
-        *reinterpret_cast<uint4*>(sKV + r * LDKV + DK + c8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(sKV + kv_off(r, DK + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
     __syncthreads();
@@ -527,7 +588,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         xc[r] = r < jc ? 0.f : accx;
       }
 #pragma unroll
-      for (int r = 0; r < kSub; ++r) sXb[(base + r) * LDX + base + jc] = __float2half_rn(xc[r]);
+      for (int r = 0; r < kSub; ++r) *reinterpret_cast<f16*>(sX + xs_off(base + r, base + jc)) = __float2half_rn(xc[r]);
+    }
+    for (int idx = tid; idx < 6 * 32; idx += NTH) {   // zeros above the block diagonal of X (16-byte chunks)
+      const int blk = idx >> 5, e = idx & 31;
+      const int ra = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int rb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      *reinterpret_cast<uint4*>(sX + xs_off(16 * ra + (e >> 1), 16 * rb + 8 * (e & 1))) = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();
 #pragma unroll
@@ -538,7 +605,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         for (int m = b; m < ab; ++m) {
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
           ldsm_x4(tc::smem_u32(sAh + (16 * ab + (lane & 15)) * LDX + 16 * m + (lane >> 4) * 8), a0, a1, a2, a3);
-          ldsm_x4_t(tc::smem_u32(sXb + (16 * m + (lane & 7) + ((lane >> 3) & 1) * 8) * LDX + 16 * b + (lane >> 4) * 8),
+          ldsm_x4_t(tc::smem_u32(sX + xs_off(16 * m + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * b + (lane >> 4) * 8)),
                     b0, b1, b2, b3);
           mma16816_f16(y[0], a0, a1, a2, a3, b0, b1);
           mma16816_f16(y[1], a0, a1, a2, a3, b2, b3);
@@ -553,63 +620,48 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(tc::smem_u32(sXb + (16 * ab + (lane & 15)) * LDX + 16 * ab + (lane >> 4) * 8), a0, a1, a2, a3);
+          ldsm_x4(tc::smem_u32(sX + xs_off(16 * ab + (lane & 15), 16 * ab + (lane >> 4) * 8)), a0, a1, a2, a3);
           ldsm_x4_t(tc::smem_u32(yb + ((lane & 7) + ((lane >> 3) & 1) * 8) * 24 + (lane >> 4) * 8), b0, b1, b2, b3);
           mma16816_f16(x[0], a0, a1, a2, a3, b0, b1);
           mma16816_f16(x[1], a0, a1, a2, a3, b2, b3);
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          *reinterpret_cast<uint32_t*>(sXb + (16 * ab + gq) * LDX + 16 * b + 8 * nt + 2 * tq) =
+          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ab + gq, 16 * b + 8 * nt + 2 * tq)) =
               pack_f16x2(-x[nt][0], -x[nt][1]);
-          *reinterpret_cast<uint32_t*>(sXb + (16 * ab + gq + 8) * LDX + 16 * b + 8 * nt + 2 * tq) =
+          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ab + gq + 8, 16 * b + 8 * nt + 2 * tq)) =
               pack_f16x2(-x[nt][2], -x[nt][3]);
         }
       }
       __syncthreads();
     }
 
-    // 7. [w | u] = X [beta k e^G | beta V]: warp -> 16 rows (mt) x a quarter of the columns
-    {
-      constexpr int NQ = (DK + DV) / 4;   // 64 or 48 columns per warp
-      constexpr int NT = NQ / 8;
-      const int mt = warp & 3, nq = warp >> 2;
-      float accw[NT][4];
+    // 7. [w | u] = X [beta k e^G | beta V] on the tensor cores (M = 64, N = d_k + d_v,
+    //    K = 64; fp32 accumulator in TMEM), read out at the start of the next task.
+    tc::fence_proxy_async_smem();   // X and the operand written by the threads, seen by the MMAs
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (tid == 0) {
+      const uint64_t dX = tc::desc_kmajor_sw128(tc::smem_u32(sX));
+      const uint64_t dKV = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sKV), 8192);
+      tc::mma_16bit_first(tmem, dX, dKV, kIdescWU);
 #pragma unroll
-      for (int i = 0; i < NT; ++i) accw[i][0] = accw[i][1] = accw[i][2] = accw[i][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (ks <= mt) {   // X is lower triangular by 16-row blocks
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(tc::smem_u32(sXb + (16 * mt + (lane & 15)) * LDX + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
-#pragma unroll
-          for (int np = 0; np < NT / 2; ++np) {
-            const int n0 = nq * NQ + 16 * np;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(tc::smem_u32(sKV + (16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8) * LDKV + n0 + (lane >> 4) * 8),
-                      b0, b1, b2, b3);
-            mma16816_f16(accw[2 * np], a0, a1, a2, a3, b0, b1);
-            mma16816_f16(accw[2 * np + 1], a0, a1, a2, a3, b2, b3);
-          }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int n = nq * NQ + 8 * nt + 2 * tq;
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = 16 * mt + gq + 8 * hr;
-          const uint32_t pv = pack_f16x2(accw[nt][2 * hr], accw[nt][2 * hr + 1]);
-          if (n < DK)
-            *reinterpret_cast<uint32_t*>(o_wq + r * DK + n) = pv;
-          else
-            *reinterpret_cast<uint32_t*>(o_u + r * DV + (n - DK)) = pv;
-        }
-      }
+      for (int kk = 1; kk < C / 16; ++kk)
+        tc::mma_16bit_acc(tmem, dX + ((kk * 32) >> 4), dKV + ((kk * 2048) >> 4), kIdescWU);
+      tc::mma_commit(bar + 1);
     }
+    wu_pending = true;
+    wu_wq = o_wq;
+    wu_u = o_u;
     __syncthreads();   // shared memory is reused by the next task
   }
   cp_async_wait_all();
+  if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
+  (void)failed;
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // -------------------------------------------------------------- chain kernel

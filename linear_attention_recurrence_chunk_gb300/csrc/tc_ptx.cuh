@@ -195,6 +195,19 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw64_atoms(uint32_t addr, uint3
   return d;
 }
 
+// MN-major 16-bit operand with 128-byte swizzle: 64-element MN atoms of
+// [K rows][128 B] (16-byte chunk index XOR-ed with k % 8), `atom_stride` bytes
+// apart; K slices of 16 rows are 2048 bytes apart.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128_atoms(uint32_t addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);               // start address >> 4
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: MN atom stride
+  d |= (uint64_t)(1024u >> 4) << 32;                    // stride byte offset: 8 K rows x 128 B
+  d |= (uint64_t)1u << 46;                              // descriptor version 1
+  d |= (uint64_t)2u << 61;                              // 128-byte swizzle
+  return d;
+}
+
 // Byte offset of the 16-byte chunk j (MN elements 8j..8j+7) of K row k in that layout.
 __host__ __device__ __forceinline__ uint32_t sw64_chunk_offset(uint32_t k, uint32_t j) {
   return k * 64u + (((j ^ (k >> 1)) & 3u) << 4);
