@@ -183,6 +183,7 @@ struct PrepTcSmem {
   static constexpr size_t oAh = oXb + (size_t)C * C * 2;             // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
   static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
+  static_assert(oKE + (size_t)C * (kWuN * 2 + 16) <= oKV, "the [w | u] staging tile fits the operand area");
   static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
                     (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
                 "ldmatrix, mbarrier and TMA alignment");
@@ -258,36 +259,48 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 
   // [w | u] of a task is multiplied on the tensor cores after its inverse and
   // read out of TMEM at the start of the next task (or after the last one):
-  // warp w reads rows 16(w%4)..+15 (lanes 32(w%4)..+15) and columns
-  // 64(w/4)..+63, and writes them to the record as fp16.
+  // warp w takes rows 16(w%4)..+15 (lanes 32(w%4)..+15) and columns
+  // 64(w/4)..+63 into a row-major fp16 tile in the (then free) operand area,
+  // which all threads then copy to the record with coalesced 16-byte stores.
   bool wu_pending = false;
   uint32_t wu_parity = 0;
   f16* wu_wq = nullptr;
   f16* wu_u = nullptr;
+  constexpr int kStg = L::kWuN * 2 + 16;   // staging row stride in bytes (padded against bank conflicts)
   auto wu_drain = [&]() -> bool {
     if (!wu_pending) return true;
     const bool okw = tc::mbar_wait(bar + 1, wu_parity, kWaitLimit);
     wu_parity ^= 1u;
     wu_pending = false;
     tc::tc_fence_after();
+    uint8_t* stg = smem + L::oKE;
     const int qw = warp & 3, cg = warp >> 2;
     if (64 * cg < L::kWuN) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float v[32];
         tc::tmem_ld32(tc::tmem_addr(tmem, (uint32_t)(32 * qw), (uint32_t)(64 * cg + 32 * hf)), v);
-        if (lane < 16 && okw) {
-          const int r = 16 * qw + lane, n = 64 * cg + 32 * hf;
-          f16* dst = n < DK ? wu_wq + r * DK + n : wu_u + r * DV + (n - DK);
+        if (lane < 16) {
+          uint4* dst = reinterpret_cast<uint4*>(stg + (16 * qw + lane) * kStg + (64 * cg + 32 * hf) * 2);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            reinterpret_cast<uint4*>(dst)[j] =
-                make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
-                           pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
+            dst[j] = make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                                pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
         }
       }
     }
     tc::tc_fence_before();
+    __syncthreads();
+    constexpr int kVec = L::kWuN / 8;   // 16-byte vectors per row
+    for (int idx = tid; idx < C * kVec && okw; idx += NTH) {
+      const int r = idx / kVec, n = (idx % kVec) * 8;
+      const uint4 x = *reinterpret_cast<const uint4*>(stg + r * kStg + n * 2);
+      if (n < DK)
+        *reinterpret_cast<uint4*>(wu_wq + r * DK + n) = x;
+      else
+        *reinterpret_cast<uint4*>(wu_u + r * DV + (n - DK)) = x;
+    }
+    __syncthreads();   // the staging tile is reused by the operands of the next task
     return okw;
   };
 
