@@ -178,12 +178,12 @@ struct PrepTcSmem {
   static constexpr size_t kAlloc = kBytes + 1024;                    // slack to align the base to 1 KB
   // reused once A and P are in registers
   static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]  A, diagonal blocks
-  // X, fp16 [64][64], K-major with 128-byte swizzle (the A operand of [w | u])
+  // X, fp16 [128][64] (rows 64-127 zero), K-major with 128-byte swizzle: the A operand of [w | u]
   static constexpr size_t oXb = (oA + (size_t)C * LDA * 4 + 1023) / 1024 * 1024;
-  static constexpr size_t oAh = oXb + (size_t)C * C * 2;             // fp16 [64][LDX]  A, blocks below them
+  static constexpr size_t oAh = oXb + (size_t)2 * C * C * 2;         // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
   static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
-  static_assert(oKE + (size_t)C * (kWuN * 2 + 16) <= oKV, "the [w | u] staging tile fits the operand area");
+  static_assert(oKE + (size_t)(kWuN / 64) * 8192 <= oKV && (oKE % 1024) == 0, "the [w | u] tiles fit the operand area");
   static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
                     (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
                 "ldmatrix, mbarrier and TMA alignment");
@@ -210,13 +210,14 @@ template <int DV>
 __global__ void __launch_bounds__(kPrepTcThreads, 1)
     chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
   using L = PrepTcSmem<DV>;
   constexpr int LDB = L::LDB, LDX = L::LDX, LDA = L::LDA;
   constexpr int NTH = kPrepTcThreads;
-  constexpr uint32_t kTmemCols = 256;   // the [w | u] accumulator, M = 64 rows in lanes 32q..32q+15
-  constexpr uint32_t kIdescWU = tc::idesc_f16_f32(64, L::kWuN) | (1u << 16);   // B (KV) MN-major
+  constexpr uint32_t kTmemCols = 256;   // the [w | u] accumulator: rows 0-63 in TMEM lanes 0-63
+  constexpr uint32_t kIdescWU = tc::idesc_f16_f32(128, L::kWuN) | (1u << 16);   // B (KV) MN-major
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   bf16* sKE = reinterpret_cast<bf16*>(smem + L::oKE);
@@ -259,48 +260,48 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 
   // [w | u] of a task is multiplied on the tensor cores after its inverse and
   // read out of TMEM at the start of the next task (or after the last one):
-  // warp w takes rows 16(w%4)..+15 (lanes 32(w%4)..+15) and columns
-  // 64(w/4)..+63 into a row-major fp16 tile in the (then free) operand area,
-  // which all threads then copy to the record with coalesced 16-byte stores.
-  bool wu_pending = false;
+  // the warps of lane quarters 0 and 1 take rows 32(w%4)..+31 and columns
+  // 64(w/4)..+63 into 64-column tiles (128-byte swizzle) in the then free
+  // operand area, which thread 0 stores to the record with TMA; the tiles are
+  // released (bulk read wait) before the operand area is rewritten.
+  bool wu_pending = false, wu_storing = false;
   uint32_t wu_parity = 0;
-  f16* wu_wq = nullptr;
-  f16* wu_u = nullptr;
-  constexpr int kStg = L::kWuN * 2 + 16;   // staging row stride in bytes (padded against bank conflicts)
+  int64_t wu_rec = 0;
   auto wu_drain = [&]() -> bool {
     if (!wu_pending) return true;
     const bool okw = tc::mbar_wait(bar + 1, wu_parity, kWaitLimit);
     wu_parity ^= 1u;
     wu_pending = false;
     tc::tc_fence_after();
-    uint8_t* stg = smem + L::oKE;
+    uint8_t* stg = smem + L::oKE;   // tile t (columns 64t..64t+63) at stg + 8 KB * t
     const int qw = warp & 3, cg = warp >> 2;
-    if (64 * cg < L::kWuN) {
+    if (qw < 2 && 64 * cg < L::kWuN) {
+      const int r = 32 * qw + lane;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float v[32];
         tc::tmem_ld32(tc::tmem_addr(tmem, (uint32_t)(32 * qw), (uint32_t)(64 * cg + 32 * hf)), v);
-        if (lane < 16) {
-          uint4* dst = reinterpret_cast<uint4*>(stg + (16 * qw + lane) * kStg + (64 * cg + 32 * hf) * 2);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
-                                pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
-        }
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(stg + cg * 8192 + xs_off(r, 32 * hf + 8 * j)) =
+              make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                         pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
       }
     }
+    tc::fence_proxy_async_smem();   // the tiles, written by the threads, read by the TMA unit
     tc::tc_fence_before();
     __syncthreads();
-    constexpr int kVec = L::kWuN / 8;   // 16-byte vectors per row
-    for (int idx = tid; idx < C * kVec && okw; idx += NTH) {
-      const int r = idx / kVec, n = (idx % kVec) * 8;
-      const uint4 x = *reinterpret_cast<const uint4*>(stg + r * kStg + n * 2);
-      if (n < DK)
-        *reinterpret_cast<uint4*>(wu_wq + r * DK + n) = x;
-      else
-        *reinterpret_cast<uint4*>(wu_u + r * DV + (n - DK)) = x;
+    if (tid == 0 && okw) {
+#pragma unroll
+      for (int t = 0; t < L::kWuN / 64; ++t) {
+        if (t < DK / 64)
+          tc::tma_store_2d(&tmWs, 64 * t, (int32_t)(wu_rec * 128), stg + t * 8192);
+        else
+          tc::tma_store_2d(&tmUs, 64 * (t - DK / 64), (int32_t)(wu_rec * C), stg + t * 8192);
+      }
+      tc::bulk_commit();
+      wu_storing = true;
     }
-    __syncthreads();   // the staging tile is reused by the operands of the next task
     return okw;
   };
 
@@ -355,7 +356,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     f16* o_wq = out.wq + rec * 128 * DK;
     f16* o_p = out.p + rec * C * C;
     f16* o_kt = out.kt + rec * DK * C;
-    f16* o_u = out.u + rec * C * DV;
     float* o_gam = out.gam + rec * DK;
 
     // 1. Thread -> channel pair (c, c+1) and the 8 rows r0..r0+7 of sub-tile a.
@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
     }
     arm(ci_next);
+    if (wu_storing) {   // thread 0: the previous [w | u] tiles have been read by the TMA unit
+      tc::bulk_wait_read0();
+      wu_storing = false;
+    }
     __syncthreads();   // every raw read is done; the group sums are visible
     issue(task + gridDim.x, ci_next);
 
@@ -609,6 +613,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       const int rb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
       *reinterpret_cast<uint4*>(sX + xs_off(16 * ra + (e >> 1), 16 * rb + 8 * (e & 1))) = make_uint4(0u, 0u, 0u, 0u);
     }
+    for (int idx = tid; idx < C * 8; idx += NTH)   // rows 64-127 of the MMA's A tile are zero
+      *reinterpret_cast<uint4*>(sX + C * 128 + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 #pragma unroll
     for (int ab = 1; ab < C / kSub; ++ab) {
@@ -665,12 +671,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       tc::mma_commit(bar + 1);
     }
     wu_pending = true;
-    wu_wq = o_wq;
-    wu_u = o_u;
+    wu_rec = rec;
     __syncthreads();   // shared memory is reused by the next task
   }
   cp_async_wait_all();
   if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
+  if (wu_storing) tc::bulk_wait0();   // thread 0: every record store has completed
   (void)failed;
   tc::tc_fence_before();
   __syncthreads();
@@ -1309,6 +1315,10 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     if (!make_input_map(&mG, p.g, DK, p.H, tok) || !make_input_map(&mK, p.k, DK, p.H, tok) ||
         !make_input_map(&mQ, p.q, DK, p.H, tok) || !make_input_map(&mV, p.v, DV, p.H, tok))
       return cudaErrorInvalidValue;
+    CUtensorMap mWs, mUs;   // [w | u] record stores: 64 x 64 boxes, 128-byte swizzle
+    if (!make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, R * 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mUs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
     const size_t smem = PrepTcSmem<DV>::kAlloc;
     e = cudaFuncSetAttribute(chunk_prep_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1318,7 +1328,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
     const int grid = (int)std::min<int64_t>(n_tasks, sms);
     prof_begin(stream, "chunk_prep_tc");
-    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, p.beta, p.num_seqs, p.H, map, rec,
+    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, mWs, mUs, p.beta, p.num_seqs, p.H, map, rec,
                                                               n_tasks, p.dev_err);
     prof_end(stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
