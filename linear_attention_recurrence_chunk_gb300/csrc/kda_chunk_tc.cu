@@ -100,11 +100,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(tc::smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
 // (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
@@ -305,50 +300,56 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     return okw;
   };
 
-  // Chunk records of this CTA's tasks: one 16-byte load, fetched a task ahead.
+  // This CTA's tasks are blockIdx.x + i * gridDim.x; (chunk, head) of the
+  // next one are tracked incrementally, without 64-bit divisions.
   const int32_t n_chunks = map.seq_chunk0[num_seqs];   // negative after malformed cu_seqlens
-  auto fetch = [&](int64_t t) -> int4 {
-    return (t < n_tasks && t / H < n_chunks) ? map.chunk_info[t / H] : make_int4(0, 0, 0, 0);
+  const int32_t dj = (int32_t)(gridDim.x / (unsigned)H), dh = (int32_t)(gridDim.x % (unsigned)H);
+  int32_t j_next = (int32_t)(blockIdx.x / (unsigned)H), h_next = (int32_t)(blockIdx.x % (unsigned)H);
+  // Chunk record of a task: one 16-byte load, fetched a task ahead.
+  auto fetch = [&](int64_t t, int32_t jt) -> int4 {
+    return (t < n_tasks && jt < n_chunks) ? map.chunk_info[jt] : make_int4(0, 0, 0, 0);
   };
   // Staging of a task's raw rows: 64 tokens of one head of g, k, q, v by TMA
   // (zero-filled past the token array; rows past the sequence end are masked
-  // by the gate and by beta = 0) and beta by cp.async.  The barrier is armed
-  // by thread 0 before the CTA barrier that precedes the four copies, which
-  // lanes 0 of warps 12-15 issue.
+  // by the gate and by beta = 0).  The barrier is armed by thread 0 before the
+  // CTA barrier that precedes the four copies, which lanes 0 of warps 12-15
+  // issue.  beta is loaded a task ahead into a register of threads 0-63.
   auto arm = [&](int4 ci) {
     if (ci.y > 0 && tid == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)C * (3 * DK + DV) * 2);
   };
-  auto issue = [&](int64_t t, int4 ci) {
+  auto issue = [&](int32_t ht, int4 ci) {
     if (ci.y <= 0 || warp < 12 || warp >= 16 || lane != 0) return;
     const int which = warp - 12;
     const CUtensorMap* m = which == 0 ? &tmG : (which == 1 ? &tmK : (which == 2 ? &tmQ : &tmV));
-    tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, (int32_t)(t % H), ci.z, bar);
+    tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, ht, ci.z, bar);
   };
-  auto stage_beta = [&](int64_t t, int4 ci) {
-    if (ci.y <= 0) return;
-    if (tid < C) {
-      const bool ok = tid < ci.y;
-      cp_async4(sBeta + tid, ok ? beta + ((int64_t)ci.z + tid) * H + t % H : beta, ok ? 4u : 0u);
-    }
-    cp_async_commit();
+  auto load_beta = [&](int32_t ht, int4 ci) -> float {
+    return (tid < ci.y) ? beta[((int64_t)(uint32_t)ci.z + tid) * H + ht] : 0.f;   // ci.y <= 64
   };
-  int4 ci_next = fetch(blockIdx.x);
+  int4 ci_next = fetch(blockIdx.x, j_next);
+  float beta_next = tid < C ? load_beta(h_next, ci_next) : 0.f;
   arm(ci_next);
   __syncthreads();
-  issue(blockIdx.x, ci_next);
-  stage_beta(blockIdx.x, ci_next);
+  issue(h_next, ci_next);
   uint32_t parity = 0;
 
   bool failed = false;
   // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
     const int4 ci = ci_next;
-    ci_next = fetch(task + gridDim.x);
+    const float beta_cur = beta_next;
+    j_next += dj;
+    h_next += dh;
+    if (h_next >= H) {
+      h_next -= H;
+      ++j_next;
+    }
+    ci_next = fetch(task + gridDim.x, j_next);
     if (ci.y <= 0) {
+      if (tid < C) beta_next = load_beta(h_next, ci_next);
       arm(ci_next);
       __syncthreads();
-      issue(task + gridDim.x, ci_next);
-      stage_beta(task + gridDim.x, ci_next);
+      issue(h_next, ci_next);
       continue;
     }
     const int len = ci.y;
@@ -362,7 +363,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     //    Gate and inclusive cumulative sum over the thread's rows, in registers;
     //    the raw k, q, v of the thread are read before the area is reused.
     const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2, r0 = 8 * rg;
-    cp_async_wait_all();   // beta
+    if (tid < C) sBeta[tid] = beta_cur;   // visible after the next CTA barrier
     const bool ok = tc::mbar_wait(bar, parity, kWaitLimit);
     if (__syncthreads_or(!ok)) {   // a staging copy never landed: report, drain, stop
       if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       wu_storing = false;
     }
     __syncthreads();   // every raw read is done; the group sums are visible
-    issue(task + gridDim.x, ci_next);
+    issue(h_next, ci_next);
 
     // 2. Offsets from the group sums: G_s(a') = cumulative decay before sub-tile
     //    a', G_last; then per-thread factors e^{G_s(a)}, e^{G_last - G_s(a)},
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       }
     }
     __syncthreads();
-    stage_beta(task + gridDim.x, ci_next);   // beta is no longer read by this task
+    if (tid < C) beta_next = load_beta(h_next, ci_next);
 
     // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
     //    diagonal 16x16 blocks (only their strictly lower parts are read) by
@@ -674,7 +675,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     wu_rec = rec;
     __syncthreads();   // shared memory is reused by the next task
   }
-  cp_async_wait_all();
   if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
   if (wu_storing) tc::bulk_wait0();   // thread 0: every record store has completed
   (void)failed;
