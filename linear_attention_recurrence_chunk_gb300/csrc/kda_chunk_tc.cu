@@ -133,6 +133,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Global loads issued where they stand (the compiler may not sink them to the
+// first use), for values needed a task later.
+__device__ __forceinline__ float ld_early_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int4 ld_early_v4(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 // Byte offset of element (row, col) of a [rows][64] fp16 tile, K-major, 128-byte swizzle.
 __device__ __forceinline__ uint32_t xs_off(int row, int col) { return tc::sw128_offset(row, col); }
 // Byte offset of element (k, n) of the [beta k e^G | beta V] operand: MN-major (n contiguous),
@@ -165,7 +178,8 @@ struct PrepTcSmem {
   // [beta k e^G | beta V], fp16, the B operand of [w | u] = X (...): MN-major,
   // 128-byte swizzle, 64-column atoms [64 tokens][128 B] of 8 KB
   static constexpr size_t oKV = (oCopl + (size_t)C * LDB * 2 + 1023) / 1024 * 1024;
-  static constexpr size_t oTot = oKV + (size_t)(kWuN / 64) * 8192;   // fp32 [8][DK] group sums; later P partials
+  static constexpr size_t oPst = oKV + (size_t)(kWuN / 64) * 8192;   // fp16 [64][64] P, 128-byte swizzle (TMA store)
+  static constexpr size_t oTot = oPst + (size_t)C * C * 2;           // fp32 [8][DK] group sums; later P partials
   static constexpr size_t oBeta = oTot + (size_t)8 * DK * 4;         // fp32 [64]
   static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarriers: raw rows, [w | u] products
   static constexpr size_t oTmem = oBar + 16;                          // TMEM base address
@@ -206,6 +220,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
+                  const __grid_constant__ CUtensorMap tmPs,
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
   using L = PrepTcSmem<DV>;
@@ -221,6 +236,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   bf16* sCop = reinterpret_cast<bf16*>(smem + L::oCop);
   bf16* sCopl = reinterpret_cast<bf16*>(smem + L::oCopl);
   uint8_t* sKV = smem + L::oKV;
+  uint8_t* sPst = smem + L::oPst;
   float* sTot = reinterpret_cast<float*>(smem + L::oTot);
   float* sBeta = reinterpret_cast<float*>(smem + L::oBeta);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::oBar);
@@ -259,7 +275,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   // 64(w/4)..+63 into 64-column tiles (128-byte swizzle) in the then free
   // operand area, which thread 0 stores to the record with TMA; the tiles are
   // released (bulk read wait) before the operand area is rewritten.
-  bool wu_pending = false, wu_storing = false;
+  bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
   uint32_t wu_parity = 0;
   int64_t wu_rec = 0;
   auto wu_drain = [&]() -> bool {
@@ -295,25 +311,34 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
           tc::tma_store_2d(&tmUs, 64 * (t - DK / 64), (int32_t)(wu_rec * C), stg + t * 8192);
       }
       tc::bulk_commit();
-      wu_storing = true;
+      bulk_pending = true;
     }
     return okw;
   };
 
   // This CTA's tasks are blockIdx.x + i * gridDim.x; (chunk, head) of the
-  // next one are tracked incrementally, without 64-bit divisions.
+  // next two are tracked incrementally, without 64-bit divisions.
   const int32_t n_chunks = map.seq_chunk0[num_seqs];   // negative after malformed cu_seqlens
   const int32_t dj = (int32_t)(gridDim.x / (unsigned)H), dh = (int32_t)(gridDim.x % (unsigned)H);
   int32_t j_next = (int32_t)(blockIdx.x / (unsigned)H), h_next = (int32_t)(blockIdx.x % (unsigned)H);
-  // Chunk record of a task: one 16-byte load, fetched a task ahead.
+  auto advance = [&](int32_t& jt, int32_t& ht) {
+    jt += dj;
+    ht += dh;
+    if (ht >= H) {
+      ht -= H;
+      ++jt;
+    }
+  };
+  // Chunk record of a task: one 16-byte load, fetched two tasks ahead.
   auto fetch = [&](int64_t t, int32_t jt) -> int4 {
-    return (t < n_tasks && jt < n_chunks) ? map.chunk_info[jt] : make_int4(0, 0, 0, 0);
+    return (t < n_tasks && jt < n_chunks) ? ld_early_v4(map.chunk_info + jt) : make_int4(0, 0, 0, 0);
   };
   // Staging of a task's raw rows: 64 tokens of one head of g, k, q, v by TMA
   // (zero-filled past the token array; rows past the sequence end are masked
   // by the gate and by beta = 0).  The barrier is armed by thread 0 before the
   // CTA barrier that precedes the four copies, which lanes 0 of warps 12-15
-  // issue.  beta is loaded a task ahead into a register of threads 0-63.
+  // issue.  beta of the next task is loaded into a register of threads 0-63
+  // at the start of the current one.
   auto arm = [&](int4 ci) {
     if (ci.y > 0 && tid == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)C * (3 * DK + DV) * 2);
   };
@@ -324,10 +349,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, ht, ci.z, bar);
   };
   auto load_beta = [&](int32_t ht, int4 ci) -> float {
-    return (tid < ci.y) ? beta[((int64_t)(uint32_t)ci.z + tid) * H + ht] : 0.f;   // ci.y <= 64
+    return (tid < ci.y) ? ld_early_f32(beta + ((int64_t)(uint32_t)ci.z + tid) * H + ht) : 0.f;   // ci.y <= 64
   };
   int4 ci_next = fetch(blockIdx.x, j_next);
   float beta_next = tid < C ? load_beta(h_next, ci_next) : 0.f;
+  int32_t j_next2 = j_next, h_next2 = h_next;
+  advance(j_next2, h_next2);
+  int4 ci_next2 = fetch((int64_t)blockIdx.x + gridDim.x, j_next2);
   arm(ci_next);
   __syncthreads();
   issue(h_next, ci_next);
@@ -338,15 +366,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
     const int4 ci = ci_next;
     const float beta_cur = beta_next;
-    j_next += dj;
-    h_next += dh;
-    if (h_next >= H) {
-      h_next -= H;
-      ++j_next;
-    }
-    ci_next = fetch(task + gridDim.x, j_next);
+    ci_next = ci_next2;   // the next task (record fetched a task ago)
+    j_next = j_next2;
+    h_next = h_next2;
+    if (tid < C) beta_next = load_beta(h_next, ci_next);
+    advance(j_next2, h_next2);
+    ci_next2 = fetch(task + 2 * (int64_t)gridDim.x, j_next2);
     if (ci.y <= 0) {
-      if (tid < C) beta_next = load_beta(h_next, ci_next);
       arm(ci_next);
       __syncthreads();
       issue(h_next, ci_next);
@@ -355,7 +381,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     const int len = ci.y;
     const int64_t rec = task;   // == j * H + h
     f16* o_wq = out.wq + rec * 128 * DK;
-    f16* o_p = out.p + rec * C * C;
     f16* o_kt = out.kt + rec * DK * C;
     float* o_gam = out.gam + rec * DK;
 
@@ -401,9 +426,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
     }
     arm(ci_next);
-    if (wu_storing) {   // thread 0: the previous [w | u] tiles have been read by the TMA unit
+    if (bulk_pending) {   // thread 0: the P and [w | u] tiles stored so far have been read by the TMA unit
       tc::bulk_wait_read0();
-      wu_storing = false;
+      bulk_pending = false;
     }
     __syncthreads();   // every raw read is done; the group sums are visible
     issue(h_next, ci_next);
@@ -542,7 +567,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
           const int r = 16 * a + gq + 8 * hr;
-          *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(acc[jb][nt][2 * hr], acc[jb][nt][2 * hr + 1]);
+          *reinterpret_cast<uint32_t*>(sPst + xs_off(r, i0)) = pack_f16x2(acc[jb][nt][2 * hr], acc[jb][nt][2 * hr + 1]);
         }
       }
     }
@@ -550,7 +575,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       const int blk = idx >> 7, e = idx & 127;
       const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
       const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      *reinterpret_cast<uint32_t*>(o_p + (16 * a + (e >> 3)) * C + 16 * b + (e & 7) * 2) = 0u;
+      *reinterpret_cast<uint32_t*>(sPst + xs_off(16 * a + (e >> 3), 16 * b + (e & 7) * 2)) = 0u;
     }
     __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
 #pragma unroll
@@ -565,7 +590,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
             const int r = 16 * a + gq + 8 * hr;
             const float v0 = acc[jb][nt][2 * hr] + sPart[((a * 2 + nt) * 4 + 2 * hr) * 32 + lane];
             const float v1 = acc[jb][nt][2 * hr + 1] + sPart[((a * 2 + nt) * 4 + 2 * hr + 1) * 32 + lane];
-            *reinterpret_cast<uint32_t*>(o_p + r * C + i0) = pack_f16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
+            *reinterpret_cast<uint32_t*>(sPst + xs_off(r, i0)) = pack_f16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
           }
         }
       }
@@ -587,8 +612,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         }
       }
     }
+    tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     __syncthreads();
-    if (tid < C) beta_next = load_beta(h_next, ci_next);
+    if (tid == 0) {   // P to the record (the tile is released at the next task's first CTA barrier)
+      tc::tma_store_2d(&tmPs, 0, (int32_t)(rec * C), sPst);
+      tc::bulk_commit();
+      bulk_pending = true;
+    }
 
     // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
     //    diagonal 16x16 blocks (only their strictly lower parts are read) by
@@ -676,7 +706,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     __syncthreads();   // shared memory is reused by the next task
   }
   if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
-  if (wu_storing) tc::bulk_wait0();   // thread 0: every record store has completed
+  if (bulk_pending) tc::bulk_wait0();   // thread 0: every record store has completed
   (void)failed;
   tc::tc_fence_before();
   __syncthreads();
@@ -1315,9 +1345,10 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     if (!make_input_map(&mG, p.g, DK, p.H, tok) || !make_input_map(&mK, p.k, DK, p.H, tok) ||
         !make_input_map(&mQ, p.q, DK, p.H, tok) || !make_input_map(&mV, p.v, DV, p.H, tok))
       return cudaErrorInvalidValue;
-    CUtensorMap mWs, mUs;   // [w | u] record stores: 64 x 64 boxes, 128-byte swizzle
+    CUtensorMap mWs, mUs, mPs;   // record stores of [w | u] and P: 64 x 64 boxes, 128-byte swizzle
     if (!make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, R * 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&mUs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&mUs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&mPs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     const size_t smem = PrepTcSmem<DV>::kAlloc;
     e = cudaFuncSetAttribute(chunk_prep_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1328,7 +1359,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
     const int grid = (int)std::min<int64_t>(n_tasks, sms);
     prof_begin(stream, "chunk_prep_tc");
-    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, mWs, mUs, p.beta, p.num_seqs, p.H, map, rec,
+    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, mWs, mUs, mPs, p.beta, p.num_seqs, p.H, map, rec,
                                                               n_tasks, p.dev_err);
     prof_end(stream);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
