@@ -209,13 +209,13 @@ def dist_setup(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
     if ws > 1 and args.impl == "kda":
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", init_method="env://")
-    elif torch.cuda.is_available():
-        torch.cuda.set_device(local)
+        # one process per GPU over NCCL; gloo where there is no GPU (host-side tests)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo", init_method="env://")
     return ws, rank, local
 
 
@@ -232,9 +232,20 @@ def max_over_ranks(x: float, ws: int) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def min_over_ranks(x: float, ws: int) -> float:
+    return -max_over_ranks(-x, ws)
+
+
+def job_throughput(units_per_rank: float, steps: int, max_ms: float, ws: int) -> float:
+    """Whole-job units/s under weak scaling: every rank processes the same
+    units per step; the job takes as long as its slowest rank."""
+    return ws * units_per_rank * steps / (max_ms / 1e3)
 
 
 def bench_prefill(args, ws_size, local):
@@ -455,7 +466,7 @@ def main():
     r = bench_prefill(args, ws_size, local)
     w = r["w"]
     steps = args.steps
-    value = ws_size * w.tokens * steps / (r["max_ms"] / 1e3)
+    value = job_throughput(w.tokens, steps, r["max_ms"], ws_size)
 
     # dominant kernel = largest total time in the timed region
     totals = {k: sum(v) for k, v in r["per_kernel"].items()}
@@ -489,7 +500,7 @@ def main():
     if not args.no_e2e:
         line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
         if ws_size > 1:
-            line["e2e"]["value"] = max_over_ranks(-line["e2e"]["value"], ws_size) * -1 * ws_size
+            line["e2e"]["value"] = min_over_ranks(line["e2e"]["value"], ws_size) * ws_size
     del r
     torch.cuda.empty_cache()
     if not args.no_decode:

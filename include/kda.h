@@ -127,6 +127,18 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
 KDA_API kda_status kda_device_error(cudaStream_t stream, int32_t* code);
 
 /*
+ * Failure-detection check (the pages have no counterpart).  Launches one small
+ * kernel on `stream` that waits on a shared-memory mbarrier nothing ever
+ * arrives at, with the same bounded wait the tensor-core kernels use, limited
+ * to `limit_cycles` SM clock cycles (1 .. 1e9).  When the limit runs out the
+ * kernel sets this device's error word and returns, so that a following
+ * kda_device_error() reports KDA_ERR_DEVICE_TIMEOUT and the CUDA context stays
+ * usable.  Returns KDA_ERR_INVALID_ARG for a limit out of range (nothing is
+ * launched) and KDA_ERR_CUDA if the launch fails.
+ */
+KDA_API kda_status kda_check_wait_timeout(int64_t limit_cycles, cudaStream_t stream);
+
+/*
  * Allocation-free variant of kda_chunk_fwd (the pages have no counterpart).
  *
  * For callers that cannot call cudaMalloc, for example a serving engine that

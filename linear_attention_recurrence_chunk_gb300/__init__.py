@@ -14,7 +14,8 @@ Functions keep the C names:
   beta ``[B, T, H]`` fp32, states ``[S, H, d_k, d_v]`` fp32.
 * ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
   sequence (same page §3.2), state updated in place.
-* ``kda_chunk_fwd_workspace_size(...)``, ``kda_device_error()``.
+* ``kda_chunk_fwd_workspace_size(...)``, ``kda_device_error()``,
+  ``kda_check_wait_timeout(limit_cycles)`` (failure-detection check).
 """
 from __future__ import annotations
 
@@ -27,7 +28,7 @@ import torch
 from . import _build
 
 __all__ = ["kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
-           "KdaError", "library_path", "load_library", "STATUS"]
+           "kda_check_wait_timeout", "KdaError", "library_path", "load_library", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
           4: "KDA_ERR_DEVICE_TIMEOUT"}
@@ -69,6 +70,8 @@ def load_library():
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.kda_device_error.restype = ctypes.c_int
+    lib.kda_check_wait_timeout.argtypes = [i64, vp]
+    lib.kda_check_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -150,3 +153,9 @@ def kda_device_error(stream=None) -> Tuple[int, int]:
     code = ctypes.c_int32(0)
     st = load_library().kda_device_error(_stream(stream), ctypes.byref(code))
     return int(st), int(code.value)
+
+
+def kda_check_wait_timeout(limit_cycles: int, stream=None) -> None:
+    """Launch the failure-detection check: a bounded wait that runs out after
+    ``limit_cycles`` SM cycles and reports through the device error word."""
+    _check(load_library().kda_check_wait_timeout(int(limit_cycles), _stream(stream)), "kda_check_wait_timeout")

@@ -75,6 +75,8 @@ void prof_end(cudaStream_t s) {
   ++g_prof_n;
 }
 
+cudaError_t device_error_ptr(int32_t** ptr) { return device_error_word(ptr); }
+
 }  // namespace kda
 
 extern "C" {

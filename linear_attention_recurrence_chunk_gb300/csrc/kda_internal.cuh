@@ -114,6 +114,8 @@ Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t
                                  kda_dtype dt);
 
 // Measurement hook: event pair around one launch when profiling is on.
+// Device address of this device's error word.
+cudaError_t device_error_ptr(int32_t** ptr);
 void prof_begin(cudaStream_t s, const char* name);
 void prof_end(cudaStream_t s);
 

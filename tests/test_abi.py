@@ -102,6 +102,13 @@ def test_decode_rejects_bad_arguments_on_host():
     assert f(p[0], p[1], p[2], p[3], p[4], p[5], 4, 96, 128, 128, 3, p[6], None) == 1      # bad dtype
 
 
+def test_wait_timeout_check_rejects_bad_limits_on_host():
+    lib = kda.load_library()
+    assert lib.kda_check_wait_timeout(0, None) == 1
+    assert lib.kda_check_wait_timeout(-5, None) == 1
+    assert lib.kda_check_wait_timeout(10**9 + 1, None) == 1
+
+
 def test_python_binding_has_no_cpu_path():
     """The binding's functions only marshal: on CPU tensors the library must
     refuse (the pointers are host pointers), never compute on the host."""
