@@ -74,17 +74,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr)
                : "memory");
 }
-// d += a * b for one m16n8k16 bf16 tile, fp32 accumulators.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// d += a * b with fp16 operands.
+// d += a * b for one m16n8k16 tile with fp16 operands, fp32 accumulators.
 __device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                              uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -160,59 +150,60 @@ constexpr int kPrepTcThreads = 512;
 
 template <int DV>
 struct PrepTcSmem {
-  static constexpr int LDB = DK + 8;          // 16-bit row stride of the 128-wide operands (272 B)
   static constexpr int LDX = C + 8;           // fp16 row stride of A's off-diagonal blocks
   static constexpr int kWuN = DK + DV;        // columns of [w | u]
   static constexpr int LDA = C + 1;           // fp32 row stride of A's diagonal blocks
-  static constexpr int kCopRows = 16 + 32 + 48 + 64;
+  // Operands of the A / P products on the tensor cores: bf16, K-major (key
+  // channels contiguous), 128-byte swizzle, one atom per 64 channels.
+  //   row operand, 192 rows:    0-63  k e^{G - G_s},  64-127 q e^{G - G_s} (high part),
+  //                             128-191 its low part
+  //   column operand, 224 rows: 0-63  k e^{G_s - G} of the own sub-tile (high part),
+  //                             64-127 its low part,
+  //                             128 + kOff[a'] + i  k_i e^{G_s(a') - G_i} for the later
+  //                             sub-tiles a' = 1..3 (columns i < 16 a', high part only)
+  static constexpr int kRowRows = 192, kColRows = 224;
+  static constexpr size_t kRowAtom = (size_t)kRowRows * 128, kColAtom = (size_t)kColRows * 128;
   // raw input rows of the next task (TMA, bf16 [64][d]), staged during this one
   static constexpr size_t oRawG = 0;
   static constexpr size_t oRawK = oRawG + (size_t)C * DK * 2;
   static constexpr size_t oRawQ = oRawK + (size_t)C * DK * 2;
   static constexpr size_t oRawV = oRawQ + (size_t)C * DK * 2;
-  static constexpr size_t oKE = (oRawV + (size_t)C * DV * 2 + 1023) / 1024 * 1024;  // bf16 [64][LDB] k e^{G - G_s}
-  static constexpr size_t oQE = oKE + (size_t)C * LDB * 2;           // bf16 [64][LDB]  q e^{G - G_s}, high part
-  static constexpr size_t oQEl = oQE + (size_t)C * LDB * 2;          // bf16 [64][LDB]  low part
-  static constexpr size_t oCop = oQEl + (size_t)C * LDB * 2;         // bf16 [160][LDB] column operands, high part
-  static constexpr size_t oCopl = oCop + (size_t)kCopRows * LDB * 2; // bf16 [64][LDB] low part, diagonal blocks
+  static constexpr size_t oRow = (oRawV + (size_t)C * DV * 2 + 1023) / 1024 * 1024;
+  static constexpr size_t oCol = oRow + (DK / 64) * kRowAtom;
   // [beta k e^G | beta V], fp16, the B operand of [w | u] = X (...): MN-major,
   // 128-byte swizzle, 64-column atoms [64 tokens][128 B] of 8 KB
-  static constexpr size_t oKV = (oCopl + (size_t)C * LDB * 2 + 1023) / 1024 * 1024;
+  static constexpr size_t oKV = oCol + (DK / 64) * kColAtom;
   static constexpr size_t oPst = oKV + (size_t)(kWuN / 64) * 8192;   // fp16 [64][64] P, 128-byte swizzle (TMA store)
-  static constexpr size_t oTot = oPst + (size_t)C * C * 2;           // fp32 [8][DK] group sums; later P partials
+  static constexpr size_t oTot = oPst + (size_t)C * C * 2;           // fp32 [8][DK] group sums
   static constexpr size_t oBeta = oTot + (size_t)8 * DK * 4;         // fp32 [64]
-  static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarriers: raw rows, [w | u] products
-  static constexpr size_t oTmem = oBar + 16;                          // TMEM base address
+  static constexpr size_t oBar = oBeta + (size_t)C * 4;              // mbarriers: raw rows, [w | u], A / P products
+  static constexpr size_t oTmem = oBar + 24;                          // TMEM base address
   static constexpr size_t kBytes = oTmem + 8;
   static constexpr size_t kAlloc = kBytes + 1024;                    // slack to align the base to 1 KB
-  // reused once A and P are in registers
-  static constexpr size_t oA = oKE;                                   // fp32 [64][LDA]  A, diagonal blocks
+  // reused once the A / P products are done
+  static constexpr size_t oA = oRow;                                  // fp32 [64][LDA]  A, diagonal blocks
   // X, fp16 [128][64] (rows 64-127 zero), K-major with 128-byte swizzle: the A operand of [w | u]
   static constexpr size_t oXb = (oA + (size_t)C * LDA * 4 + 1023) / 1024 * 1024;
   static constexpr size_t oAh = oXb + (size_t)2 * C * C * 2;         // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
+  static constexpr size_t oWst = oRow;                               // [w | u] tiles of the previous task (8 KB each)
   static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
-  static_assert(oKE + (size_t)(kWuN / 64) * 8192 <= oKV && (oKE % 1024) == 0, "the [w | u] tiles fit the operand area");
-  static_assert((oKE % 16) == 0 && (oQEl % 16) == 0 && (oCop % 16) == 0 && (oCopl % 16) == 0 && (oKV % 16) == 0 &&
-                    (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oBar % 8) == 0 && (oRawV % 1024) == 0,
-                "ldmatrix, mbarrier and TMA alignment");
+  static_assert(oWst + (size_t)(kWuN / 64) * 8192 <= oKV, "the [w | u] tiles fit the operand area");
+  static_assert((oRow % 1024) == 0 && (oCol % 1024) == 0 && (kRowAtom % 1024) == 0 && (kColAtom % 1024) == 0 &&
+                    (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oPst % 1024) == 0 && (oBar % 8) == 0 &&
+                    (oRawV % 1024) == 0,
+                "TMA, tcgen05 operand and mbarrier alignment");
   static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
 };
 
-// A/P jobs per warp (16 warps): (kind, row block a, column block b).  Kinds:
-// 1 = A block (k e^{G-G_s} x column operand), 2 = P block below the diagonal
-// (q e^{G-G_s} x column operand, high parts), 3 = P diagonal block, high row
-// part x (high + low) column parts, 4 = the low row part x high column part of
-// the same diagonal block, handed to the kind-3 warp through shared memory;
-// 0 = none.  Every warp carries at most 32 MMAs.
-__constant__ int8_t kApJobs[16][2][3] = {
-    {{3, 0, 0}, {0, 0, 0}}, {{3, 1, 1}, {0, 0, 0}}, {{3, 2, 2}, {0, 0, 0}}, {{3, 3, 3}, {0, 0, 0}},
-    {{4, 0, 0}, {1, 3, 3}}, {{4, 1, 1}, {1, 3, 2}}, {{4, 2, 2}, {1, 3, 1}}, {{4, 3, 3}, {1, 3, 0}},
-    {{2, 3, 2}, {1, 2, 2}}, {{2, 3, 1}, {1, 2, 1}}, {{2, 3, 0}, {1, 2, 0}}, {{2, 2, 1}, {1, 1, 1}},
-    {{2, 2, 0}, {0, 0, 0}}, {{2, 1, 0}, {0, 0, 0}}, {{1, 1, 0}, {0, 0, 0}}, {{1, 0, 0}, {0, 0, 0}}};
+// Row (in the column operand) of column i of later sub-tile a' = 1..3, minus 128.
+__device__ __forceinline__ int later_row0(int a2) { return a2 == 1 ? 0 : (a2 == 2 ? 16 : 48); }
 
-// First row (in the column-operand area) of block-row a's column operand.
-__device__ __forceinline__ int cop_row0(int a) { return a == 0 ? 0 : (a == 1 ? 16 : (a == 2 ? 48 : 96)); }
+// Byte offset of (row, channel) in a K-major 128-byte-swizzled operand whose
+// 64-channel atoms hold `rows` rows each.
+__device__ __forceinline__ uint32_t opnd_off(int rows, int row, int ch) {
+  return (uint32_t)(ch >> 6) * (uint32_t)rows * 128u + tc::sw128_offset(row, ch & 63);
+}
 
 
 template <int DV>
@@ -224,17 +215,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
   using L = PrepTcSmem<DV>;
-  constexpr int LDB = L::LDB, LDX = L::LDX, LDA = L::LDA;
+  constexpr int LDX = L::LDX, LDA = L::LDA;
   constexpr int NTH = kPrepTcThreads;
-  constexpr uint32_t kTmemCols = 256;   // the [w | u] accumulator: rows 0-63 in TMEM lanes 0-63
+  // TMEM: the A / P accumulators (columns 0-287) and, after them, the [w | u]
+  // accumulator (columns 0-255, rows 0-63 in lanes 0-63)
+  constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescWU = tc::idesc_f16_f32(128, L::kWuN) | (1u << 16);   // B (KV) MN-major
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-  bf16* sKE = reinterpret_cast<bf16*>(smem + L::oKE);
-  bf16* sQE = reinterpret_cast<bf16*>(smem + L::oQE);
-  bf16* sQEl = reinterpret_cast<bf16*>(smem + L::oQEl);
-  bf16* sCop = reinterpret_cast<bf16*>(smem + L::oCop);
-  bf16* sCopl = reinterpret_cast<bf16*>(smem + L::oCopl);
+  uint8_t* sRow = smem + L::oRow;   // row operand of the A / P products
+  uint8_t* sCol = smem + L::oCol;   // column operand
   uint8_t* sKV = smem + L::oKV;
   uint8_t* sPst = smem + L::oPst;
   float* sTot = reinterpret_cast<float*>(smem + L::oTot);
@@ -254,6 +244,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   if (tid == 0) {
     tc::mbar_init(bar, 1);       // raw rows staged
     tc::mbar_init(bar + 1, 1);   // [w | u] products done
+    tc::mbar_init(bar + 2, 1);   // A / P products done
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&tmG);
     tc::tma_prefetch_desc(&tmK);
@@ -276,7 +267,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   // operand area, which thread 0 stores to the record with TMA; the tiles are
   // released (bulk read wait) before the operand area is rewritten.
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
-  uint32_t wu_parity = 0;
+  uint32_t wu_parity = 0, ap_parity = 0;
   int64_t wu_rec = 0;
   auto wu_drain = [&]() -> bool {
     if (!wu_pending) return true;
@@ -284,7 +275,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     wu_parity ^= 1u;
     wu_pending = false;
     tc::tc_fence_after();
-    uint8_t* stg = smem + L::oKE;   // tile t (columns 64t..64t+63) at stg + 8 KB * t
+    uint8_t* stg = smem + L::oWst;   // tile t (columns 64t..64t+63) at stg + 8 KB * t
     const int qw = warp & 3, cg = warp >> 2;
     if (qw < 2 && 64 * cg < L::kWuN) {
       const int r = 32 * qw + lane;
@@ -434,8 +425,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     issue(h_next, ci_next);
 
     // 2. Offsets from the group sums: G_s(a') = cumulative decay before sub-tile
-    //    a', G_last; then per-thread factors e^{G_s(a)}, e^{G_last - G_s(a)},
-    //    e^{G_s(a') - G_s(a)} for a' >= a.
+    //    a', G_last; then the per-thread factors e^{G_s(a') - G_s(a)}, a' >= a.
     float2 gsA[4], gl;
     {
       float2 acc = make_float2(0.f, 0.f), excl = acc;
@@ -458,8 +448,6 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 #pragma unroll
     for (int a2 = 1; a2 < 4; ++a2)
       if (a2 == a) gs = gsA[a2];
-    const float2 lam = make_float2(ex2_approx(gs.x), ex2_approx(gs.y));
-    const float2 psi = make_float2(ex2_approx(gl.x - gs.x), ex2_approx(gl.y - gs.y));
     float2 om[4];
 #pragma unroll
     for (int a2 = 0; a2 < 4; ++a2)
@@ -467,35 +455,84 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                       : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
     if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(ex2_approx(gl.x), ex2_approx(gl.y));
 
-    // 3. Elementwise operands; every 16-bit operand is stored as a 32-bit pair.
+    // 3. The operands of the A / P products (every 16-bit operand is stored as
+    //    a 32-bit pair).
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+      const int r = r0 + rr;
+      const float2 gr = G[rr];
+      const float e0 = ex2_approx(gr.x - gs.x), e1 = ex2_approx(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]: normal
+      const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
+      const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
+      const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
+      *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, r, c)) = pack_bf16x2(k0 * e0, k1 * e1);
+      uint32_t hi, lo;
+      split_bf16x2(q0 * e0, q1 * e1, hi, lo);
+      *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, C + r, c)) = hi;
+      *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, 2 * C + r, c)) = lo;
+      const float kf0 = k0 * f0, kf1 = k1 * f1;
+      split_bf16x2(kf0, kf1, hi, lo);   // own sub-tile: high and low parts
+      *reinterpret_cast<uint32_t*>(sCol + opnd_off(L::kColRows, r, c)) = hi;
+      *reinterpret_cast<uint32_t*>(sCol + opnd_off(L::kColRows, C + r, c)) = lo;
+#pragma unroll
+      for (int a2 = 1; a2 < 4; ++a2) {   // later sub-tiles: factors <= 1, high part only
+        if (a2 > a)
+          *reinterpret_cast<uint32_t*>(sCol + opnd_off(L::kColRows, 2 * C + later_row0(a2) + r, c)) =
+              pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
+      }
+    }
+    tc::fence_proxy_async_smem();   // the operands, written by the threads, read by the MMAs
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    // 4. A and P on the tensor cores (bf16 operands, fp32 accumulators in TMEM):
+    //      D1 = [k e^G ; q e^G high] (M = 128) x (column operand)^T (N = 224, K = d_k)
+    //      D2 = [q e^G high ; low]   (M = 128) x (own sub-tile, high part)^T (N = 64)
+    //    A_ri = beta_r D1[r][..] (rows 0-63); P_ri = D1[64 + r][..], plus, on the
+    //    diagonal blocks, the low-part products D1[64 + r][64 + i] + D2[64 + r][i].
+    if (tid == 0) {
+      const uint64_t dR = tc::desc_kmajor_sw128(tc::smem_u32(sRow));
+      const uint64_t dC = tc::desc_kmajor_sw128(tc::smem_u32(sCol));
+      constexpr uint32_t kId1 = tc::idesc_bf16_f32(128, L::kColRows), kId2 = tc::idesc_bf16_f32(128, C);
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint64_t oR = (((kk >> 2) * L::kRowAtom) + (kk & 3) * 32) >> 4;
+        const uint64_t oC = (((kk >> 2) * L::kColAtom) + (kk & 3) * 32) >> 4;
+        if (kk == 0)
+          tc::mma_16bit_first(tmem, dR + oR, dC + oC, kId1);
+        else
+          tc::mma_16bit_acc(tmem, dR + oR, dC + oC, kId1);
+      }
+#pragma unroll
+      for (int kk = 0; kk < DK / 16; ++kk) {
+        const uint64_t oR = (((kk >> 2) * L::kRowAtom) + C * 128 + (kk & 3) * 32) >> 4;
+        const uint64_t oC = (((kk >> 2) * L::kColAtom) + (kk & 3) * 32) >> 4;
+        if (kk == 0)
+          tc::mma_16bit_first(tmem + L::kColRows, dR + oR, dC + oC, kId2);
+        else
+          tc::mma_16bit_acc(tmem + L::kColRows, dR + oR, dC + oC, kId2);
+      }
+      tc::mma_commit(bar + 2);
+    }
+
+    // While they run: [beta k e^G | beta V] (the operand of [w | u]), and the
+    // record's q e^G rows and (k e^{G_last - G})^T, with G taken from the chunk
+    // start (2^G and 2^{G_last - G} directly).
     {
       uint32_t kt0[4], kt1[4];   // K~^T rows c and c+1, tokens r0..r0+7, fp16 pairs
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = r0 + rr;
         const float2 gr = G[rr];
-        const float e0 = ex2_approx(gr.x - gs.x), e1 = ex2_approx(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]: normal
-        const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
+        const float eg0 = ex2_approx(gr.x), eg1 = ex2_approx(gr.y);                 // e^{G_r}
+        const float el0 = ex2_approx(gl.x - gr.x), el1 = ex2_approx(gl.y - gr.y);   // e^{G_last - G_r}
         const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
         const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
         const float br = sBeta[r];
-        *reinterpret_cast<__nv_bfloat162*>(sKE + r * LDB + c) = __floats2bfloat162_rn(k0 * e0, k1 * e1);
-        uint32_t hi, lo;
-        split_bf16x2(q0 * e0, q1 * e1, hi, lo);
-        *reinterpret_cast<uint32_t*>(sQE + r * LDB + c) = hi;
-        *reinterpret_cast<uint32_t*>(sQEl + r * LDB + c) = lo;
-        const float kf0 = k0 * f0, kf1 = k1 * f1;
-        split_bf16x2(kf0, kf1, hi, lo);   // own sub-tile: high and low parts
-        *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a) + r) * LDB + c) = hi;
-        *reinterpret_cast<uint32_t*>(sCopl + r * LDB + c) = lo;
-#pragma unroll
-        for (int a2 = 1; a2 < 4; ++a2) {   // later sub-tiles: factors <= 1, high part only
-          if (a2 > a)
-            *reinterpret_cast<uint32_t*>(sCop + (cop_row0(a2) + r) * LDB + c) = pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
-        }
-        *reinterpret_cast<uint32_t*>(sKV + kv_off(r, c)) = pack_f16x2(br * k0 * e0 * lam.x, br * k1 * e1 * lam.y);
-        *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * e0 * lam.x, q1 * e1 * lam.y);
-        const __half2 kt = __floats2half2_rn(kf0 * psi.x, kf1 * psi.y);
+        *reinterpret_cast<uint32_t*>(sKV + kv_off(r, c)) = pack_f16x2(br * k0 * eg0, br * k1 * eg1);
+        *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * eg0, q1 * eg1);
+        const __half2 kt = __floats2half2_rn(k0 * el0, k1 * el1);
         const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
         if (rr & 1) {
           kt0[rr >> 1] |= lo16 << 16;
@@ -519,99 +556,62 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         *reinterpret_cast<uint4*>(sKV + kv_off(r, DK + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
-    __syncthreads();
-
-    // 5. A and P, one 16x16 block (row block a, column block b <= a) per job.
-    float acc[2][2][4];
+    // 5. A and P out of TMEM: A to shared memory, P to the record tile.
+    {
+      const bool okap = tc::mbar_wait(bar + 2, ap_parity, kWaitLimit);
+      ap_parity ^= 1u;
+      if (!okap) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      tc::tc_fence_after();
+      // Warp -> TMEM lane quarter q (rows 32(q%2).. of A for q < 2, of P for
+      // q >= 2) and 16-column block b; each lane holds one row r of sub-tile ar.
+      const int q = warp & 3, b = warp >> 2;
+      const uint32_t tl = (uint32_t)(32 * q);
+      const int rr = 32 * (q & 1) + lane, ar = rr >> 4;
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb)
+      for (int part = 0; part < 2; ++part) {
+        const int ap = 2 * (q & 1) + part;   // the sub-tile of lanes 16 part .. 16 part + 15
+        float v[16];
+        if (q < 2) {
+          if (b > ap) continue;
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, b == ap ? 16 * b : 2 * C + later_row0(ap) + 16 * b), v);
+          if (ar != ap) continue;
+          const float br = sBeta[rr];
+          if (b == ap) {   // diagonal block, fp32 (only its strictly lower part is read)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) acc[jb][nt][0] = acc[jb][nt][1] = acc[jb][nt][2] = acc[jb][nt][3] = 0.f;
+            for (int i = 0; i < 16; ++i) sA[rr * LDA + 16 * b + i] = br * v[i];
+          } else {         // below the diagonal, fp16
+            uint4* dst = reinterpret_cast<uint4*>(sAh + rr * LDX + 16 * b);
 #pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
-      if (kind == 0) continue;
-      const bf16* rowop = (kind == 1 ? sKE : (kind == 4 ? sQEl : sQE)) + (16 * a) * LDB;
-      const bf16* colop = sCop + (cop_row0(a) + 16 * b) * LDB;
-      const bf16* collo = sCopl + (16 * a) * LDB;
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        const int aoff = (lane & 15) * LDB + ks * 16 + (lane >> 4) * 8;
-        const int boff = ((lane & 7) + (lane >> 4) * 8) * LDB + ks * 16 + ((lane >> 3) & 1) * 8;
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(tc::smem_u32(rowop + aoff), a0, a1, a2, a3);
-        ldsm_x4(tc::smem_u32(colop + boff), b0, b1, b2, b3);
-        mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
-        mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
-        if (kind == 3) {
-          ldsm_x4(tc::smem_u32(collo + boff), b0, b1, b2, b3);
-          mma16816(acc[jb][0], a0, a1, a2, a3, b0, b1);
-          mma16816(acc[jb][1], a0, a1, a2, a3, b2, b3);
-        }
-      }
-    }
-    float* sPart = sTot;   // [4][2][4][32] low-part partials of the diagonal P blocks
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {   // P blocks below the diagonal to the record; diagonal partials to SMEM
-      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
-      if (kind == 4) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sPart[((a * 2 + nt) * 4 + e) * 32 + lane] = acc[jb][nt][e];
-      }
-      if (kind != 2) continue;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int i0 = 16 * b + 8 * nt + 2 * tq;
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = 16 * a + gq + 8 * hr;
-          *reinterpret_cast<uint32_t*>(sPst + xs_off(r, i0)) = pack_f16x2(acc[jb][nt][2 * hr], acc[jb][nt][2 * hr + 1]);
-        }
-      }
-    }
-    for (int idx = tid; idx < 6 * 128; idx += NTH) {   // the 6 blocks of P above the block diagonal, as pairs
-      const int blk = idx >> 7, e = idx & 127;
-      const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      *reinterpret_cast<uint32_t*>(sPst + xs_off(16 * a + (e >> 3), 16 * b + (e & 7) * 2)) = 0u;
-    }
-    __syncthreads();   // every read of the operand area is done: it becomes A / X / Xb
-#pragma unroll
-    for (int jb = 0; jb < 2; ++jb) {
-      const int kind = kApJobs[warp][jb][0], a = kApJobs[warp][jb][1], b = kApJobs[warp][jb][2];
-      if (kind == 3) {   // diagonal P block: add the low-part partial, keep the inclusive lower triangle
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int i0 = 16 * b + 8 * nt + 2 * tq;
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int r = 16 * a + gq + 8 * hr;
-            const float v0 = acc[jb][nt][2 * hr] + sPart[((a * 2 + nt) * 4 + 2 * hr) * 32 + lane];
-            const float v1 = acc[jb][nt][2 * hr + 1] + sPart[((a * 2 + nt) * 4 + 2 * hr + 1) * 32 + lane];
-            *reinterpret_cast<uint32_t*>(sPst + xs_off(r, i0)) = pack_f16x2(i0 <= r ? v0 : 0.f, i0 + 1 <= r ? v1 : 0.f);
+            for (int j = 0; j < 2; ++j)
+              dst[j] = make_uint4(pack_f16x2(br * v[8 * j + 0], br * v[8 * j + 1]), pack_f16x2(br * v[8 * j + 2], br * v[8 * j + 3]),
+                                  pack_f16x2(br * v[8 * j + 4], br * v[8 * j + 5]), pack_f16x2(br * v[8 * j + 6], br * v[8 * j + 7]));
           }
-        }
-      }
-      if (kind != 1) continue;
+        } else {
+          if (b > ap) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {   // A = beta_r * (strictly lower part): diagonal blocks fp32, the rest fp16
-        const int i0 = 16 * b + 8 * nt + 2 * tq;
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          } else if (b == ap) {
+            float w2[16];
+            tc::tmem_ld16(tc::tmem_addr(tmem, tl, 16 * b), v);
+            tc::tmem_ld16(tc::tmem_addr(tmem, tl, C + 16 * b), w2);
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = 16 * a + gq + 8 * hr;
-          const float br = sBeta[r];
-          if (a == b) {
-            sA[r * LDA + i0] = br * acc[jb][nt][2 * hr];
-            sA[r * LDA + i0 + 1] = br * acc[jb][nt][2 * hr + 1];
+            for (int i = 0; i < 16; ++i) v[i] += w2[i];
+            tc::tmem_ld16(tc::tmem_addr(tmem, tl, L::kColRows + 16 * b), w2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = i <= (rr & 15) ? v[i] + w2[i] : 0.f;   // inclusive lower triangle
           } else {
-            *reinterpret_cast<uint32_t*>(sAh + r * LDX + i0) =
-                pack_f16x2(br * acc[jb][nt][2 * hr], br * acc[jb][nt][2 * hr + 1]);
+            tc::tmem_ld16(tc::tmem_addr(tmem, tl, 2 * C + later_row0(ap) + 16 * b), v);
           }
+          if (ar != ap) continue;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4*>(sPst + xs_off(rr, 16 * b + 8 * j)) =
+                make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                           pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
         }
       }
     }
+    tc::tc_fence_before();
     tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     __syncthreads();
     if (tid == 0) {   // P to the record (the tile is released at the next task's first CTA barrier)
