@@ -5,13 +5,19 @@
 //  chunk_prep_tc   persistent, one 512-thread CTA per SM over (64-token chunk,
 //                  head) tasks in chunk-major order; the next task's raw rows
 //                  arrive by TMA while the current one is processed.  Gate,
-//                  cumulative log-decay, the exp(+-G) scalings, the
-//                  beta-weighted decayed k k^T matrix A and the intra-chunk
-//                  read-out matrix P per 16-row sub-tile (mma.sync: the
-//                  sub-tiles are 16 rows tall), X = (I + A)^{-1} by blocked
-//                  forward substitution, then w, u = X Diag(beta) [k e^G | V]
-//                  (mma.sync).  Writes fp16 records: [w; q e^G], P,
-//                  (k e^{G_last - G})^T, u and fp32 e^{G_last}.
+//                  cumulative log-decay, the exp(+-G) scalings as bf16
+//                  operand tiles (128-byte swizzle), then the beta-weighted
+//                  decayed k k^T matrix A and the intra-chunk read-out matrix
+//                  P as two tcgen05 products (M = 128: the rows of every
+//                  16-row sub-tile against the columns it needs, fp32 in
+//                  TMEM) while the threads write the q e^G and K~^T records
+//                  and the [beta k e^G | beta V] operand; X = (I + A)^{-1} by
+//                  blocked forward substitution (diagonal blocks in registers,
+//                  blocks below on mma.sync), then w, u = X [beta k e^G |
+//                  beta V] as one tcgen05 product whose TMEM result is drained
+//                  and stored by TMA during the next task.  Writes fp16
+//                  records: [w; q e^G], P, (k e^{G_last - G})^T, u and fp32
+//                  e^{G_last}.
 //
 //  chunk_chain_tc  one CTA per (sequence, head, 32 value columns); the wide
 //  (_wide_tc)      form takes 64 or all value columns per CTA.  Walks the
