@@ -191,9 +191,9 @@ struct PrepTcSmem {
   // X, fp16 [128][64] (rows 64-127 zero), K-major with 128-byte swizzle: the A operand of [w | u]
   static constexpr size_t oXb = (oA + (size_t)C * LDA * 4 + 1023) / 1024 * 1024;
   static constexpr size_t oAh = oXb + (size_t)2 * C * C * 2;         // fp16 [64][LDX]  A, blocks below them
-  static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [3][16][24] per-warp Y blocks
+  static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [7][16][24] scratch blocks of the inverse
   static constexpr size_t oWst = oRow;                               // [w | u] tiles of the previous task (8 KB each)
-  static_assert(oYh + 3 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
+  static_assert(oYh + 7 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
   static_assert(oWst + (size_t)(kWuN / 64) * 8192 <= oKV, "the [w | u] tiles fit the operand area");
   static_assert((oRow % 1024) == 0 && (oCol % 1024) == 0 && (kRowAtom % 1024) == 0 && (kColAtom % 1024) == 0 &&
                     (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oPst % 1024) == 0 && (oBar % 8) == 0 &&
@@ -629,67 +629,147 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
     //    diagonal 16x16 blocks (only their strictly lower parts are read) by
     //    forward substitution in fp32, one column per thread in registers;
-    //    then, block-row after block-row, on tensor cores,
-    //    Y_b = sum_{b<=m<a} A_am X_mb and X_ab = -X_aa Y_b.
-    if (tid < C) {
-      const int base = (tid / kSub) * kSub, jc = tid % kSub;
+    //    then the blocks below them on tensor cores, in two stages of
+    //    dependent 16x16 products (T blocks rounded to fp16 like X):
+    //      1: X_10 = -X_11 A_10 X_00,  X_32 = -X_33 A_32 X_22,  T_21 = A_21 X_11,  T_31 = A_31 X_11
+    //      2: X_20 = -X_22 T_20,  X_21 = -X_22 T_21,  X_30 = -(X_32 T_20 + X_33 T_30),
+    //         X_31 = -(X_32 T_21 + X_33 T_31),  with T_a0 = A_a0 X_00 + A_a1 X_10.
+    if (warp < C / kSub && lane < kSub) {   // block `warp`, column `lane`
+      const int base = warp * kSub, jc = lane;
       float xc[kSub];
 #pragma unroll
-      for (int r = 0; r < kSub; ++r) {
-        float accx = (r == jc) ? 1.f : 0.f;
+      for (int r = 0; r < kSub; ++r) xc[r] = (r == jc) ? 1.f : 0.f;
+      // right-looking: once x_i is final it is folded into every later row, so
+      // the dependent chain is 16 steps long (rows above jc stay exactly 0)
 #pragma unroll
-        for (int i = 0; i < r; ++i) accx -= sA[(base + r) * LDA + base + i] * xc[i];
-        xc[r] = r < jc ? 0.f : accx;
+      for (int i = 0; i < kSub - 1; ++i) {
+#pragma unroll
+        for (int r = i + 1; r < kSub; ++r) xc[r] -= sA[(base + r) * LDA + base + i] * xc[i];
       }
 #pragma unroll
       for (int r = 0; r < kSub; ++r) *reinterpret_cast<f16*>(sX + xs_off(base + r, base + jc)) = __float2half_rn(xc[r]);
     }
-    for (int idx = tid; idx < 6 * 32; idx += NTH) {   // zeros above the block diagonal of X (16-byte chunks)
-      const int blk = idx >> 5, e = idx & 31;
-      const int ra = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int rb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      *reinterpret_cast<uint4*>(sX + xs_off(16 * ra + (e >> 1), 16 * rb + 8 * (e & 1))) = make_uint4(0u, 0u, 0u, 0u);
+    constexpr int kZeroThreads = NTH - 32 * (C / kSub);   // the warps not inverting a block
+    if (tid >= NTH - kZeroThreads) {
+      const int z = tid - (NTH - kZeroThreads);
+      for (int idx = z; idx < 6 * 32; idx += kZeroThreads) {   // zeros above the block diagonal of X (16-byte chunks)
+        const int blk = idx >> 5, e = idx & 31;
+        const int ra = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int rb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        *reinterpret_cast<uint4*>(sX + xs_off(16 * ra + (e >> 1), 16 * rb + 8 * (e & 1))) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int idx = z; idx < C * 8; idx += kZeroThreads)   // rows 64-127 of the MMA's A tile are zero
+        *reinterpret_cast<uint4*>(sX + C * 128 + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int idx = tid; idx < C * 8; idx += NTH)   // rows 64-127 of the MMA's A tile are zero
-      *reinterpret_cast<uint4*>(sX + C * 128 + idx * 16) = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-#pragma unroll
-    for (int ab = 1; ab < C / kSub; ++ab) {
-      if (warp < ab) {   // warp b computes X_{ab, b}
-        const int b = warp;
-        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int m = b; m < ab; ++m) {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(tc::smem_u32(sAh + (16 * ab + (lane & 15)) * LDX + 16 * m + (lane >> 4) * 8), a0, a1, a2, a3);
-          ldsm_x4_t(tc::smem_u32(sX + xs_off(16 * m + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * b + (lane >> 4) * 8)),
-                    b0, b1, b2, b3);
-          mma16816_f16(y[0], a0, a1, a2, a3, b0, b1);
-          mma16816_f16(y[1], a0, a1, a2, a3, b2, b3);
-        }
-        f16* yb = sYh + warp * 16 * 24;
+    {
+      // m16n8k16 fragments: A_am (row-major, fp16 [64][LDX]), X_am as the A
+      // operand, X_mb or a [16][24] scratch block as the B operand (two n-tiles).
+      auto ld_a = [&](int ra, int m, uint32_t (&f)[4]) {
+        ldsm_x4(tc::smem_u32(sAh + (16 * ra + (lane & 15)) * LDX + 16 * m + (lane >> 4) * 8), f[0], f[1], f[2], f[3]);
+      };
+      auto ld_xa = [&](int ra, int m, uint32_t (&f)[4]) {
+        ldsm_x4(tc::smem_u32(sX + xs_off(16 * ra + (lane & 15), 16 * m + (lane >> 4) * 8)), f[0], f[1], f[2], f[3]);
+      };
+      auto ld_xb = [&](int m, int rb, uint32_t (&f)[4]) {
+        ldsm_x4_t(tc::smem_u32(sX + xs_off(16 * m + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * rb + (lane >> 4) * 8)),
+                  f[0], f[1], f[2], f[3]);
+      };
+      auto ld_tb = [&](const f16* t, uint32_t (&f)[4]) {
+        ldsm_x4_t(tc::smem_u32(t + ((lane & 7) + ((lane >> 3) & 1) * 8) * 24 + (lane >> 4) * 8), f[0], f[1], f[2], f[3]);
+      };
+      auto mma_nn = [&](float (&y)[2][4], const uint32_t (&fa)[4], const uint32_t (&fb)[4]) {
+        mma16816_f16(y[0], fa[0], fa[1], fa[2], fa[3], fb[0], fb[1]);
+        mma16816_f16(y[1], fa[0], fa[1], fa[2], fa[3], fb[2], fb[3]);
+      };
+      auto st_t = [&](f16* t, const float (&y)[2][4]) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          *reinterpret_cast<uint32_t*>(yb + gq * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][0], y[nt][1]);
-          *reinterpret_cast<uint32_t*>(yb + (gq + 8) * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][2], y[nt][3]);
+          *reinterpret_cast<uint32_t*>(t + gq * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][0], y[nt][1]);
+          *reinterpret_cast<uint32_t*>(t + (gq + 8) * 24 + 8 * nt + 2 * tq) = pack_f16x2(y[nt][2], y[nt][3]);
         }
+      };
+      auto st_x = [&](int ra, int rb, const float (&y)[2][4]) {   // X_ab = -y
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ra + gq, 16 * rb + 8 * nt + 2 * tq)) = pack_f16x2(-y[nt][0], -y[nt][1]);
+          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ra + gq + 8, 16 * rb + 8 * nt + 2 * tq)) = pack_f16x2(-y[nt][2], -y[nt][3]);
+        }
+      };
+      constexpr int kBlk = 16 * 24;   // one scratch block: 0, 1 stage-1 products, 2 T_21, 3 T_31, 4, 5 T_20, 6 T_30
+      uint32_t fa[4], fb[4];
+      if (warp < 2) {   // stage 1: X_10 (warp 0), X_32 (warp 1)
+        const int ra = warp == 0 ? 1 : 3, rb = ra - 1;
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ld_a(ra, rb, fa);
+        ld_xb(rb, rb, fb);
+        mma_nn(y, fa, fb);
+        f16* yb = sYh + warp * kBlk;
+        st_t(yb, y);
         __syncwarp();
         float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(tc::smem_u32(sX + xs_off(16 * ab + (lane & 15), 16 * ab + (lane >> 4) * 8)), a0, a1, a2, a3);
-          ldsm_x4_t(tc::smem_u32(yb + ((lane & 7) + ((lane >> 3) & 1) * 8) * 24 + (lane >> 4) * 8), b0, b1, b2, b3);
-          mma16816_f16(x[0], a0, a1, a2, a3, b0, b1);
-          mma16816_f16(x[1], a0, a1, a2, a3, b2, b3);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ab + gq, 16 * b + 8 * nt + 2 * tq)) =
-              pack_f16x2(-x[nt][0], -x[nt][1]);
-          *reinterpret_cast<uint32_t*>(sX + xs_off(16 * ab + gq + 8, 16 * b + 8 * nt + 2 * tq)) =
-              pack_f16x2(-x[nt][2], -x[nt][3]);
-        }
+        ld_xa(ra, ra, fa);
+        ld_tb(yb, fb);
+        mma_nn(x, fa, fb);
+        st_x(ra, rb, x);
+      } else if (warp < 4) {   // stage 1: T_21 (warp 2), T_31 (warp 3)
+        float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ld_a(warp, 1, fa);
+        ld_xb(1, 1, fb);
+        mma_nn(y, fa, fb);
+        st_t(sYh + warp * kBlk, y);
       }
       __syncthreads();
+      float x[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (warp == 1) {          // X_21 = -X_22 T_21
+        ld_xa(2, 2, fa);
+        ld_tb(sYh + 2 * kBlk, fb);
+        mma_nn(x, fa, fb);
+        st_x(2, 1, x);
+      } else if (warp == 3) {   // X_31 = -(X_32 T_21 + X_33 T_31)
+        ld_xa(3, 2, fa);
+        ld_tb(sYh + 2 * kBlk, fb);
+        mma_nn(x, fa, fb);
+        ld_xa(3, 3, fa);
+        ld_tb(sYh + 3 * kBlk, fb);
+        mma_nn(x, fa, fb);
+        st_x(3, 1, x);
+      } else if (warp == 0 || warp == 2) {   // X_20 (warp 0), X_30 (warp 2): both form T_20
+        float t[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        ld_a(2, 0, fa);
+        ld_xb(0, 0, fb);
+        mma_nn(t, fa, fb);
+        ld_a(2, 1, fa);
+        ld_xb(1, 0, fb);
+        mma_nn(t, fa, fb);
+        f16* t20 = sYh + (warp == 0 ? 4 : 5) * kBlk;
+        st_t(t20, t);
+        if (warp == 2) {
+          float t3[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          ld_a(3, 0, fa);
+          ld_xb(0, 0, fb);
+          mma_nn(t3, fa, fb);
+          ld_a(3, 1, fa);
+          ld_xb(1, 0, fb);
+          mma_nn(t3, fa, fb);
+          st_t(sYh + 6 * kBlk, t3);
+        }
+        __syncwarp();
+        if (warp == 0) {
+          ld_xa(2, 2, fa);
+          ld_tb(t20, fb);
+          mma_nn(x, fa, fb);
+          st_x(2, 0, x);
+        } else {
+          ld_xa(3, 2, fa);
+          ld_tb(t20, fb);
+          mma_nn(x, fa, fb);
+          ld_xa(3, 3, fa);
+          ld_tb(sYh + 6 * kBlk, fb);
+          mma_nn(x, fa, fb);
+          st_x(3, 0, x);
+        }
+      }
     }
 
     // 7. [w | u] = X [beta k e^G | beta V] on the tensor cores (M = 64, N = d_k + d_v,
