@@ -25,9 +25,9 @@
 //                  registers, feeding tcgen05 MMAs (fp32 accumulators in TMEM,
 //                  issued by one warp) from TMA-staged fp16 tiles
 //                  (double-buffered by a producer warp):
-//                     round 1:  D12 = [w; q e^G] . S                (M=128, K=d_k)
+//                     group 1:  D12 = [w; q e^G] . S                (M=128, K=d_k)
 //                               V_new = u - D12[0:64]
-//                     round 2:  D12 += [0; P] . V_new               (M=128, K=64)
+//                     group 2:  D12 += [0; P] . V_new               (M=128, K=64)
 //                               D3   = (k e^{G_last-G})^T . V_new   (M=128, K=64)
 //                     o = D12[64:128];   S = Diag(e^{G_last}) S + D3
 //
@@ -851,10 +851,10 @@ __device__ __forceinline__ void store_bf16x16(bf16* dst, const float (&x)[16]) {
 
 // Inter-chunk pass of one (sequence, head, 32-column value block): the state
 // lives in fp32 registers of the consumer threads (key channel = TMEM lane),
-// its fp16 copy is the B operand of both MMA rounds of the next chunk.
-//   round 1: D12 = [w; q e^G] S                       (rows 0-63: w S, 64-127: q e^G S)
+// its fp16 copy is the B operand of both MMA groups of the next chunk.
+//   group 1: D12 = [w; q e^G] S                       (rows 0-63: w S, 64-127: q e^G S)
 //   V_new  = u - (w S)                                 (consumers, to SMEM)
-//   round 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
+//   group 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
 //   S      = e^{G_last} S + D3                          (consumers)
 template <int DV>
 __global__ void __launch_bounds__(kChainTcThreads, 1)
@@ -953,7 +953,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         tc::tc_fence_after();
         const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
         const uint32_t d12 = tmem + kTmemD12 + (uint32_t)st * 32;
-        tc::mma_16bit_first(d12, dA, dS0, kIdescMN);   // round 1
+        tc::mma_16bit_first(d12, dA, dS0, kIdescMN);   // group 1
 #pragma unroll
         for (int kk = 1; kk < DK / 16; ++kk)
           tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN);
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)   // round 2
+        for (int kk = 0; kk < C / 16; ++kk)   // group 2
           tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
         tc::mma_16bit_first(tmem + kTmemD3, dA + (L::oKT >> 4), dV0, kIdescMN);
 #pragma unroll
@@ -1212,7 +1212,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         tc::tc_fence_after();
         const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
         const uint32_t d12 = tmem + (uint32_t)st * NC;
-        tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // round 1
+        tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // group 1
 #pragma unroll
         for (int kk = 1; kk < DK / 16; ++kk)
           tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdesc);
@@ -1222,7 +1222,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)   // round 2
+        for (int kk = 0; kk < C / 16; ++kk)   // group 2
           tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc);
         tc::mma_16bit_first(tmem + kD3, dA + (L::oKT >> 4), dV0, kIdesc);
 #pragma unroll
