@@ -962,14 +962,17 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         ok = tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
         if (!ok) break;
         tc::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)   // group 2
-          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
+        // group 2: the state product first, committed on its own, then the o rows;
+        // the o rows are read once group 1 of the next chunk (issued after
+        // them) has completed, or after the final drain
         tc::mma_16bit_first(tmem + kTmemD3, dA + (L::oKT >> 4), dV0, kIdescMN);
 #pragma unroll
         for (int kk = 1; kk < C / 16; ++kk)
           tc::mma_16bit_acc(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
         tc::mma_commit(mma2);
+#pragma unroll
+        for (int kk = 0; kk < C / 16; ++kk)
+          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
         tc::mma_commit(empty + st);
       }
       if (!ok) atomicExch(dev_err, (int32_t)kDevErrTimeout);
@@ -1010,19 +1013,31 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         break;
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
-      if (i > 0 && q >= 2) {   // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer
-        const int r = c - 64;
-        float ov[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
-        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+      if (q >= 2) {
+        // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer,
+        // read while the state product is issued: its o product completed
+        // before this chunk's group 1 (mma1)
+        bad |= !tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
+        bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
+        if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+          bad = true;
+          break;
+        }
+        tc::tc_fence_after();
+        if (i > 0) {
+          const int r = c - 64;
+          float ov[16];
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
+          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+        }
       }
-      bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
-      if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
-        bad = true;
-        break;
-      }
-      tc::tc_fence_after();
       if (q < 2) {   // V_new rows (tokens) 0-63: u - w S
+        bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
+        if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
+          bad = true;
+          break;
+        }
+        tc::tc_fence_after();
         float d[16];
         tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)st * 32 + 16 * hf), d);
 #pragma unroll
@@ -1058,7 +1073,11 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
-    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
+    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o, once the final drain has completed
+      bad = __any_sync(0xffffffffu, !tc::mbar_wait(drain, 0, kWaitLimit));
+      tc::tc_fence_after();
+    }
+    if (i == nch && !bad && nch > 0 && q >= 2) {
       const int r = c - 64;
       float ov[16];
       tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
