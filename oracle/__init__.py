@@ -50,6 +50,9 @@ def _lib():
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.kda_oracle_chains.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp]
         lib.kda_oracle_chains.restype = ctypes.c_int
+        lib.kda_oracle_chains_snap.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                               i64, vp, vp]
+        lib.kda_oracle_chains_snap.restype = ctypes.c_int
         lib.kda_oracle_max_threads.argtypes = []
         lib.kda_oracle_max_threads.restype = ctypes.c_int
         _handle = lib
@@ -68,7 +71,7 @@ def _arr(x, dtype_code):
 
 
 def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
-           row0: Sequence[int], n: Sequence[int], s0: Optional[np.ndarray] = None):
+           row0: Sequence[int], n: Sequence[int], s0: Optional[np.ndarray] = None, snap_every: int = 0):
     """Run independent chains over shared token arrays.
 
     ``q, k, g``: rows of ``d_k`` values, ``v``: rows of ``d_v`` (storage dtype:
@@ -76,7 +79,9 @@ def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
     Chain c reads rows ``row0[c] + j*row_stride`` for ``j < n[c]``; ``s0`` is
     ``[nchains, d_k, d_v]`` fp64 (or None = zeros).
     Returns (list of ``[n[c], d_v]`` fp64 outputs, ``[nchains, d_k, d_v]`` fp64
-    final states, threads used)."""
+    final states, threads used); with ``snap_every > 0`` a fourth item, the list
+    of ``[n[c] // snap_every, d_k, d_v]`` fp64 states after every ``snap_every``
+    tokens of each chain."""
     q, k, g = _arr(q, dtype), _arr(k, dtype), _arr(g, dtype)
     v = _arr(v, dtype)
     beta = np.ascontiguousarray(beta, dtype=np.float32)
@@ -93,12 +98,23 @@ def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
     if s0 is not None:
         s0 = np.ascontiguousarray(s0, dtype=np.float64).reshape(nc, d_k, d_v)
         s0p = s0.ctypes.data
-    used = _lib().kda_oracle_chains(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, dtype,
-                                    beta.ctypes.data, row_stride, d_k, d_v, nc, r0.ctypes.data, nn.ctypes.data,
-                                    s0p, o.ctypes.data, off.ctypes.data, s_out.ctypes.data)
+    snap_every = int(snap_every)
+    if snap_every < 0:
+        raise ValueError("snap_every must be >= 0")
+    counts = nn // snap_every if snap_every > 0 else np.zeros(nc, dtype=np.int64)
+    soff = np.zeros(nc, dtype=np.int64)
+    if nc > 1:
+        soff[1:] = np.cumsum(counts[:-1])
+    snaps = np.zeros((max(int(counts.sum()), 1), d_k, d_v), dtype=np.float64)
+    used = _lib().kda_oracle_chains_snap(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, dtype,
+                                         beta.ctypes.data, row_stride, d_k, d_v, nc, r0.ctypes.data,
+                                         nn.ctypes.data, s0p, o.ctypes.data, off.ctypes.data, s_out.ctypes.data,
+                                         snap_every, snaps.ctypes.data, soff.ctypes.data)
     if used < 0:
         raise ValueError("kda_oracle_chains: bad arguments")
     outs = [o[off[c]: off[c] + nn[c] * d_v].reshape(int(nn[c]), d_v) for c in range(nc)]
+    if snap_every > 0:
+        return outs, s_out, used, [snaps[soff[c]: soff[c] + counts[c]] for c in range(nc)]
     return outs, s_out, used
 
 

@@ -60,10 +60,14 @@ static double decay_alpha(double logit) {
  *   of its array (d = d_k or d_v).  beta: element row0 + j*row_stride.
  *   s0: d_k x d_v initial state (row major, d_v contiguous) or NULL for zeros.
  *   o:  n x d_v outputs; s_out: d_k x d_v final state (both fp64, may be NULL).
+ *   snaps: with snap_every > 0, the state after the first m * snap_every tokens
+ *   (the prefix-cache snapshots of the first page's §9) for m = 1 .. n / snap_every,
+ *   one d_k x d_v matrix each (may be NULL).
  */
 static void run_chain(const void* q, const void* k, const void* v, const void* g, int dtype,
                       const float* beta, int64_t row0, int64_t row_stride, int64_t n,
-                      int32_t d_k, int32_t d_v, const double* s0, double* o, double* s_out) {
+                      int32_t d_k, int32_t d_v, const double* s0, double* o, double* s_out,
+                      int64_t snap_every, double* snaps) {
   double* S = (double*)calloc((size_t)d_k * d_v, sizeof(double));
   double* kk = (double*)malloc(sizeof(double) * d_k);
   double* qq = (double*)malloc(sizeof(double) * d_k);
@@ -99,6 +103,9 @@ static void run_chain(const void* q, const void* k, const void* v, const void* g
         o[j * d_v + c] = acc;
       }
     }
+    /* 6. snapshot of the state after j + 1 tokens */
+    if (snaps && snap_every > 0 && (j + 1) % snap_every == 0)
+      memcpy(snaps + ((j + 1) / snap_every - 1) * (int64_t)d_k * d_v, S, sizeof(double) * (size_t)d_k * d_v);
   }
   if (s_out) memcpy(s_out, S, sizeof(double) * (size_t)d_k * d_v);
   free(S);
@@ -112,15 +119,18 @@ static void run_chain(const void* q, const void* k, const void* v, const void* g
  * Many independent chains, OpenMP over chains.  Chain c covers n[c] tokens
  * whose first row is row0[c] (rows advance by row_stride); its initial state is
  * s0 + c*d_k*d_v (s0 may be NULL), its outputs go to o + o_off[c] (n[c] x d_v)
- * and s_out + c*d_k*d_v (either may be NULL).
+ * and s_out + c*d_k*d_v (either may be NULL).  With snap_every > 0 its
+ * n[c] / snap_every snapshots go to snaps + snap_off[c]*d_k*d_v.
  * Returns the number of threads used, or -1 on bad arguments.
  */
-int kda_oracle_chains(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
-                      const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
-                      const int64_t* row0, const int64_t* n, const double* s0, double* o,
-                      const int64_t* o_off, double* s_out) {
+int kda_oracle_chains_snap(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
+                           const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
+                           const int64_t* row0, const int64_t* n, const double* s0, double* o,
+                           const int64_t* o_off, double* s_out, int64_t snap_every, double* snaps,
+                           const int64_t* snap_off) {
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return -1;
-  if (d_k <= 0 || d_v <= 0 || nchains < 0 || row_stride <= 0) return -1;
+  if (d_k <= 0 || d_v <= 0 || nchains < 0 || row_stride <= 0 || snap_every < 0) return -1;
+  if (snap_every > 0 && snaps && !snap_off) return -1;
   int used = 1;
 #pragma omp parallel
   {
@@ -134,10 +144,19 @@ int kda_oracle_chains(const void* q, const void* k, const void* v, const void* g
     for (int32_t c = 0; c < nchains; ++c) {
       const int64_t dd = (int64_t)d_k * d_v;
       run_chain(q, k, v, g, dtype, beta, row0[c], row_stride, n[c], d_k, d_v, s0 ? s0 + c * dd : NULL,
-                o ? o + o_off[c] : NULL, s_out ? s_out + c * dd : NULL);
+                o ? o + o_off[c] : NULL, s_out ? s_out + c * dd : NULL, snap_every,
+                (snap_every > 0 && snaps) ? snaps + snap_off[c] * dd : NULL);
     }
   }
   return used;
+}
+
+int kda_oracle_chains(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
+                      const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
+                      const int64_t* row0, const int64_t* n, const double* s0, double* o,
+                      const int64_t* o_off, double* s_out) {
+  return kda_oracle_chains_snap(q, k, v, g, dtype, beta, row_stride, d_k, d_v, nchains, row0, n, s0, o, o_off,
+                                s_out, 0, NULL, NULL);
 }
 
 int kda_oracle_max_threads(void) {

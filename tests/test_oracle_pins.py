@@ -138,6 +138,78 @@ def test_brute_force_transition_product(seed):
         np.testing.assert_allclose(o[m - 1], St.T @ q[m - 1], rtol=1e-12, atol=1e-13)
 
 
+def _brute_states(q, k, v, g, beta, s0):
+    """S_t for t = 1..n from explicit transition matrices M_t = (I - beta_t k_t k_t^T) Diag(alpha_t)."""
+    alpha = np.exp(-5.0 / (1.0 + np.exp(-g)))
+    d_k = k.shape[1]
+    St, out = np.array(s0, dtype=np.float64), []
+    for t in range(len(q)):
+        M = (np.eye(d_k) - float(beta[t]) * np.outer(k[t], k[t])) @ np.diag(alpha[t])
+        St = M @ St + float(beta[t]) * np.outer(k[t], v[t])
+        out.append(St.copy())
+    return out
+
+
+@pytest.mark.parametrize("every", [1, 2, 3, 7])
+def test_snapshots_match_brute_force_states(every):
+    """State snapshots (the prefix-cache states of the first page's §9): the
+    m-th snapshot of a chain is S after its first m*every tokens, checked
+    against explicit transition-matrix products for several chains of
+    different lengths (one of them empty) sharing the token arrays."""
+    rng = np.random.default_rng(300 + every)
+    H, d_k, d_v = 3, 3, 4
+    lens = [9, 0, 14]
+    n = max(lens)
+    q, k, v, g, beta = _rand_inputs(rng, n * H, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(H, d_k, d_v))
+    outs, S, _, snaps = oracle.chains(q, k, v, g, beta, oracle.F64, d_k, d_v, H, list(range(H)), lens, s0,
+                                      snap_every=every)
+    for h, L in enumerate(lens):
+        rows = slice(h, h + H * L, H) if L else slice(0, 0)
+        ref = _brute_states(q[rows], k[rows], v[rows], g[rows], beta[rows], s0[h])
+        assert snaps[h].shape == (L // every, d_k, d_v)
+        for m in range(1, L // every + 1):
+            np.testing.assert_allclose(snaps[h][m - 1], ref[m * every - 1], rtol=1e-12, atol=1e-13)
+        if L and L % every == 0:
+            np.testing.assert_array_equal(snaps[h][-1], S[h])
+
+
+def test_snapshot_planted_off_by_one_fails_the_pin(tmp_path):
+    """A snapshot taken one token early, planted in a compiled copy of the
+    oracle, is rejected by the brute-force state comparison."""
+    import ctypes
+    import subprocess
+
+    src = open(oracle._SRC).read()
+    old = "(j + 1) % snap_every == 0)"
+    assert src.count(old) == 1
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, "(j + 2) % snap_every == 0 && j + 2 <= n)").replace(
+        "memcpy(snaps + ((j + 1) / snap_every - 1)", "memcpy(snaps + ((j + 2) / snap_every - 1)"))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fopenmp", "-fPIC", "-shared", str(mpath), "-o", str(so), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.kda_oracle_chains_snap.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                           i64, vp, vp]
+    lib.kda_oracle_chains_snap.restype = ctypes.c_int
+    rng = np.random.default_rng(17)
+    n, d_k, d_v, every = 8, 3, 4, 4
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = np.zeros((n, d_v)), np.zeros((d_k, d_v))
+    snaps = np.zeros((n // every, d_k, d_v))
+    z, nn = np.zeros(1, np.int64), np.array([n], np.int64)
+    arrs = [np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, g)]
+    assert lib.kda_oracle_chains_snap(*(a.ctypes.data for a in arrs), oracle.F64, beta.ctypes.data, 1, d_k, d_v, 1,
+                                      z.ctypes.data, nn.ctypes.data, s0.ctypes.data, o.ctypes.data, z.ctypes.data,
+                                      S.ctypes.data, every, snaps.ctypes.data, z.ctypes.data) > 0
+    ref = _brute_states(q, k, v, g, beta, s0)
+    err = max(np.abs(snaps[m - 1] - ref[m * every - 1]).max() for m in range(1, n // every + 1))
+    assert err > 1e-6, f"off-by-one snapshot was not caught (err {err:g})"
+
+
 def test_gate_lower_bound_tile_edge():
     """All logits +30: alpha sits on the e^{-5} bound, and 16 steps reach a
     cumulative log-decay of -80, the edge of the 16-token tile bound (§3.3).
