@@ -105,6 +105,38 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
                          cudaStream_t stream);
 
 /*
+ * Chunked prefill that also keeps the recurrent state every
+ * `snapshot_interval` tokens of each sequence: the state snapshots that page
+ * "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §9 stores every 512 tokens so that a
+ * prefix cache can resume a sequence at any such boundary without recomputing
+ * it.  Arguments, layouts, results and errors are those of kda_chunk_fwd, plus:
+ *  snapshots          device fp32 [slots][H][d_k][d_v] (d_v contiguous), owned by
+ *                     the caller, 16-byte aligned, overlapping no other argument.
+ *                     Snapshot m (m = 1 .. floor(len_s / snapshot_interval)) of
+ *                     sequence s is the state after its first m * snapshot_interval
+ *                     tokens, stored at slot first(s) + m - 1, where first(s) is the
+ *                     number of snapshots of the sequences before s (sequence
+ *                     order).  Without cu_seqlens that is slot
+ *                     s * floor(T / snapshot_interval) + m - 1.  Slots beyond the
+ *                     snapshots taken are not written.
+ *  snapshot_interval  tokens between snapshots, a positive multiple of 64.
+ *  snapshot_capacity  slots available in `snapshots`; must be at least
+ *                     B * floor(T / snapshot_interval) (batched) or
+ *                     floor(T / snapshot_interval) (cu_seqlens, an upper bound of
+ *                     the total), else KDA_ERR_INVALID_ARG before anything is
+ *                     launched.  `snapshots` may be NULL only when that bound is 0.
+ * The snapshot at a sequence's last token (length a multiple of the interval)
+ * equals its final state.  Uses the same workspace as kda_chunk_fwd.
+ */
+KDA_API kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const void* v, const void* g,
+                                           const float* beta, const float* initial_state,
+                                           const int32_t* cu_seqlens, int32_t num_seqs, int64_t B, int64_t T,
+                                           int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                                           float* final_state, float* snapshots, int32_t snapshot_interval,
+                                           int64_t snapshot_capacity, void* workspace, size_t workspace_bytes,
+                                           cudaStream_t stream);
+
+/*
  * One decode step for N independent sequences (one new token each), the
  * single-token interface of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读"
  * §3.2 restricted to the recurrence: (q, k, v, g, beta, S_{t-1}) -> (o_t, S_t).

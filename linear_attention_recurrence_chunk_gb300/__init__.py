@@ -12,6 +12,9 @@ Functions keep the C names:
   -> ``(o, final_state)``: chunked prefill (page "Kimi K3：架构、训练与百万 Token
   Agentic RL 技术解读" §3.3), q/k/g ``[B, T, H, d_k]``, v ``[B, T, H, d_v]``,
   beta ``[B, T, H]`` fp32, states ``[S, H, d_k, d_v]`` fp32.
+* ``kda_chunk_fwd_snapshots(q, k, v, g, beta, snapshot_interval, ...)`` ->
+  ``(o, final_state, snapshots)``: the same, also keeping the state every
+  ``snapshot_interval`` tokens of each sequence (same page §9, prefix cache).
 * ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
   sequence (same page §3.2), state updated in place.
 * ``kda_chunk_fwd_workspace_size(...)``, ``kda_device_error()``,
@@ -27,7 +30,7 @@ import torch
 
 from . import _build
 
-__all__ = ["kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_decode_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
            "kda_check_wait_timeout", "KdaError", "library_path", "load_library", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
@@ -66,6 +69,9 @@ def load_library():
     lib.kda_chunk_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int, vp, vp,
                                   vp, sz, vp]
     lib.kda_chunk_fwd.restype = ctypes.c_int
+    lib.kda_chunk_fwd_snapshots.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int,
+                                            vp, vp, vp, i32, i64, vp, sz, vp]
+    lib.kda_chunk_fwd_snapshots.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -131,6 +137,44 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "kda_chunk_fwd")
     return o, final_state
+
+
+def kda_chunk_fwd_snapshots(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                            beta: torch.Tensor, snapshot_interval: int, initial_state: Optional[torch.Tensor] = None,
+                            cu_seqlens: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                            o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                            snapshots: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor], torch.Tensor]:
+    """Chunked prefill that also keeps the state every ``snapshot_interval``
+    tokens (a multiple of 64) of each sequence.  Returns ``(o, final_state,
+    snapshots)``; ``snapshots`` is ``[slots, H, d_k, d_v]`` fp32 with
+    ``slots = B * (T // snapshot_interval)`` (batched) or ``T // snapshot_interval``
+    (``cu_seqlens``: an upper bound, the sequences' snapshots come first, in
+    sequence order)."""
+    lib = load_library()
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    num_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((num_seqs, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    interval = int(snapshot_interval)
+    cap = (B * (T // interval) if cu_seqlens is None else (B * T) // interval) if interval > 0 else 0
+    if snapshots is None:
+        snapshots = torch.empty((max(cap, 1), H, d_k, d_v), dtype=torch.float32, device=q.device)
+    ws_bytes = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd_snapshots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                     _ptr(cu_seqlens), num_seqs, B, T, H, d_k, d_v, _dtype_code(q), _ptr(o),
+                                     _ptr(final_state), _ptr(snapshots), interval,
+                                     snapshots.shape[0] if cap > 0 else 0, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "kda_chunk_fwd_snapshots")
+    return o, final_state, snapshots[:cap]
 
 
 def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,

@@ -101,10 +101,17 @@ size_t kda_chunk_fwd_workspace_size(int64_t B, int64_t T, int32_t H, int32_t d_k
   return kda::chunk_workspace_layout(B * T, num_seqs, H, d_k, d_v, dt).bytes;
 }
 
-kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const float* beta,
-                         const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
-                         int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o, float* final_state,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// kda_chunk_fwd with optional state snapshots every snapshot_interval tokens
+// (snapshots == nullptr and snapshot_interval == 0: none).
+kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                          const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
+                          int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                          float* final_state, float* snapshots, int32_t snapshot_interval,
+                          int64_t snapshot_capacity, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   const bool varlen = cu_seqlens != nullptr;
   kda_status st = check_chunk_shape(B, T, H, d_k, d_v, num_seqs, dt, varlen);
   if (st != KDA_OK) return st;
@@ -139,6 +146,22 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
   if (final_state && initial_state && final_state != initial_state && overlaps(final_state, ns, initial_state, ns))
     return KDA_ERR_INVALID_ARG;
 
+  // Snapshots: every snapshot_interval tokens (a positive multiple of the
+  // 64-token chunk) of each sequence; floor(T / interval) slots per batched
+  // sequence, floor(total tokens / interval) bound the varlen total.
+  if (snapshot_interval != 0 || snapshots) {
+    if (snapshot_interval <= 0 || snapshot_interval % kda::kChunk != 0 || snapshot_capacity < 0)
+      return KDA_ERR_INVALID_ARG;
+    const int64_t need = varlen ? tokens / snapshot_interval : B * (T / snapshot_interval);
+    if (snapshot_capacity < need || (need > 0 && !snapshots)) return KDA_ERR_INVALID_ARG;
+    if (snapshots && !aligned16(snapshots)) return KDA_ERR_INVALID_ARG;
+    const size_t nsnap = (size_t)snapshot_capacity * H * d_k * d_v * sizeof(float);
+    const Range all[] = {{q, nqk}, {k, nqk}, {g, nqk}, {v, nv}, {beta, nb}, {initial_state, ns},
+                         {cu_seqlens, ncu}, {o, nv}, {final_state, ns}, {workspace, ws.bytes}};
+    for (const Range& r : all)
+      if (overlaps(snapshots, nsnap, r.p, r.n)) return KDA_ERR_INVALID_ARG;
+  }
+
   if (num_seqs == 0) return KDA_OK;
 
   int32_t* dev_err = nullptr;
@@ -148,7 +171,33 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.s0 = initial_state;
   p.cu = cu_seqlens; p.num_seqs = num_seqs; p.T_seq = varlen ? 0 : T; p.total_tokens = tokens;
   p.H = H; p.d_k = d_k; p.d_v = d_v; p.dt = dt; p.o = o; p.s_final = final_state; p.dev_err = dev_err;
+  p.snaps = snapshots;
+  p.snap_every = snapshots ? snapshot_interval / kda::kChunk : 0;
   return kda::launch_chunk_fwd(p, ws, workspace, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
+                         int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o, float* final_state,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
+                        final_state, nullptr, 0, 0, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                                   const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs,
+                                   int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                                   float* final_state, float* snapshots, int32_t snapshot_interval,
+                                   int64_t snapshot_capacity, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  if (snapshot_interval <= 0) return KDA_ERR_INVALID_ARG;
+  return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
+                        final_state, snapshots, snapshot_interval, snapshot_capacity, workspace, workspace_bytes,
+                        stream);
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g, const float* beta,

@@ -32,6 +32,7 @@ namespace kda {
 __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restrict__ cu, int32_t num_seqs,
                                                          int64_t T_seq, int64_t total, int32_t* seq_chunk0,
                                                          int4* chunk_info, int32_t* seq_order, int32_t max_chunks,
+                                                         int32_t snap_every, int32_t* snap_slot0,
                                                          int32_t* dev_err) {
   __shared__ int32_t s_scan[1024];
   __shared__ int32_t s_carry;
@@ -51,30 +52,38 @@ __global__ void __launch_bounds__(1024) chunk_map_kernel(const int32_t* __restri
     if (tid == 0) seq_chunk0[num_seqs] = -1;
     return;
   }
-  if (tid == 0) s_carry = 0;
-  __syncthreads();
-  for (int base = 0; base < num_seqs; base += blockDim.x) {
-    const int s = base + tid;
-    int32_t n = 0;
-    if (s < num_seqs) {
-      const int64_t len = cu ? (int64_t)(cu[s + 1] - cu[s]) : T_seq;
-      n = (int32_t)((len + kChunk - 1) / kChunk);
-    }
-    s_scan[tid] = n;
+  // Exclusive scans over the sequences: pass 0 the chunk counts (-> seq_chunk0),
+  // pass 1 the snapshot counts, floor(len / (64 snap_every)) (-> snap_slot0).
+  int32_t n_chunks = 0;
+  for (int pass = 0; pass < (snap_every > 0 ? 2 : 1); ++pass) {
+    int32_t* dst = pass == 0 ? seq_chunk0 : snap_slot0;
+    if (tid == 0) s_carry = 0;
     __syncthreads();
-    for (int off = 1; off < (int)blockDim.x; off <<= 1) {  // inclusive Hillis-Steele scan
-      const int32_t add = tid >= off ? s_scan[tid - off] : 0;
+    for (int base = 0; base < num_seqs; base += blockDim.x) {
+      const int s = base + tid;
+      int32_t n = 0;
+      if (s < num_seqs) {
+        const int64_t len = cu ? (int64_t)(cu[s + 1] - cu[s]) : T_seq;
+        n = pass == 0 ? (int32_t)((len + kChunk - 1) / kChunk) : (int32_t)(len / ((int64_t)kChunk * snap_every));
+      }
+      s_scan[tid] = n;
       __syncthreads();
-      s_scan[tid] += add;
+      for (int off = 1; off < (int)blockDim.x; off <<= 1) {  // inclusive Hillis-Steele scan
+        const int32_t add = tid >= off ? s_scan[tid - off] : 0;
+        __syncthreads();
+        s_scan[tid] += add;
+        __syncthreads();
+      }
+      const int32_t start = s_carry + s_scan[tid] - n;
+      if (s < num_seqs) dst[s] = start;
+      __syncthreads();
+      if (tid == blockDim.x - 1) s_carry += s_scan[tid];
       __syncthreads();
     }
-    const int32_t start = s_carry + s_scan[tid] - n;
-    if (s < num_seqs) seq_chunk0[s] = start;
-    __syncthreads();
-    if (tid == blockDim.x - 1) s_carry += s_scan[tid];
+    if (pass == 0) n_chunks = min(s_carry, max_chunks);
+    else if (tid == 0) dst[num_seqs] = s_carry;
     __syncthreads();
   }
-  const int32_t n_chunks = min(s_carry, max_chunks);
   if (tid == 0) seq_chunk0[num_seqs] = n_chunks;
   __syncthreads();
   // Per chunk: its sequence (the last s with seq_chunk0[s] <= j, which skips
@@ -404,6 +413,12 @@ __global__ void __launch_bounds__(kChainThreads) chunk_chain_simt(const int32_t*
     __syncthreads();
 #pragma unroll
     for (int ii = 0; ii < DK / NW; ++ii) sS[(warp + ii * NW) * BV + lane] = snew[ii];
+    const int64_t slot = snapshot_slot(map, s, j - j0, seq_end - seq_start);
+    if (slot >= 0) {
+#pragma unroll
+      for (int ii = 0; ii < DK / NW; ++ii)
+        map.snaps[((slot * H + h) * DK + warp + ii * NW) * DV + n0 + lane] = snew[ii];
+    }
     __syncthreads();
   }
 
@@ -434,7 +449,8 @@ Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t
   w.off_seq_chunk0 = 0;
   w.off_chunk_info = align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
   w.off_seq_order = w.off_chunk_info + align256(sizeof(int4) * (size_t)std::max<int64_t>(max_chunks, 1));
-  w.off_inter = w.off_seq_order + align256(sizeof(int32_t) * (size_t)std::max<int32_t>(num_seqs, 1));
+  w.off_snap_slot0 = w.off_seq_order + align256(sizeof(int32_t) * (size_t)std::max<int32_t>(num_seqs, 1));
+  w.off_inter = w.off_snap_slot0 + align256(sizeof(int32_t) * ((size_t)num_seqs + 1));
   const size_t R = (size_t)max_chunks * (size_t)H;
   if (w.tc) {
     w.off_wq = w.off_inter;
@@ -491,11 +507,15 @@ cudaError_t launch_chunk_fwd(const ChunkProblem& p, const Workspace& ws, void* w
   map.chunk_info = reinterpret_cast<int4*>(base + ws.off_chunk_info);
   map.seq_order = reinterpret_cast<int32_t*>(base + ws.off_seq_order);
   map.max_chunks = ws.max_chunks;
+  map.snaps = p.snap_every > 0 ? p.snaps : nullptr;
+  map.snap_slot0 = reinterpret_cast<int32_t*>(base + ws.off_snap_slot0);
+  map.snap_every = p.snaps ? p.snap_every : 0;
   float* inter = reinterpret_cast<float*>(base + ws.off_inter);
 
   prof_begin(stream, "chunk_map");
   chunk_map_kernel<<<1, 1024, 0, stream>>>(p.cu, p.num_seqs, p.T_seq, p.total_tokens, map.seq_chunk0,
-                                           map.chunk_info, map.seq_order, map.max_chunks, p.dev_err);
+                                           map.chunk_info, map.seq_order, map.max_chunks, map.snap_every,
+                                           map.snap_slot0, p.dev_err);
   prof_end(stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

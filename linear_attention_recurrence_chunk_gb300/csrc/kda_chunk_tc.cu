@@ -1070,6 +1070,11 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(s_ready);
       }
+      if (const int64_t slot = snapshot_slot(map, s, i, seq_end - seq_start); slot >= 0) {
+        float* dst = map.snaps + ((slot * H + h) * DK + c) * DV + n0 + 16 * hf;
+#pragma unroll
+        for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+      }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
@@ -1342,6 +1347,11 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(s_ready);
+      }
+      if (const int64_t slot = snapshot_slot(map, s, i, seq_end - seq_start); slot >= 0) {
+        float* dst = map.snaps + ((slot * H + h) * DK + c) * DV + n0 + 32 * cg;
+#pragma unroll
+        for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
       }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);

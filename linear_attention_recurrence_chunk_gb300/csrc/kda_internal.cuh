@@ -40,13 +40,29 @@ __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-// Sequence -> chunk map built on the device from cu_seqlens (or from B, T).
+// Sequence -> chunk map built on the device from cu_seqlens (or from B, T),
+// plus where the state snapshots of each sequence go.
 struct ChunkMap {
   int32_t* seq_chunk0;   // [num_seqs + 1] first global chunk of each sequence (exclusive scan)
   int4* chunk_info;      // [max_chunks] per global chunk: (sequence, rows, first token low, high word)
   int32_t* seq_order;    // [num_seqs] sequences by decreasing chunk count (the chain's launch order)
   int32_t max_chunks;    // upper bound used to size the grid
+  // State snapshots (page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §9: the
+  // recurrent state kept every 512 tokens for the prefix cache): with
+  // snap_every > 0, the state after every snap_every full chunks of a sequence
+  // is written to snaps [slot][H][d_k][d_v], slot = snap_slot0[s] + m - 1 for
+  // the m-th snapshot of sequence s.
+  float* snaps;
+  int32_t* snap_slot0;   // [num_seqs + 1] first snapshot slot of each sequence (exclusive scan)
+  int32_t snap_every;    // chunks between snapshots, 0 = none
 };
+
+// Snapshot slot of the state after local chunk i (0-based) of sequence s, whose
+// length is len tokens, or -1 when no snapshot is taken there.
+__device__ __forceinline__ int64_t snapshot_slot(const ChunkMap& m, int32_t s, int32_t i, int64_t len) {
+  if (m.snap_every <= 0 || (i + 1) % m.snap_every != 0 || (int64_t)(i + 1) * kChunk > len) return -1;
+  return (int64_t)m.snap_slot0[s] + (i + 1) / m.snap_every - 1;
+}
 
 // Where chunk j of the map lives in the packed token array.
 struct ChunkPos {
@@ -83,6 +99,8 @@ struct ChunkProblem {
   kda_dtype dt;
   void* o;
   float* s_final;
+  float* snaps;          // state snapshots or nullptr
+  int32_t snap_every;    // chunks between snapshots (0 = none)
   int32_t* dev_err;
 };
 
@@ -91,7 +109,7 @@ struct ChunkProblem {
 // separate arrays so that each can be read with 2D TMA tiles.
 struct Workspace {
   size_t bytes;
-  size_t off_seq_chunk0, off_chunk_info, off_seq_order, off_inter;
+  size_t off_seq_chunk0, off_chunk_info, off_seq_order, off_snap_slot0, off_inter;
   int32_t max_chunks;
   size_t inter_bytes_per_chunk_head;
   bool tc;

@@ -89,6 +89,35 @@ def test_chunk_fwd_rejects_bad_arguments_on_host():
     assert _chunk(lib, B=0, num_seqs=0) == 0
 
 
+def _snap(lib, **kw):
+    args = dict(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), g=FAKE + (3 << 30), beta=FAKE + (4 << 30),
+                s0=None, cu=None, num_seqs=2, B=2, T=1024, H=2, dk=128, dv=128, dt=1, o=FAKE + (5 << 30),
+                sf=None, snaps=FAKE + (8 << 30), interval=512, cap=4, ws=FAKE + (6 << 30), wsb=1 << 40)
+    args.update(kw)
+    return lib.kda_chunk_fwd_snapshots(args["q"], args["k"], args["v"], args["g"], args["beta"], args["s0"],
+                                       args["cu"], args["num_seqs"], args["B"], args["T"], args["H"], args["dk"],
+                                       args["dv"], args["dt"], args["o"], args["sf"], args["snaps"],
+                                       args["interval"], args["cap"], args["ws"], args["wsb"], None)
+
+
+def test_chunk_fwd_snapshots_rejects_bad_arguments_on_host():
+    lib = kda.load_library()
+    assert _snap(lib, interval=0) == 1                          # no interval
+    assert _snap(lib, interval=-64) == 1
+    assert _snap(lib, interval=100) == 1                        # not a multiple of the 64-token chunk
+    assert _snap(lib, cap=3) == 1                               # B * floor(T / interval) = 4 slots needed
+    assert _snap(lib, cap=-1) == 1
+    assert _snap(lib, snaps=None) == 1                          # snapshots needed but no buffer
+    assert _snap(lib, snaps=FAKE + (8 << 30) + 4) == 1          # 16-byte alignment
+    assert _snap(lib, snaps=FAKE + (2 << 30) + 64) == 1         # overlaps v
+    assert _snap(lib, snaps=FAKE + (5 << 30) + 64) == 1         # overlaps o
+    # varlen: floor(T / interval) slots bound the total
+    assert _snap(lib, B=1, num_seqs=3, cu=FAKE + (7 << 30), T=2048, cap=3) == 1
+    assert _snap(lib, q=None) == 1                              # the kda_chunk_fwd checks still apply
+    assert _snap(lib, dk=96) == 2
+    assert _snap(lib, B=0, num_seqs=0, cap=0) == 0              # nothing to do, no CUDA call
+
+
 def test_decode_rejects_bad_arguments_on_host():
     lib = kda.load_library()
     f = lib.kda_decode_step
