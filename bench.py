@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-snapshots", action="store_true")
+    ap.add_argument("--snapshot-interval", type=int, default=512)
     ap.add_argument("--decode-steps", type=int, default=100)
     ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD, "prefill_b8_h96_t8192_d128",
                                            "varlen_12seq_1m_h32_d128"], default=WORKLOAD,
@@ -147,9 +149,26 @@ def _collect(lib, max_records=4096):
     return seen, recs
 
 
-def _kernel_src_sha() -> str:
+# Source text each kernel's machine code depends on: the shared headers, plus
+# its own translation unit with the other kernels' sections cut out (marker
+# lines of kda_chunk_tc.cu), so that a change elsewhere does not invalidate a
+# committed ncu traffic figure.
+_TC_SECTIONS = {"chunk_prep_tc": [("// -------------------------------------------------------------- chain kernel",
+                                   "// --------------------------------------------------------------- host side")]}
+
+
+def _kernel_src_sha(kernel: str = "") -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "linear_attention_recurrence_chunk_gb300", "csrc")
+    if kernel in _TC_SECTIONS:
+        for fn in ("kda_internal.cuh", "tc_ptx.cuh"):
+            h.update(open(os.path.join(d, fn), "rb").read())
+        text = open(os.path.join(d, "kda_chunk_tc.cu"), encoding="utf-8").read()
+        for a, b in _TC_SECTIONS[kernel]:
+            i, j = text.index(a), text.index(b)
+            text = text[:i] + text[j:]
+        h.update(text.encode("utf-8"))
+        return h.hexdigest()[:16]
     for fn in sorted(os.listdir(d)):
         if fn.endswith((".cu", ".cuh")):
             h.update(open(os.path.join(d, fn), "rb").read())
@@ -162,7 +181,7 @@ def _traffic_from_profiles(kernel: str, units_per_launch: float):
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    sha = _kernel_src_sha()
+    sha = _kernel_src_sha(kernel)
     pat = re.compile(r"^traffic:\s+kernel=(\S+)\s+dram_bytes_per_unit=([0-9.eE+-]+)\s+src_sha=(\S+)")
     for fn in sorted(os.listdir(pdir)):
         if not fn.endswith((".md", ".txt")):
@@ -298,6 +317,45 @@ def bench_prefill(args, ws_size, local):
         per_kernel.setdefault(nm, []).append(ms)
     return {"w": w, "t": t, "elapsed_ms": elapsed_ms, "max_ms": max_ms, "launches": seen,
             "per_kernel": per_kernel, "clocks": clocks, "o": o, "sf": sf, "wsp": wsp}
+
+
+def bench_snapshots(args, r, steps):
+    """The same prefill with the state kept every ``--snapshot-interval`` tokens
+    (the prefix-cache snapshots, 512 tokens on the pages), timed with CUDA
+    events on the launch stream like the main leg."""
+    import torch
+
+    import linear_attention_recurrence_chunk_gb300 as kda
+
+    w, t = r["w"], r["t"]
+    every = args.snapshot_interval
+    slots = (w.tokens // every) if t["cu"] is not None else w.B * (w.T // every)
+    snaps = torch.empty((max(slots, 1), w.H, w.d_k, w.d_v), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.kda_chunk_fwd_snapshots(t["q"], t["k"], t["v"], t["g"], t["beta"], every, initial_state=t["s0"],
+                                    cu_seqlens=t["cu"], o=r["o"], final_state=r["sf"], snapshots=snaps,
+                                    workspace=r["wsp"], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, code = kda.kda_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {code} in the snapshot leg")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    plain_ms = r["elapsed_ms"] / args.steps
+    del snaps
+    return {"interval_tokens": every, "snapshots_per_step": slots * w.H,
+            "snapshot_bytes_per_step": slots * w.H * w.d_k * w.d_v * 4, "value": w.tokens / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "slowdown_vs_plain": ms / plain_ms}
 
 
 def bench_e2e(args, w, wsp, steps):
@@ -497,6 +555,8 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if not args.no_snapshots:
+        line["snapshots"] = bench_snapshots(args, r, max(3, steps // 10))
     if not args.no_e2e:
         line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
         if ws_size > 1:
