@@ -150,6 +150,41 @@ KDA_API kda_status kda_decode_step(const void* q, const void* k, const void* v, 
                            void* o, cudaStream_t stream);
 
 /*
+ * Fused decode step of a whole KDA layer from the token's per-head
+ * projections, for N sequences (page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读"
+ * §3.2: the interface (x_t, S_{t-1}, C^conv_{t-1}) -> (y_t, S_t, C^conv_t) and the
+ * input branches; §3.3: the lower-bounded gate; §3.2: the gated output), up to
+ * the output projection W_o:
+ *   [q; k; v] = Swish(ShortConv([q_in; k_in; v_in]))  per channel, causal, width
+ *               conv_width: y = sum_j w[j] x_{t-W+1+j} (tap W-1 on the current token)
+ *   q, k      = q / sqrt(|q|^2 + eps_l2), k / sqrt(|k|^2 + eps_l2)
+ *   log alpha = -5 Sigmoid(exp(A_log[h]) z),  beta = Sigmoid(beta_logit)
+ *   S, o~     = the kda_decode_step recurrence on these
+ *   o         = Sigmoid(out_gate) * o~ / sqrt(mean(o~^2) + eps_rms) * norm_weight
+ *               (per head over d_v), or o = o~ when out_gate is NULL.
+ *  q_in, k_in, z [N, H, d_k], v_in [N, H, d_v], out_gate [N, H, d_v]: dtype dt
+ *      (the projections W_q x, W_k x, W_v x, the gate input z, W_g x);
+ *  A_log [H], beta_logit [N, H]: fp32;
+ *  conv_cache [N, H, conv_width - 1, 2 d_k + d_v] dtype dt, read and updated in
+ *      place: the previous conv_width - 1 inputs of the q, k, v channels (in that
+ *      order), oldest first; zeros for a new sequence; may be NULL when
+ *      conv_width = 1;
+ *  conv_weight [H, 2 d_k + d_v, conv_width] fp32;  conv_width in 1..8;
+ *  state [N, H, d_k, d_v] fp32, 16-byte aligned, updated in place;
+ *  norm_weight [H, d_v] fp32 or NULL (ones);  eps_l2, eps_rms >= 0;
+ *  o [N, H, d_v] dtype dt.
+ * Other arrays need their element alignment.  o, state and conv_cache overlap no
+ * input and no one another.  N = 0 is a no-op.  Errors as kda_decode_step.
+ */
+KDA_API kda_status kda_decode_layer_step(const void* q_in, const void* k_in, const void* v_in, const void* z,
+                                         const float* A_log, const float* beta_logit, void* conv_cache,
+                                         const float* conv_weight, int32_t conv_width, float* state,
+                                         const void* out_gate, const float* norm_weight, float eps_l2,
+                                         float eps_rms, int32_t N, int32_t H, int32_t d_k, int32_t d_v,
+                                         kda_dtype dt, void* o, cudaStream_t stream);
+
+/*
+ * Reads and clears this device's error word/*
  * Reads and clears this device's error word (on the current device), after
  * waiting for `stream`.  *code receives the raw word (0 = none).  Returns
  * KDA_OK when it was 0, KDA_ERR_INVALID_ARG for a malformed cu_seqlens,

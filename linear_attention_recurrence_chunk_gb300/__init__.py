@@ -17,6 +17,10 @@ Functions keep the C names:
   ``snapshot_interval`` tokens of each sequence (same page §9, prefix cache).
 * ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
   sequence (same page §3.2), state updated in place.
+* ``kda_decode_layer_step(q_in, k_in, v_in, z, A_log, beta_logit, conv_cache,
+  conv_weight, state, out_gate=None, norm_weight=None)`` -> ``o``: the decode
+  step of a whole layer from the token's projections (ShortConv with its cache,
+  Swish, L2Norm, gate scale, recurrence, Sigmoid-gated RMSNorm output).
 * ``kda_chunk_fwd_workspace_size(...)``, ``kda_device_error()``,
   ``kda_check_wait_timeout(limit_cycles)`` (failure-detection check).
 """
@@ -30,7 +34,7 @@ import torch
 
 from . import _build
 
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_decode_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_decode_step", "kda_decode_layer_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
            "kda_check_wait_timeout", "KdaError", "library_path", "load_library", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
@@ -74,6 +78,10 @@ def load_library():
     lib.kda_chunk_fwd_snapshots.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.kda_decode_layer_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, f32, f32, i32, i32, i32,
+                                          i32, ctypes.c_int, vp, vp]
+    lib.kda_decode_layer_step.restype = ctypes.c_int
     lib.kda_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.kda_device_error.restype = ctypes.c_int
     lib.kda_check_wait_timeout.argtypes = [i64, vp]
@@ -189,6 +197,31 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), N, H, d_k, d_v,
                              _dtype_code(q), _ptr(o), _stream(stream))
     _check(st, "kda_decode_step")
+    return o
+
+
+def kda_decode_layer_step(q_in: torch.Tensor, k_in: torch.Tensor, v_in: torch.Tensor, z: torch.Tensor,
+                          A_log: torch.Tensor, beta_logit: torch.Tensor, conv_cache: Optional[torch.Tensor],
+                          conv_weight: torch.Tensor, state: torch.Tensor, out_gate: Optional[torch.Tensor] = None,
+                          norm_weight: Optional[torch.Tensor] = None, eps_l2: float = 1e-6, eps_rms: float = 1e-6,
+                          o: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step of a KDA layer from the token's projections.
+    q_in/k_in/z ``[N, H, d_k]``, v_in/out_gate ``[N, H, d_v]`` (input dtype),
+    A_log ``[H]``, beta_logit ``[N, H]`` fp32, conv_cache ``[N, H, W-1, 2 d_k + d_v]``
+    (input dtype, updated in place), conv_weight ``[H, 2 d_k + d_v, W]`` fp32,
+    state ``[N, H, d_k, d_v]`` fp32 (updated in place), norm_weight ``[H, d_v]``
+    fp32.  Returns o ``[N, H, d_v]``."""
+    lib = load_library()
+    N, H, d_k = q_in.shape
+    d_v = v_in.shape[-1]
+    W = conv_weight.shape[-1]
+    if o is None:
+        o = torch.empty(v_in.shape, dtype=v_in.dtype, device=v_in.device)
+    st = lib.kda_decode_layer_step(_ptr(q_in), _ptr(k_in), _ptr(v_in), _ptr(z), _ptr(A_log), _ptr(beta_logit),
+                                   _ptr(conv_cache), _ptr(conv_weight), W, _ptr(state), _ptr(out_gate),
+                                   _ptr(norm_weight), float(eps_l2), float(eps_rms), N, H, d_k, d_v,
+                                   _dtype_code(q_in), _ptr(o), _stream(stream))
+    _check(st, "kda_decode_layer_step")
     return o
 
 

@@ -225,6 +225,47 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const vo
              : KDA_ERR_CUDA;
 }
 
+kda_status kda_decode_layer_step(const void* q_in, const void* k_in, const void* v_in, const void* z,
+                                 const float* A_log, const float* beta_logit, void* conv_cache,
+                                 const float* conv_weight, int32_t conv_width, float* state, const void* out_gate,
+                                 const float* norm_weight, float eps_l2, float eps_rms, int32_t N, int32_t H,
+                                 int32_t d_k, int32_t d_v, kda_dtype dt, void* o, cudaStream_t stream) {
+  if (dt != KDA_F32 && dt != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (N < 0 || H <= 0 || (int64_t)N * H > (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (conv_width < 1 || conv_width > 8) return KDA_ERR_INVALID_ARG;
+  if (!(eps_l2 >= 0.f && eps_l2 < 1e30f) || !(eps_rms >= 0.f && eps_rms < 1e30f)) return KDA_ERR_INVALID_ARG;
+  if (!head_dims_supported(d_k, d_v)) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  const size_t eb = dtype_bytes(dt), heads = (size_t)N * H, ch = (size_t)2 * d_k + d_v;
+  const bool need_cache = conv_width > 1;
+  const void* req[] = {q_in, k_in, v_in, z, A_log, beta_logit, conv_weight, state, o};
+  for (const void* p : req)
+    if (!p) return KDA_ERR_INVALID_ARG;
+  if (need_cache && !conv_cache) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
+  const void* elem[] = {q_in, k_in, v_in, z, conv_cache, out_gate, o};
+  for (const void* p : elem)
+    if (p && (reinterpret_cast<uintptr_t>(p) % eb) != 0) return KDA_ERR_INVALID_ARG;
+  const void* f32s[] = {A_log, beta_logit, conv_weight, norm_weight};
+  for (const void* p : f32s)
+    if (p && !aligned4(p)) return KDA_ERR_INVALID_ARG;
+  struct Range { const void* p; size_t n; };
+  const size_t nqk = heads * d_k * eb, nv = heads * d_v * eb, ns = heads * d_k * d_v * sizeof(float);
+  const size_t ncache = need_cache ? heads * (size_t)(conv_width - 1) * ch * eb : 0;
+  const Range reads[] = {{q_in, nqk}, {k_in, nqk}, {v_in, nv}, {z, nqk}, {A_log, (size_t)H * 4},
+                         {beta_logit, heads * 4}, {conv_weight, (size_t)H * ch * conv_width * 4},
+                         {out_gate, out_gate ? nv : 0}, {norm_weight, norm_weight ? (size_t)H * d_v * 4 : 0}};
+  for (const Range& r : reads) {   // the three outputs overlap no input and no other output
+    if (overlaps(o, nv, r.p, r.n) || overlaps(state, ns, r.p, r.n) || overlaps(conv_cache, ncache, r.p, r.n))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, nv, state, ns) || overlaps(o, nv, conv_cache, ncache) || overlaps(state, ns, conv_cache, ncache))
+    return KDA_ERR_INVALID_ARG;
+  kda::DecodeLayerProblem p{q_in, k_in, v_in, z, A_log, beta_logit, conv_cache, conv_weight, conv_width, state,
+                            out_gate, norm_weight, eps_l2, eps_rms, N, H, d_k, d_v, dt, o};
+  return kda::launch_decode_layer(p, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_profile_enable(int32_t on) {
   g_prof_on = on != 0;
   return KDA_OK;

@@ -99,6 +99,176 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const T* __
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode layer step: the token's input branches, the recurrence step and
+// the output gate of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.2-§3.3
+// in one kernel, from the per-head projections of the token:
+//   [q; k; v] = Swish(ShortConv([W_q x; W_k x; W_v x]))   (causal depthwise, width W,
+//               the conv cache holds the W-1 previous inputs, oldest first)
+//   q, k     <- L2Norm(q), L2Norm(k)
+//   log alpha = -5 Sigmoid(e^{A^h} z),  beta = Sigmoid(beta logit)
+//   the recurrence step above,  then optionally  o = Sigmoid(gate) * RMSNorm(o) * w.
+// One CTA per (sequence, head) as above; threads take the 2 d_k + d_v conv
+// channels while the state loads are in flight.
+template <typename T>
+struct LayerArgs {
+  const T* q_in;
+  const T* k_in;
+  const T* v_in;
+  const T* z;
+  const float* A_log;
+  const float* beta_logit;
+  T* conv_cache;              // [N, H, W-1, 2 d_k + d_v]
+  const float* conv_weight;   // [H, 2 d_k + d_v, W]
+  int32_t W;
+  float* state;
+  const T* out_gate;          // [N, H, d_v] or nullptr
+  const float* norm_weight;   // [H, d_v] or nullptr (ones)
+  float eps_l2, eps_rms;
+  int32_t H;
+  T* o;
+};
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kDecodeThreads) decode_layer_kernel(const LayerArgs<T> a) {
+  constexpr int TX = DV / 4;
+  constexpr int TY = kDecodeThreads / TX;
+  constexpr int RPT = DK / TY;
+  constexpr int CH = 2 * DK + DV;   // conv channels of a head: q, then k, then v
+  static_assert(RPT * TY == DK, "row split");
+
+  __shared__ float s_k[DK], s_q[DK], s_alpha[DK], s_v[DV];
+  __shared__ __align__(16) float s_red[2][TY][DV];
+  __shared__ __align__(16) float s_delta[DV];
+  __shared__ float s_kq, s_scale[2], s_ss[DV / 32];
+
+  const int64_t head = blockIdx.x;   // n * H + h
+  const int h = (int)(head % a.H);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tx = tid % TX;
+  const int ty = tid / TX;
+
+  float4* st = reinterpret_cast<float4*>(a.state + head * DK * DV);
+  float4 S[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) S[i] = __ldcs(st + (ty + i * TY) * TX + tx);
+
+  // Input branches: conv over the cached inputs and the new one, cache shifted, Swish.
+  for (int c = tid; c < CH; c += kDecodeThreads) {
+    const T xr = c < DK ? a.q_in[head * DK + c] : (c < 2 * DK ? a.k_in[head * DK + c - DK] : a.v_in[head * DV + c - 2 * DK]);
+    const float* wc = a.conv_weight + ((int64_t)h * CH + c) * a.W;
+    T* cc = a.conv_cache + head * (int64_t)(a.W - 1) * CH + c;
+    float y = wc[a.W - 1] * to_f32(xr);
+    for (int j = 0; j < a.W - 1; ++j) {
+      const T xj = cc[(int64_t)j * CH];
+      y += wc[j] * to_f32(xj);
+      if (j > 0) cc[(int64_t)(j - 1) * CH] = xj;
+    }
+    if (a.W > 1) cc[(int64_t)(a.W - 2) * CH] = xr;
+    const float act = y * sigmoidf_(y);
+    if (c < DK) s_q[c] = act;
+    else if (c < 2 * DK) s_k[c - DK] = act;
+    else s_v[c - 2 * DK] = act;
+  }
+  const float gscale = expf(a.A_log[h]);
+  for (int i = tid; i < DK; i += kDecodeThreads)
+    s_alpha[i] = expf(-5.f * sigmoidf_(gscale * to_f32(a.z[head * DK + i])));
+  __syncthreads();
+
+  if (warp < 2) {   // L2Norm scales of q (warp 0) and k (warp 1)
+    const float* x = warp == 0 ? s_q : s_k;
+    float acc = 0.f;
+    for (int i = lane; i < DK; i += 32) acc += x[i] * x[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) s_scale[warp] = rsqrtf(acc + a.eps_l2);
+  }
+  __syncthreads();
+  for (int i = tid; i < DK; i += kDecodeThreads) {
+    s_q[i] *= s_scale[0];
+    s_k[i] *= s_scale[1];
+  }
+  __syncthreads();
+
+  if (tid < 32) {   // k . q
+    float acc = 0.f;
+    for (int i = tid; i < DK; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (tid == 0) s_kq = acc;
+  }
+
+  float4 vh = make_float4(0.f, 0.f, 0.f, 0.f), aq = vh;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int row = ty + i * TY;
+    const float al = s_alpha[row], kr = s_k[row], qr = s_q[row];
+    S[i].x *= al; S[i].y *= al; S[i].z *= al; S[i].w *= al;
+    vh.x += S[i].x * kr; vh.y += S[i].y * kr; vh.z += S[i].z * kr; vh.w += S[i].w * kr;
+    aq.x += S[i].x * qr; aq.y += S[i].y * qr; aq.z += S[i].z * qr; aq.w += S[i].w * qr;
+  }
+  reinterpret_cast<float4*>(&s_red[0][ty][0])[tx] = vh;
+  reinterpret_cast<float4*>(&s_red[1][ty][0])[tx] = aq;
+  __syncthreads();
+
+  float ov = 0.f;
+  if (tid < DV) {
+    float vhat = 0.f, acc = 0.f;
+#pragma unroll
+    for (int y = 0; y < TY; ++y) {
+      vhat += s_red[0][y][tid];
+      acc += s_red[1][y][tid];
+    }
+    const float d = sigmoidf_(a.beta_logit[head]) * (s_v[tid] - vhat);
+    s_delta[tid] = d;
+    ov = acc + s_kq * d;
+  }
+  if (a.out_gate) {   // RMSNorm over the head's d_v outputs, weight, Sigmoid gate
+    if (tid < DV) {
+      float sq = ov * ov;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0) s_ss[warp] = sq;
+    }
+    __syncthreads();
+    if (tid < DV) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < DV / 32; ++w) tot += s_ss[w];
+      const float wn = a.norm_weight ? a.norm_weight[h * DV + tid] : 1.f;
+      ov = ov * rsqrtf(tot / DV + a.eps_rms) * wn * sigmoidf_(to_f32(a.out_gate[head * DV + tid]));
+    }
+  }
+  if (tid < DV) a.o[head * DV + tid] = from_f32<T>(ov);
+  __syncthreads();
+
+  const float4 d4 = reinterpret_cast<const float4*>(s_delta)[tx];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const float kr = s_k[ty + i * TY];
+    S[i].x += kr * d4.x; S[i].y += kr * d4.y; S[i].z += kr * d4.z; S[i].w += kr * d4.w;
+    __stcs(st + (ty + i * TY) * TX + tx, S[i]);
+  }
+}
+
+template <typename T>
+cudaError_t launch_layer_typed(const LayerArgs<T>& a, int32_t N, int32_t d_k, int32_t d_v, cudaStream_t stream) {
+  const dim3 grid((unsigned)((int64_t)N * a.H));
+  prof_begin(stream, "decode_layer");
+  if (d_k == 128 && d_v == 128)
+    decode_layer_kernel<128, 128, T><<<grid, kDecodeThreads, 0, stream>>>(a);
+  else if (d_k == 128 && d_v == 64)
+    decode_layer_kernel<128, 64, T><<<grid, kDecodeThreads, 0, stream>>>(a);
+  else if (d_k == 64 && d_v == 128)
+    decode_layer_kernel<64, 128, T><<<grid, kDecodeThreads, 0, stream>>>(a);
+  else
+    decode_layer_kernel<64, 64, T><<<grid, kDecodeThreads, 0, stream>>>(a);
+  prof_end(stream);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const void* g, const float* beta,
                          float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, void* o,
@@ -129,6 +299,23 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v, cons
                                void* o, cudaStream_t stream) {
   if (dt == KDA_F32) return launch_typed<float>(q, k, v, g, beta, state, N, H, d_k, d_v, o, stream);
   return launch_typed<__nv_bfloat16>(q, k, v, g, beta, state, N, H, d_k, d_v, o, stream);
+}
+
+cudaError_t launch_decode_layer(const DecodeLayerProblem& p, cudaStream_t stream) {
+  if (p.dt == KDA_F32) {
+    const LayerArgs<float> a{static_cast<const float*>(p.q_in), static_cast<const float*>(p.k_in),
+                             static_cast<const float*>(p.v_in), static_cast<const float*>(p.z), p.A_log, p.beta_logit,
+                             static_cast<float*>(p.conv_cache), p.conv_weight, p.conv_width, p.state,
+                             static_cast<const float*>(p.out_gate), p.norm_weight, p.eps_l2, p.eps_rms, p.H,
+                             static_cast<float*>(p.o)};
+    return launch_layer_typed<float>(a, p.N, p.d_k, p.d_v, stream);
+  }
+  using B = __nv_bfloat16;
+  const LayerArgs<B> a{static_cast<const B*>(p.q_in), static_cast<const B*>(p.k_in), static_cast<const B*>(p.v_in),
+                       static_cast<const B*>(p.z), p.A_log, p.beta_logit, static_cast<B*>(p.conv_cache),
+                       p.conv_weight, p.conv_width, p.state, static_cast<const B*>(p.out_gate), p.norm_weight,
+                       p.eps_l2, p.eps_rms, p.H, static_cast<B*>(p.o)};
+  return launch_layer_typed<B>(a, p.N, p.d_k, p.d_v, stream);
 }
 
 }  // namespace kda

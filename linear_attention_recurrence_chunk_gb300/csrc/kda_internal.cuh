@@ -143,4 +143,25 @@ cudaError_t launch_decode_step(const void* q, const void* k, const void* v, cons
                                float* state, int32_t N, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
                                void* o, cudaStream_t stream);
 
+// Fused decode layer step (validated by the API layer).
+struct DecodeLayerProblem {
+  const void* q_in;
+  const void* k_in;
+  const void* v_in;
+  const void* z;
+  const float* A_log;
+  const float* beta_logit;
+  void* conv_cache;
+  const float* conv_weight;
+  int32_t conv_width;
+  float* state;
+  const void* out_gate;
+  const float* norm_weight;
+  float eps_l2, eps_rms;
+  int32_t N, H, d_k, d_v;
+  kda_dtype dt;
+  void* o;
+};
+cudaError_t launch_decode_layer(const DecodeLayerProblem& p, cudaStream_t stream);
+
 }  // namespace kda

@@ -131,6 +131,33 @@ def test_decode_rejects_bad_arguments_on_host():
     assert f(p[0], p[1], p[2], p[3], p[4], p[5], 4, 96, 128, 128, 3, p[6], None) == 1      # bad dtype
 
 
+def _layer(lib, **kw):
+    p = [FAKE + (i << 30) for i in range(14)]
+    a = dict(q=p[0], k=p[1], v=p[2], z=p[3], A=p[4], bl=p[5], cache=p[6], w=p[7], W=4, state=p[8], gate=p[9],
+             nw=p[10], e1=1e-6, e2=1e-6, N=4, H=8, dk=128, dv=128, dt=1, o=p[11])
+    a.update(kw)
+    return lib.kda_decode_layer_step(a["q"], a["k"], a["v"], a["z"], a["A"], a["bl"], a["cache"], a["w"], a["W"],
+                                     a["state"], a["gate"], a["nw"], a["e1"], a["e2"], a["N"], a["H"], a["dk"],
+                                     a["dv"], a["dt"], a["o"], None)
+
+
+def test_decode_layer_step_rejects_bad_arguments_on_host():
+    lib = kda.load_library()
+    assert _layer(lib, N=0) == 0                                   # no-op, no CUDA call
+    assert _layer(lib, q=None) == 1
+    assert _layer(lib, W=0) == 1 and _layer(lib, W=9) == 1          # conv width 1..8
+    assert _layer(lib, cache=None) == 1                             # width 4 needs the cache
+    assert _layer(lib, dk=96) == 2
+    assert _layer(lib, dt=7) == 1
+    assert _layer(lib, e1=-1.0) == 1 and _layer(lib, e2=float("nan")) == 1
+    assert _layer(lib, state=FAKE + (8 << 30) + 4) == 1             # state: 16-byte alignment
+    assert _layer(lib, q=FAKE + 1) == 1                             # bf16 element alignment
+    assert _layer(lib, A=FAKE + (4 << 30) + 2) == 1                 # fp32 alignment
+    assert _layer(lib, o=FAKE + (2 << 30) + 64) == 1                # o overlaps v_in
+    assert _layer(lib, cache=FAKE + (8 << 30) + 256) == 1           # the cache overlaps the state
+    assert _layer(lib, H=0) == 1
+
+
 def test_wait_timeout_check_rejects_bad_limits_on_host():
     lib = kda.load_library()
     assert lib.kda_check_wait_timeout(0, None) == 1
