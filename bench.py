@@ -441,8 +441,44 @@ def bench_decode(args, peak_gbs):
     kms = [m for n, m in recs if n == "decode_step"]
     kmean = statistics.mean(kms) if kms else ms / steps
     gbs = per_step_bytes / (kmean / 1e3) / 1e9
-    return {"workload": d.name, "steps": steps, "ms_per_step": ms / steps, "kernel_ms": kmean,
-            "bytes_per_step": per_step_bytes, "GB/s": gbs, "frac": gbs / peak_gbs, "gpu_launches": seen}
+    res = {"workload": d.name, "steps": steps, "ms_per_step": ms / steps, "kernel_ms": kmean,
+           "bytes_per_step": per_step_bytes, "GB/s": gbs, "frac": gbs / peak_gbs, "gpu_launches": seen}
+
+    # The fused layer step on the same shapes: conv width 4, gated RMSNorm output.
+    # Per head-step it moves the state (R+W), q/k/v/z/gate in, o out, beta logit
+    # and the conv cache (R+W); the conv and norm weights are shared by all sequences.
+    W, C = 4, 2 * d.d_k + d.d_v
+    cache = torch.zeros((d.N, d.H, W - 1, C), dtype=torch.bfloat16, device="cuda")
+    conv_w = torch.full((d.H, C, W), 0.25, dtype=torch.float32, device="cuda")
+    A_log = torch.zeros(d.H, dtype=torch.float32, device="cuda")
+    nw = torch.ones((d.H, d.d_v), dtype=torch.float32, device="cuda")
+
+    def layer(x, st):
+        kda.kda_decode_layer_step(x["q"], x["k"], x["v"], x["g"], A_log, x["beta"], cache, conv_w, st,
+                                  out_gate=x["v"], norm_weight=nw, o=o, stream=stream)
+
+    scratch = state.clone()
+    for s in range(3):
+        layer(toks[s], scratch)
+    del scratch
+    torch.cuda.synchronize()
+    _prof(lib, True)
+    e0.record(stream)
+    for s in range(steps):
+        layer(toks[s], state)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _prof(lib, False)
+    seen2, recs2 = _collect(lib)
+    ms2 = e0.elapsed_time(e1)
+    layer_bytes = heads * (2 * d.d_k * d.d_v * 4 + (3 * d.d_k + 2 * d.d_v) * 2 + 4 + d.d_v * 2 + 2 * (W - 1) * C * 2) \
+        + d.H * (C * W + d.d_v + 1) * 4
+    kms2 = [m for n, m in recs2 if n == "decode_layer"]
+    kmean2 = statistics.mean(kms2) if kms2 else ms2 / steps
+    gbs2 = layer_bytes / (kmean2 / 1e3) / 1e9
+    res["layer_step"] = {"conv_width": W, "out_gate": True, "ms_per_step": ms2 / steps, "kernel_ms": kmean2,
+                         "bytes_per_step": layer_bytes, "GB/s": gbs2, "frac": gbs2 / peak_gbs, "gpu_launches": seen2}
+    return res
 
 
 def oracle_sample(w, ntok):

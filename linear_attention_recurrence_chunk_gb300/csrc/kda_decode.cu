@@ -131,6 +131,28 @@ struct LayerArgs {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
+// Loads issued where they stand (the compiler may not sink them past the work
+// that follows), for the per-token values of the layer step.
+__device__ __forceinline__ float ld_f32_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_early(const float* p) { return ld_f32_early(p); }
+__device__ __forceinline__ float ld_early(const __nv_bfloat16* p) {
+  unsigned short b;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(b) : "l"(p));
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// Streaming (evict-first) 16-byte load issued where it stands: the compiler may
+// not sink it past the front-end work that follows.
+__device__ __forceinline__ float4 ld_cs_early(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kDecodeThreads) decode_layer_kernel(const LayerArgs<T> a) {
   constexpr int TX = DV / 4;
@@ -153,28 +175,62 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_layer_kernel(const Laye
   float4* st = reinterpret_cast<float4*>(a.state + head * DK * DV);
   float4 S[RPT];
 #pragma unroll
-  for (int i = 0; i < RPT; ++i) S[i] = __ldcs(st + (ty + i * TY) * TX + tx);
+  for (int i = 0; i < RPT; ++i) S[i] = ld_cs_early(st + (ty + i * TY) * TX + tx);
 
-  // Input branches: conv over the cached inputs and the new one, cache shifted, Swish.
-  for (int c = tid; c < CH; c += kDecodeThreads) {
-    const T xr = c < DK ? a.q_in[head * DK + c] : (c < 2 * DK ? a.k_in[head * DK + c - DK] : a.v_in[head * DV + c - 2 * DK]);
-    const float* wc = a.conv_weight + ((int64_t)h * CH + c) * a.W;
-    T* cc = a.conv_cache + head * (int64_t)(a.W - 1) * CH + c;
-    float y = wc[a.W - 1] * to_f32(xr);
-    for (int j = 0; j < a.W - 1; ++j) {
-      const T xj = cc[(int64_t)j * CH];
-      y += wc[j] * to_f32(xj);
-      if (j > 0) cc[(int64_t)(j - 1) * CH] = xj;
-    }
-    if (a.W > 1) cc[(int64_t)(a.W - 2) * CH] = xr;
-    const float act = y * sigmoidf_(y);
-    if (c < DK) s_q[c] = act;
-    else if (c < 2 * DK) s_k[c - DK] = act;
-    else s_v[c - 2 * DK] = act;
+  // Every per-token value besides the state, issued up front: the gate input,
+  // beta's logit, the output gate and its norm weight.
+  const float zraw = tid < DK ? ld_early(a.z + head * DK + tid) : 0.f;
+  const float blog = ld_f32_early(a.beta_logit + head);
+  const float alog = ld_f32_early(a.A_log + h);
+  float graw = 0.f, nwv = 1.f;
+  if (tid < DV && a.out_gate) {
+    graw = ld_early(a.out_gate + head * DV + tid);
+    if (a.norm_weight) nwv = ld_f32_early(a.norm_weight + h * DV + tid);
   }
-  const float gscale = expf(a.A_log[h]);
-  for (int i = tid; i < DK; i += kDecodeThreads)
-    s_alpha[i] = expf(-5.f * sigmoidf_(gscale * to_f32(a.z[head * DK + i])));
+
+  // Input branches: conv over the cached inputs and the new one, cache shifted,
+  // Swish.  Every load of the thread's channels (the input, up to kMaxConv - 1
+  // cached inputs and kMaxConv taps each) is issued before any store.
+  constexpr int kMaxConv = 8;
+  constexpr int kChIter = (CH + kDecodeThreads - 1) / kDecodeThreads;
+  const int W = a.W;
+  T xr[kChIter], xv[kChIter][kMaxConv - 1];
+  float wcur[kChIter], wp[kChIter][kMaxConv - 1];   // the current token's tap, the earlier taps
+#pragma unroll
+  for (int it = 0; it < kChIter; ++it) {
+    const int c = tid + it * kDecodeThreads;
+    const bool ok = c < CH;
+    const int cs = ok ? c : 0;
+    xr[it] = cs < DK ? a.q_in[head * DK + cs] : (cs < 2 * DK ? a.k_in[head * DK + cs - DK] : a.v_in[head * DV + cs - 2 * DK]);
+    const float* wc = a.conv_weight + ((int64_t)h * CH + cs) * W;
+    const T* cc = a.conv_cache + head * (int64_t)(W - 1) * CH + cs;
+    wcur[it] = wc[W - 1];
+#pragma unroll
+    for (int j = 0; j < kMaxConv - 1; ++j) {
+      const bool tap = ok && j < W - 1;
+      wp[it][j] = tap ? wc[j] : 0.f;
+      xv[it][j] = tap ? cc[(int64_t)j * CH] : T(0.f);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kChIter; ++it) {
+    const int c = tid + it * kDecodeThreads;
+    if (c < CH) {
+      float y = wcur[it] * to_f32(xr[it]);
+#pragma unroll
+      for (int j = 0; j < kMaxConv - 1; ++j) y += wp[it][j] * to_f32(xv[it][j]);   // zero beyond tap W - 2
+      T* cc = a.conv_cache + head * (int64_t)(W - 1) * CH + c;
+#pragma unroll
+      for (int j = 1; j < kMaxConv - 1; ++j)
+        if (j < W - 1) cc[(int64_t)(j - 1) * CH] = xv[it][j];
+      if (W > 1) cc[(int64_t)(W - 2) * CH] = xr[it];
+      const float act = y * sigmoidf_(y);
+      if (c < DK) s_q[c] = act;
+      else if (c < 2 * DK) s_k[c - DK] = act;
+      else s_v[c - 2 * DK] = act;
+    }
+  }
+  if (tid < DK) s_alpha[tid] = expf(-5.f * sigmoidf_(expf(alog) * zraw));
   __syncthreads();
 
   if (warp < 2) {   // L2Norm scales of q (warp 0) and k (warp 1)
@@ -221,7 +277,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_layer_kernel(const Laye
       vhat += s_red[0][y][tid];
       acc += s_red[1][y][tid];
     }
-    const float d = sigmoidf_(a.beta_logit[head]) * (s_v[tid] - vhat);
+    const float d = sigmoidf_(blog) * (s_v[tid] - vhat);
     s_delta[tid] = d;
     ov = acc + s_kq * d;
   }
@@ -237,8 +293,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_layer_kernel(const Laye
       float tot = 0.f;
 #pragma unroll
       for (int w = 0; w < DV / 32; ++w) tot += s_ss[w];
-      const float wn = a.norm_weight ? a.norm_weight[h * DV + tid] : 1.f;
-      ov = ov * rsqrtf(tot / DV + a.eps_rms) * wn * sigmoidf_(to_f32(a.out_gate[head * DV + tid]));
+      ov = ov * rsqrtf(tot / DV + a.eps_rms) * nwv * sigmoidf_(graw);
     }
   }
   if (tid < DV) a.o[head * DV + tid] = from_f32<T>(ov);
