@@ -137,6 +137,27 @@ KDA_API kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const v
                                            cudaStream_t stream);
 
 /*
+ * Chunked prefill with the output epilogue of page "Kimi K3：架构、训练与百万 Token
+ * Agentic RL 技术解读" §3.2 applied before o is written (the input of the output
+ * projection W_o):  o = Sigmoid(out_gate) * o~ / sqrt(mean(o~^2) + eps_rms) * w,
+ * per token and head over d_v, where o~ is kda_chunk_fwd's output.  Arguments,
+ * layouts, results and errors are those of kda_chunk_fwd, plus:
+ *  out_gate     [B, T, H, d_v] dtype dt (W_g x), 16-byte aligned, required;
+ *  norm_weight  [H, d_v] fp32, 16-byte aligned, or NULL for ones;
+ *  eps_rms      >= 0.
+ * Supported on the bf16 path with d_k = 128 (d_v = 64 or 128); other head sizes
+ * or fp32 inputs return KDA_ERR_UNSUPPORTED.  The inter-chunk pass then holds
+ * all d_v columns of a head in one CTA (the RMS needs the whole row).
+ */
+KDA_API kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
+                                       const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                                       int32_t num_seqs, int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v,
+                                       kda_dtype dt, void* o, float* final_state, const void* out_gate,
+                                       const float* norm_weight, float eps_rms, void* workspace,
+                                       size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One decode step for N independent sequences (one new token each), the/*
  * One decode step for N independent sequences (one new token each), the
  * single-token interface of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读"
  * §3.2 restricted to the recurrence: (q, k, v, g, beta, S_{t-1}) -> (o_t, S_t).

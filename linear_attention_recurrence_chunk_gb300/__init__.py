@@ -15,6 +15,9 @@ Functions keep the C names:
 * ``kda_chunk_fwd_snapshots(q, k, v, g, beta, snapshot_interval, ...)`` ->
   ``(o, final_state, snapshots)``: the same, also keeping the state every
   ``snapshot_interval`` tokens of each sequence (same page §9, prefix cache).
+* ``kda_chunk_fwd_gated(q, k, v, g, beta, out_gate, norm_weight=None, ...)`` ->
+  ``(o, final_state)``: the same with the output epilogue (Sigmoid gate times
+  the per-head RMSNorm of o) applied before o is written (same page §3.2).
 * ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
   sequence (same page §3.2), state updated in place.
 * ``kda_decode_layer_step(q_in, k_in, v_in, z, A_log, beta_logit, conv_cache,
@@ -34,7 +37,7 @@ import torch
 
 from . import _build
 
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_decode_step", "kda_decode_layer_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_chunk_fwd_gated", "kda_decode_step", "kda_decode_layer_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
            "kda_check_wait_timeout", "KdaError", "library_path", "load_library", "STATUS"]
 
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
@@ -76,6 +79,9 @@ def load_library():
     lib.kda_chunk_fwd_snapshots.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int,
                                             vp, vp, vp, i32, i64, vp, sz, vp]
     lib.kda_chunk_fwd_snapshots.restype = ctypes.c_int
+    lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int,
+                                        vp, vp, vp, vp, ctypes.c_float, vp, sz, vp]
+    lib.kda_chunk_fwd_gated.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
     f32 = ctypes.c_float
@@ -183,6 +189,36 @@ def kda_chunk_fwd_snapshots(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g
                                      workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "kda_chunk_fwd_snapshots")
     return o, final_state, snapshots[:cap]
+
+
+def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                        out_gate: torch.Tensor, norm_weight: Optional[torch.Tensor] = None, eps_rms: float = 1e-6,
+                        initial_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                        output_final_state: bool = True, o: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill with ``o = Sigmoid(out_gate) * RMSNorm(o~) * norm_weight``
+    (per token and head over d_v) applied before o is written.  ``out_gate`` is
+    ``[B, T, H, d_v]`` in the input dtype, ``norm_weight`` ``[H, d_v]`` fp32."""
+    lib = load_library()
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    num_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((num_seqs, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    ws_bytes = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                 _ptr(cu_seqlens), num_seqs, B, T, H, d_k, d_v, _dtype_code(q), _ptr(o),
+                                 _ptr(final_state), _ptr(out_gate), _ptr(norm_weight), float(eps_rms),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "kda_chunk_fwd_gated")
+    return o, final_state
 
 
 def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,

@@ -111,7 +111,8 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
                           const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
                           int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
                           float* final_state, float* snapshots, int32_t snapshot_interval,
-                          int64_t snapshot_capacity, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                          int64_t snapshot_capacity, const void* out_gate, const float* norm_weight, float eps_rms,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   const bool varlen = cu_seqlens != nullptr;
   kda_status st = check_chunk_shape(B, T, H, d_k, d_v, num_seqs, dt, varlen);
   if (st != KDA_OK) return st;
@@ -162,6 +163,21 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
       if (overlaps(snapshots, nsnap, r.p, r.n)) return KDA_ERR_INVALID_ARG;
   }
 
+  // Output epilogue: on the bf16 tensor-core path (d_k = 128) only.
+  if (out_gate || norm_weight) {
+    if (!out_gate) return KDA_ERR_INVALID_ARG;
+    if (!kda::tc_path_supported(d_k, d_v, dt)) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(out_gate) || (norm_weight && !aligned16(norm_weight))) return KDA_ERR_INVALID_ARG;
+    if (!(eps_rms >= 0.f && eps_rms < 1e30f)) return KDA_ERR_INVALID_ARG;
+    const Range gr[] = {{out_gate, nv}, {norm_weight, norm_weight ? (size_t)H * d_v * sizeof(float) : 0}};
+    for (const Range& r : gr) {
+      if (overlaps(o, nv, r.p, r.n) || overlaps(final_state, ns, r.p, r.n) || overlaps(workspace, ws.bytes, r.p, r.n))
+        return KDA_ERR_INVALID_ARG;
+      if (snapshots && overlaps(snapshots, (size_t)snapshot_capacity * H * d_k * d_v * sizeof(float), r.p, r.n))
+        return KDA_ERR_INVALID_ARG;
+    }
+  }
+
   if (num_seqs == 0) return KDA_OK;
 
   int32_t* dev_err = nullptr;
@@ -173,6 +189,9 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
   p.H = H; p.d_k = d_k; p.d_v = d_v; p.dt = dt; p.o = o; p.s_final = final_state; p.dev_err = dev_err;
   p.snaps = snapshots;
   p.snap_every = snapshots ? snapshot_interval / kda::kChunk : 0;
+  p.out_gate = out_gate;
+  p.norm_weight = norm_weight;
+  p.eps_rms = eps_rms;
   return kda::launch_chunk_fwd(p, ws, workspace, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -185,7 +204,18 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void
                          int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o, float* final_state,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
-                        final_state, nullptr, 0, 0, workspace, workspace_bytes, stream);
+                        final_state, nullptr, 0, 0, nullptr, nullptr, 0.f, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs, int64_t B,
+                               int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                               float* final_state, const void* out_gate, const float* norm_weight, float eps_rms,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!out_gate) return KDA_ERR_INVALID_ARG;
+  return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
+                        final_state, nullptr, 0, 0, out_gate, norm_weight, eps_rms, workspace, workspace_bytes,
+                        stream);
 }
 
 kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const void* v, const void* g, const float* beta,
@@ -196,8 +226,8 @@ kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const void* v, 
                                    cudaStream_t stream) {
   if (snapshot_interval <= 0) return KDA_ERR_INVALID_ARG;
   return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
-                        final_state, snapshots, snapshot_interval, snapshot_capacity, workspace, workspace_bytes,
-                        stream);
+                        final_state, snapshots, snapshot_interval, snapshot_capacity, nullptr, nullptr, 0.f,
+                        workspace, workspace_bytes, stream);
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const void* g, const float* beta,

@@ -1125,9 +1125,10 @@ struct ChainWideSmem {
   static constexpr uint32_t kSAtom = DK * 64, kVAtom = C * 64;   // MN atom strides
   static constexpr uint32_t oS = 2 * kStage;                      // state block, DV/32 atoms
   static constexpr uint32_t oVN = oS + (DV / 32) * kSAtom;        // V_new, DV/32 atoms
-  static constexpr uint32_t oBar = oVN + (DV / 32) * kVAtom;      // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready
-  static constexpr uint32_t oTmem = oBar + 9 * 8;
-  static constexpr uint32_t kBytes = oTmem + 16;
+  static constexpr uint32_t oBar = oVN + (DV / 32) * kVAtom;      // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, rs[2]
+  static constexpr uint32_t oTmem = oBar + 11 * 8;
+  static constexpr uint32_t oRss = oTmem + 16;                    // output epilogue: fp32 [2][DV/32][64] row sums of squares
+  static constexpr uint32_t kBytes = oRss + 2 * (DV / 32) * 64 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
 };
@@ -1147,7 +1148,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
                         const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu,
                         int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0,
-                        float* __restrict__ s_final, bf16* __restrict__ o, int32_t* dev_err) {
+                        float* __restrict__ s_final, bf16* __restrict__ o, OutEpilogue ep, int32_t* dev_err) {
   using L = ChainWideSmem<NC>;
   constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, NC) | (1u << 16);
   constexpr uint32_t kD3 = 2 * NC;
@@ -1161,7 +1162,9 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   uint64_t* drain = full + 6;
   uint64_t* vn_ready = full + 7;
   uint64_t* s_ready = full + 8;
+  uint64_t* rs_full = full + 9;   // [2] output epilogue: row sums of squares of a chunk published
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
+  float* rss = reinterpret_cast<float*>(sm + L::oRss);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
@@ -1178,6 +1181,8 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
     tc::mbar_init(vn_ready, L::kConsumerWarps / 2);   // one arrival per V_new warp
     tc::mbar_init(s_ready, L::kConsumerWarps);        // one arrival per consumer warp
+    tc::mbar_init(rs_full, L::kConsumerWarps / 2);    // one arrival per o warp
+    tc::mbar_init(rs_full + 1, L::kConsumerWarps / 2);
     tc::fence_mbar_init();
   }
   for (int i = tid; i < 2 * 512; i += L::kThreads) {   // rows 0-63 of both [0; P] tiles stay zero
@@ -1265,6 +1270,59 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     const int q = warp & 3, cg = warp >> 2;   // TMEM lane quarter, 32-column group
     const int c = 32 * q + lane;
     const uint32_t tl = (uint32_t)(32 * q);
+    // o rows (tokens t0 + r, r = c - 64 < len) of local chunk j from D12 buffer
+    // `buf`, with the optional output epilogue: each o warp publishes its 32
+    // columns' sum of squares per row, the row's total over the NC/32 column
+    // groups gives the RMS, then the weight and the Sigmoid gate scale the row.
+    auto emit_o = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
+      const int r = c - 64;
+      float sc = 1.f;
+      if (ep.gate) {   // first pass over TMEM: this warp's share of the row's sum of squares
+        float ss = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float ov[16];
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, buf * NC + 32 * cg + 16 * hf), ov);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ss += ov[e] * ov[e];
+        }
+        float* rp = rss + (j & 1) * (NC / 32) * 64;
+        rp[cg * 64 + r] = ss;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(rs_full + (j & 1));
+        if (!tc::mbar_wait(rs_full + (j & 1), (uint32_t)(j >> 1) & 1u, kWaitLimit)) return false;
+        float tot = 0.f;
+#pragma unroll
+        for (int g2 = 0; g2 < NC / 32; ++g2) tot += rp[g2 * 64 + r];
+        sc = rsqrtf(tot * (1.f / DV) + ep.eps);
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float ov[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, buf * NC + 32 * cg + 16 * hf), ov);
+        if (r < len) {
+          const int col0 = n0 + 32 * cg + 16 * hf;
+          if (ep.gate) {
+            const uint4* gp = reinterpret_cast<const uint4*>(ep.gate + ((t0 + r) * H + h) * DV + col0);
+#pragma unroll
+            for (int v8 = 0; v8 < 2; ++v8) {
+              const uint4 raw = gp[v8];
+              const bf16* gv = reinterpret_cast<const bf16*>(&raw);
+              float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
+              if (ep.weight) {
+                w0 = *reinterpret_cast<const float4*>(ep.weight + (int64_t)h * DV + col0 + 8 * v8);
+                w1 = *reinterpret_cast<const float4*>(ep.weight + (int64_t)h * DV + col0 + 8 * v8 + 4);
+              }
+              const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ov[8 * v8 + e] *= sc * wv[e] / (1.f + __expf(-__bfloat162float(gv[e])));
+            }
+          }
+          store_bf16x16(o + ((t0 + r) * H + h) * DV + col0, ov);
+        }
+      }
+      return true;
+    };
     float S[32];
     {
       const int64_t off = (((int64_t)s * H + h) * DK + c) * DV + n0 + 32 * cg;
@@ -1293,12 +1351,10 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
       if (i > 0 && q >= 2) {   // previous chunk's o rows from the other buffer
-        const int r = c - 64;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float ov[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)(st ^ 1) * NC + 32 * cg + 16 * hf), ov);
-          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 32 * cg + 16 * hf, ov);
+        bad |= !emit_o((uint32_t)(st ^ 1), prev_t0, prev_len, i - 1);
+        if (__any_sync(0xffffffffu, bad)) {
+          bad = true;
+          break;
         }
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
@@ -1356,15 +1412,8 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
-    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
-      const int r = c - 64;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float ov[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)((nch - 1) & 1) * NC + 32 * cg + 16 * hf), ov);
-        if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 32 * cg + 16 * hf, ov);
-      }
-    }
+    if (i == nch && !bad && nch > 0 && q >= 2)   // the last chunk's o
+      bad = __any_sync(0xffffffffu, !emit_o((uint32_t)((nch - 1) & 1), prev_t0, prev_len, nch - 1));
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
     } else if (s_final) {
@@ -1430,7 +1479,7 @@ cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, 
   prof_begin(stream, "chunk_chain_wide_tc");
   chunk_chain_wide_tc<DV, NC><<<(unsigned)p.num_seqs * p.H * (DV / NC), W::kThreads, W::kAlloc, stream>>>(
       mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-      p.dev_err);
+      OutEpilogue{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms}, p.dev_err);
   prof_end(stream);
   return cudaGetLastError();
 }
@@ -1491,6 +1540,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int cols = std::atoi(env);
     if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
+  if (p.out_gate) ncol = DV;   // the output epilogue needs a token's d_v outputs in one CTA
   const bool wide = ncol != BV;
   CUtensorMap mWQ, mP, mKT, mU, mGam;
   const uint64_t Rr = R > 0 ? R : 1;

@@ -101,7 +101,19 @@ struct ChunkProblem {
   float* s_final;
   float* snaps;          // state snapshots or nullptr
   int32_t snap_every;    // chunks between snapshots (0 = none)
+  const void* out_gate;       // output epilogue: gate logits [tokens][H][d_v] or nullptr (none)
+  const float* norm_weight;   // its RMSNorm weight [H][d_v] or nullptr (ones)
+  float eps_rms;
   int32_t* dev_err;
+};
+
+// Output epilogue of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.2,
+// applied before o is written: o = Sigmoid(gate) * o~ / sqrt(mean(o~^2) + eps) * w,
+// per token and head over d_v.
+struct OutEpilogue {
+  const __nv_bfloat16* gate;   // [tokens][H][d_v] or nullptr (no epilogue)
+  const float* weight;         // [H][d_v] or nullptr (ones)
+  float eps;
 };
 
 // Workspace layout (all offsets 256-byte aligned).  `tc` selects the bf16

@@ -118,6 +118,30 @@ def test_chunk_fwd_snapshots_rejects_bad_arguments_on_host():
     assert _snap(lib, B=0, num_seqs=0, cap=0) == 0              # nothing to do, no CUDA call
 
 
+def _gated(lib, **kw):
+    args = dict(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), g=FAKE + (3 << 30), beta=FAKE + (4 << 30),
+                s0=None, cu=None, num_seqs=1, B=1, T=64, H=2, dk=128, dv=128, dt=1, o=FAKE + (5 << 30),
+                sf=None, gate=FAKE + (8 << 30), nw=FAKE + (9 << 30), eps=1e-6, ws=FAKE + (6 << 30), wsb=1 << 40)
+    args.update(kw)
+    return lib.kda_chunk_fwd_gated(args["q"], args["k"], args["v"], args["g"], args["beta"], args["s0"], args["cu"],
+                                   args["num_seqs"], args["B"], args["T"], args["H"], args["dk"], args["dv"],
+                                   args["dt"], args["o"], args["sf"], args["gate"], args["nw"], args["eps"],
+                                   args["ws"], args["wsb"], None)
+
+
+def test_chunk_fwd_gated_rejects_bad_arguments_on_host():
+    lib = kda.load_library()
+    assert _gated(lib, gate=None) == 1                          # the gate is the point of the call
+    assert _gated(lib, dt=0) == 2                               # fp32: not on the tensor-core path
+    assert _gated(lib, dk=64) == 2
+    assert _gated(lib, gate=FAKE + (8 << 30) + 2) == 1          # 16-byte alignment
+    assert _gated(lib, nw=FAKE + (9 << 30) + 4) == 1
+    assert _gated(lib, eps=-1.0) == 1
+    assert _gated(lib, gate=FAKE + (5 << 30) + 64) == 1         # o overlaps the gate
+    assert _gated(lib, q=None) == 1                             # the kda_chunk_fwd checks still apply
+    assert _gated(lib, B=0, num_seqs=0) == 0                    # nothing to do, no CUDA call
+
+
 def test_decode_rejects_bad_arguments_on_host():
     lib = kda.load_library()
     f = lib.kda_decode_step
