@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-snapshots", action="store_true")
+    ap.add_argument("--no-gated", action="store_true")
     ap.add_argument("--snapshot-interval", type=int, default=512)
     ap.add_argument("--decode-steps", type=int, default=100)
     ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD, "prefill_b8_h96_t8192_d128",
@@ -358,6 +359,44 @@ def bench_snapshots(args, r, steps):
             "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "slowdown_vs_plain": ms / plain_ms}
 
 
+def bench_gated(args, r, steps):
+    """The same prefill with the output epilogue (Sigmoid gate times the per-head
+    RMSNorm of o) fused before o is written; synthetic gate logits and norm
+    weights of the workload's shape."""
+    import torch
+
+    import linear_attention_recurrence_chunk_gb300 as kda
+
+    w, t = r["w"], r["t"]
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    gate = torch.randn(t["v"].shape, generator=gen, device="cuda").to(torch.bfloat16)
+    nw = 1 + 0.1 * torch.randn((w.H, w.d_v), generator=gen, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kda.kda_chunk_fwd_gated(t["q"], t["k"], t["v"], t["g"], t["beta"], gate, norm_weight=nw,
+                                initial_state=t["s0"], cu_seqlens=t["cu"], o=r["o"], final_state=r["sf"],
+                                workspace=r["wsp"], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st, code = kda.kda_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {code} in the gated leg")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del gate, nw
+    return {"value": w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
+            "note": "the inter-chunk pass holds all d_v columns of a head per CTA"}
+
+
 def bench_e2e(args, w, wsp, steps):
     """Same metric through the Python API from pinned host buffers."""
     import torch
@@ -593,6 +632,8 @@ def main():
     }
     if not args.no_snapshots:
         line["snapshots"] = bench_snapshots(args, r, max(3, steps // 10))
+    if not args.no_gated:
+        line["gated"] = bench_gated(args, r, max(3, steps // 10))
     if not args.no_e2e:
         line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
         if ws_size > 1:
