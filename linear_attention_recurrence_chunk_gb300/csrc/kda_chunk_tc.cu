@@ -1142,7 +1142,7 @@ __device__ __forceinline__ void store_mn_atom_row(uint8_t* atom, int k, const fl
                    pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
 }
 
-template <int DV, int NC>
+template <int DV, int NC, bool kGated>
 __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     chunk_chain_wide_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
@@ -1273,11 +1273,13 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     // o rows (tokens t0 + r, r = c - 64 < len) of local chunk j from D12 buffer
     // `buf`, with the optional output epilogue: each o warp publishes its 32
     // columns' sum of squares per row, the row's total over the NC/32 column
-    // groups gives the RMS, then the weight and the Sigmoid gate scale the row.
+    // groups gives the RMS, then the weight and the Sigmoid gate scale the row
+    // (loaded where used: at this kernel's register limit, holding them longer
+    // spilled and measured slower).
     auto emit_o = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
       const int r = c - 64;
       float sc = 1.f;
-      if (ep.gate) {   // first pass over TMEM: this warp's share of the row's sum of squares
+      if constexpr (kGated) {   // first pass over TMEM: this warp's share of the row's sum of squares
         float ss = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -1302,7 +1304,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         tc::tmem_ld16(tc::tmem_addr(tmem, tl, buf * NC + 32 * cg + 16 * hf), ov);
         if (r < len) {
           const int col0 = n0 + 32 * cg + 16 * hf;
-          if (ep.gate) {
+          if constexpr (kGated) {
             const uint4* gp = reinterpret_cast<const uint4*>(ep.gate + ((t0 + r) * H + h) * DV + col0);
 #pragma unroll
             for (int v8 = 0; v8 < 2; ++v8) {
@@ -1412,8 +1414,9 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
-    if (i == nch && !bad && nch > 0 && q >= 2)   // the last chunk's o
+    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
       bad = __any_sync(0xffffffffu, !emit_o((uint32_t)((nch - 1) & 1), prev_t0, prev_len, nch - 1));
+    }
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
     } else if (s_final) {
@@ -1468,16 +1471,16 @@ bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DV, int NC>
+template <int DV, int NC, bool kGated>
 cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
                                  const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
                                  const ChunkMap& map, cudaStream_t stream) {
   using W = ChainWideSmem<NC>;
   cudaError_t e =
-      cudaFuncSetAttribute(chunk_chain_wide_tc<DV, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
+      cudaFuncSetAttribute(chunk_chain_wide_tc<DV, NC, kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_wide_tc");
-  chunk_chain_wide_tc<DV, NC><<<(unsigned)p.num_seqs * p.H * (DV / NC), W::kThreads, W::kAlloc, stream>>>(
+  chunk_chain_wide_tc<DV, NC, kGated><<<(unsigned)p.num_seqs * p.H * (DV / NC), W::kThreads, W::kAlloc, stream>>>(
       mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
       OutEpilogue{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms}, p.dev_err);
   prof_end(stream);
@@ -1488,8 +1491,10 @@ template <int DV>
 cudaError_t launch_chain_wide(int ncol, const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
                               const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
                               const ChunkMap& map, cudaStream_t stream) {
-  if (DV == 128 && ncol == 128) return launch_chain_wide_nc<DV, (DV == 128 ? 128 : 64)>(mWQ, mP, mKT, mU, mGam, p, map, stream);
-  return launch_chain_wide_nc<DV, 64>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+  constexpr int kFull = DV == 128 ? 128 : 64;
+  if (p.out_gate) return launch_chain_wide_nc<DV, kFull, true>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+  if (DV == 128 && ncol == 128) return launch_chain_wide_nc<DV, kFull, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+  return launch_chain_wide_nc<DV, 64, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
 }
 
 template <int DV>
