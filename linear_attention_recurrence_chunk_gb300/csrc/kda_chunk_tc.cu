@@ -772,8 +772,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       }
     }
 
-    // 7. [w | u] = X [beta k e^G | beta V] on the tensor cores (M = 64, N = d_k + d_v,
-    //    K = 64; fp32 accumulator in TMEM), read out at the start of the next task.
+    // 7. [w | u] = X [beta k e^G | beta V] on the tensor cores (M = 128 with X's rows
+    //    64-127 zero, N = d_k + d_v, K = 64; fp32 accumulator in TMEM lanes 0-63), read out
+    //    at the start of the next task.  (As an M = 64 product, whose rows reach every lane
+    //    quarter, all 16 warps could drain it, but that measured slower.)
     tc::fence_proxy_async_smem();   // X and the operand written by the threads, seen by the MMAs
     tc::tc_fence_before();
     __syncthreads();
