@@ -158,9 +158,9 @@ _TC_SECTIONS = {"chunk_prep_tc": [("// -----------------------------------------
                                    "// --------------------------------------------------------------- host side")]}
 
 
-def _kernel_src_sha(kernel: str = "") -> str:
+def _kernel_src_sha(kernel: str = "", csrc: str = "") -> str:
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "linear_attention_recurrence_chunk_gb300", "csrc")
+    d = csrc or os.path.join(ROOT, "linear_attention_recurrence_chunk_gb300", "csrc")
     if kernel in _TC_SECTIONS:
         for fn in ("kda_internal.cuh", "tc_ptx.cuh"):
             h.update(open(os.path.join(d, fn), "rb").read())
@@ -176,13 +176,13 @@ def _kernel_src_sha(kernel: str = "") -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profiles(kernel: str, units_per_launch: float):
+def _traffic_from_profiles(kernel: str, units_per_launch: float, pdir: str = "", csrc: str = ""):
     """DRAM bytes per launch of ``kernel`` from the committed ncu summaries, if
     they were taken on the current kernel sources (else None)."""
-    pdir = os.path.join(ROOT, "profiles")
+    pdir = pdir or os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    sha = _kernel_src_sha(kernel)
+    sha = _kernel_src_sha(kernel, csrc)
     pat = re.compile(r"^traffic:\s+kernel=(\S+)\s+dram_bytes_per_unit=([0-9.eE+-]+)\s+src_sha=(\S+)")
     for fn in sorted(os.listdir(pdir)):
         if not fn.endswith((".md", ".txt")):

@@ -19,8 +19,10 @@
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller, dense and
  *    contiguous in the layouts given below, 16-byte aligned (beta and
- *    cu_seqlens: 4-byte aligned).  The library
- *    allocates no memory; kda_chunk_fwd takes its scratch space from the caller.
+ *    cu_seqlens: 4-byte aligned) unless an entry point states otherwise
+ *    (kda_decode_layer_step needs 16 bytes for the state only).  The library
+ *    allocates no memory; kda_chunk_fwd and its variants take their scratch
+ *    space from the caller.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
  *    errors are detected on the host and returned before anything is launched.
  *    A launch failure returns KDA_ERR_CUDA.  Conditions only the device can see
@@ -31,6 +33,8 @@
  *    the raw decay logit (any per-head scale is already folded into it); beta is
  *    the write strength, already in (0, 1), as fp32.  No 1/sqrt(d_k) factor is
  *    applied to q.  o has the input dtype; states are always fp32.
+ *    (kda_decode_layer_step instead starts from the token's projections and
+ *    applies the conv, activations, norms and gate scale itself.)
  *  - Supported head sizes: d_k, d_v in {64, 128}; other values return
  *    KDA_ERR_UNSUPPORTED.
  */
