@@ -1116,7 +1116,7 @@ struct ChainWideSmem {
   static constexpr int kConsumerWarps = 4 * (DV / 32);
   static constexpr int kThreads = 32 * (kConsumerWarps + 2);
   static constexpr int kTmaWarp = kConsumerWarps, kMmaWarp = kConsumerWarps + 1;
-  static constexpr uint32_t kTmemCols = DV == 128 ? 512 : 256;   // D12 x 2 + D3, DV columns each
+  static constexpr uint32_t kTmemCols = DV == 128 ? 512 : 256;   // D12 x 3 + D3, DV columns each
   static constexpr uint32_t oWQ = 0;           // [w; q e^G] 128 x 128: two 64-column atoms of 16 KB
   static constexpr uint32_t oPZ = 32768;       // [0; P] 128 x 64 (rows 0-63 stay zero)
   static constexpr uint32_t oKT = 49152;       // (k e^{G_last-G})^T 128 x 64
@@ -1153,7 +1153,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
                         float* __restrict__ s_final, bf16* __restrict__ o, OutEpilogue ep, int32_t* dev_err) {
   using L = ChainWideSmem<NC>;
   constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, NC) | (1u << 16);
-  constexpr uint32_t kD3 = 2 * NC;
+  constexpr uint32_t kD3 = 3 * NC;   // D12 buffers 0-2 (chunk i in buffer i % 3), then D3
   if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1242,7 +1242,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
         const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
-        const uint32_t d12 = tmem + (uint32_t)st * NC;
+        const uint32_t d12 = tmem + (uint32_t)(i % 3) * NC;
         tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // group 1
 #pragma unroll
         for (int kk = 1; kk < DK / 16; ++kk)
@@ -1354,11 +1354,13 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         break;
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
-      if (i > 0 && q >= 2) {   // previous chunk's o rows from the other buffer
-        bad |= !emit_o((uint32_t)(st ^ 1), prev_t0, prev_len, i - 1);
-        if (__any_sync(0xffffffffu, bad)) {
-          bad = true;
-          break;
+      if constexpr (kGated) {   // the previous chunk's o rows, before this chunk's products are seen
+        if (i > 0 && q >= 2) {
+          bad |= !emit_o((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
+          if (__any_sync(0xffffffffu, bad)) {
+            bad = true;
+            break;
+          }
         }
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
@@ -1372,7 +1374,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float d[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)st * NC + 32 * cg + 16 * hf), d);
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, (uint32_t)(i % 3) * NC + 32 * cg + 16 * hf), d);
 #pragma unroll
           for (int q4 = 0; q4 < 2; ++q4) {
             const uint4 raw =
@@ -1413,11 +1415,23 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
 #pragma unroll
         for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
       }
+      // Without the epilogue the previous chunk's o rows are emitted after the
+      // state hand-off (off the chain's critical path): their buffer, (i - 1) % 3,
+      // is next written by the first group of chunk i + 2, issued only after this
+      // warp's next hand-off.  (With the epilogue, whose row exchange among the
+      // o warps timed out there for d_v = 128, they are emitted at the step start.)
+      if (!kGated && i > 0 && q >= 2) {
+        bad |= !emit_o((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
+        if (__any_sync(0xffffffffu, bad)) {
+          bad = true;
+          break;
+        }
+      }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
     if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o
-      bad = __any_sync(0xffffffffu, !emit_o((uint32_t)((nch - 1) & 1), prev_t0, prev_len, nch - 1));
+      bad = __any_sync(0xffffffffu, !emit_o((uint32_t)((nch - 1) % 3), prev_t0, prev_len, nch - 1));
     }
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
