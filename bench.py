@@ -394,7 +394,7 @@ def bench_gated(args, r, steps):
     del gate, nw
     return {"value": w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
-            "note": "the inter-chunk pass holds all d_v columns of a head per CTA"}
+            "note": "fused into the chain where its CTAs hold all d_v columns of a head, else a pass of its own over o"}
 
 
 def bench_e2e(args, w, wsp, steps):

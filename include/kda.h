@@ -150,8 +150,9 @@ KDA_API kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const v
  *  norm_weight  [H, d_v] fp32, 16-byte aligned, or NULL for ones;
  *  eps_rms      >= 0.
  * Supported on the bf16 path with d_k = 128 (d_v = 64 or 128); other head sizes
- * or fp32 inputs return KDA_ERR_UNSUPPORTED.  The inter-chunk pass then holds
- * all d_v columns of a head in one CTA (the RMS needs the whole row).
+ * or fp32 inputs return KDA_ERR_UNSUPPORTED.  The RMS needs a token's whole
+ * row: where the inter-chunk pass holds all d_v columns of a head per CTA (many
+ * heads) the epilogue is applied there, else by a pass of its own over o.
  */
 KDA_API kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
                                        const float* beta, const float* initial_state, const int32_t* cu_seqlens,

@@ -50,6 +50,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -1446,6 +1447,58 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
+// ------------------------------------------------- output epilogue, own pass
+// The output epilogue as a pass of its own over o, for chains whose CTAs hold
+// only part of a token's d_v outputs: each warp takes kRows (token, head) rows,
+// issues all their loads (o, gate logits: 8 bytes per lane and row) before using
+// any, then writes each row back as Sigmoid(gate) * row / RMS(row) * weight.
+constexpr int kEpiRows = 4;   // rows per warp
+
+template <int DV>
+__global__ void __launch_bounds__(256) out_epilogue_kernel(bf16* __restrict__ o, const bf16* __restrict__ gate,
+                                                           const float* __restrict__ weight, float eps,
+                                                           int64_t rows, int32_t H) {
+  constexpr int V = DV / 32;   // values per lane: 4 or 2
+  using Vec = typename std::conditional<V == 4, uint2, uint32_t>::type;
+  const int lane = threadIdx.x & 31;
+  const int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * kEpiRows;
+  Vec xo[kEpiRows], xg[kEpiRows];
+#pragma unroll
+  for (int k = 0; k < kEpiRows; ++k) {
+    const int64_t row = row0 + k;
+    if (row < rows) {
+      xo[k] = *reinterpret_cast<const Vec*>(o + row * DV + lane * V);
+      xg[k] = *reinterpret_cast<const Vec*>(gate + row * DV + lane * V);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kEpiRows; ++k) {
+    const int64_t row = row0 + k;
+    if (row >= rows) break;   // rows are contiguous: the rest of this warp's rows are past the end too
+    const int h = (int)(row % H);
+    const bf16* xv = reinterpret_cast<const bf16*>(&xo[k]);
+    const bf16* gv = reinterpret_cast<const bf16*>(&xg[k]);
+    float x[V];
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      x[e] = __bfloat162float(xv[e]);
+      ss += x[e] * x[e];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float sc = rsqrtf(ss * (1.f / DV) + eps);
+    Vec out;
+    bf16* ov = reinterpret_cast<bf16*>(&out);
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      const float w = weight ? weight[(int64_t)h * DV + lane * V + e] : 1.f;
+      ov[e] = __float2bfloat16_rn(x[e] * sc * w / (1.f + __expf(-__bfloat162float(gv[e]))));
+    }
+    *reinterpret_cast<Vec*>(o + row * DV + lane * V) = out;
+  }
+}
+
 // --------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1496,19 +1549,21 @@ cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, 
       cudaFuncSetAttribute(chunk_chain_wide_tc<DV, NC, kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)W::kAlloc);
   if (e != cudaSuccess) return e;
   prof_begin(stream, "chunk_chain_wide_tc");
+  const OutEpilogue ep = kGated ? OutEpilogue{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms}
+                                : OutEpilogue{nullptr, nullptr, 0.f};
   chunk_chain_wide_tc<DV, NC, kGated><<<(unsigned)p.num_seqs * p.H * (DV / NC), W::kThreads, W::kAlloc, stream>>>(
-      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-      OutEpilogue{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms}, p.dev_err);
+      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o), ep,
+      p.dev_err);
   prof_end(stream);
   return cudaGetLastError();
 }
 
 template <int DV>
-cudaError_t launch_chain_wide(int ncol, const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
-                              const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
-                              const ChunkMap& map, cudaStream_t stream) {
+cudaError_t launch_chain_wide(int ncol, bool fuse_epilogue, const CUtensorMap& mWQ, const CUtensorMap& mP,
+                              const CUtensorMap& mKT, const CUtensorMap& mU, const CUtensorMap& mGam,
+                              const ChunkProblem& p, const ChunkMap& map, cudaStream_t stream) {
   constexpr int kFull = DV == 128 ? 128 : 64;
-  if (p.out_gate) return launch_chain_wide_nc<DV, kFull, true>(mWQ, mP, mKT, mU, mGam, p, map, stream);
+  if (fuse_epilogue) return launch_chain_wide_nc<DV, kFull, true>(mWQ, mP, mKT, mU, mGam, p, map, stream);
   if (DV == 128 && ncol == 128) return launch_chain_wide_nc<DV, kFull, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
   return launch_chain_wide_nc<DV, 64, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
 }
@@ -1561,7 +1616,9 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int cols = std::atoi(env);
     if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
-  if (p.out_gate) ncol = DV;   // the output epilogue needs a token's d_v outputs in one CTA
+  // The output epilogue needs a token's d_v outputs: fused into the chain when
+  // its CTAs hold all of them, else applied by a pass of its own afterwards.
+  const bool fuse = p.out_gate && ncol == DV;
   const bool wide = ncol != BV;
   CUtensorMap mWQ, mP, mKT, mU, mGam;
   const uint64_t Rr = R > 0 ? R : 1;
@@ -1572,13 +1629,24 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
                 wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (wide) return launch_chain_wide<DV>(ncol, mWQ, mP, mKT, mU, mGam, p, map, stream);
-  e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
-  if (e != cudaSuccess) return e;
-  prof_begin(stream, "chunk_chain_tc");
-  chunk_chain_tc<DV><<<(unsigned)p.num_seqs * p.H * (DV / BV), kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
-      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-      p.dev_err);
+  if (wide) {
+    e = launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
+  } else {
+    e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
+    if (e != cudaSuccess) return e;
+    prof_begin(stream, "chunk_chain_tc");
+    chunk_chain_tc<DV><<<(unsigned)p.num_seqs * p.H * (DV / BV), kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
+        mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
+        p.dev_err);
+    prof_end(stream);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess || !p.out_gate || fuse) return e;
+  const int64_t rows = p.total_tokens * p.H;
+  if (rows == 0) return cudaSuccess;
+  prof_begin(stream, "out_epilogue");
+  out_epilogue_kernel<DV><<<(unsigned)((rows + 8 * kEpiRows - 1) / (8 * kEpiRows)), 256, 0, stream>>>(
+      static_cast<bf16*>(p.o), static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms, rows, p.H);
   prof_end(stream);
   return cudaGetLastError();
 }
