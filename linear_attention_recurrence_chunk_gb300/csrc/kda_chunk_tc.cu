@@ -792,7 +792,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     }
     wu_pending = true;
     wu_rec = rec;
-    __syncthreads();   // shared memory is reused by the next task
+    // No barrier here: until the next task's first one the threads write only
+    // sBeta, whose last readers (the A / P epilogue, the operand of [w | u])
+    // finished before the barrier above; thread 0, held while the tensor pipe
+    // takes the [w | u] products, joins there (a barrier here cost 7 %).
   }
   if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
   if (bulk_pending) tc::bulk_wait0();   // thread 0: every record store has completed
