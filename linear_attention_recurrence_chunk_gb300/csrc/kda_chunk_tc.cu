@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   // accumulator (columns 0-255, rows 0-63 in lanes 0-63)
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescWU = tc::idesc_f16_f32(128, L::kWuN) | (1u << 16);   // B (KV) MN-major
+  constexpr int kWuIssuer = 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sRow = smem + L::oRow;   // row operand of the A / P products
@@ -276,8 +277,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
   uint32_t wu_parity = 0, ap_parity = 0;
   int64_t wu_rec = 0;
-  auto wu_drain = [&]() -> bool {
-    if (!wu_pending) return true;
+  // Returns the OR over the CTA of `raw_bad` (taken at the drain's CTA
+  // barrier, or at one of its own when nothing is pending); sets drain_ok.
+  bool drain_ok = true;
+  auto wu_drain = [&](bool raw_bad) -> bool {
+    drain_ok = true;
+    if (!wu_pending) return __syncthreads_or(raw_bad);
     const bool okw = tc::mbar_wait(bar + 1, wu_parity, kWaitLimit);
     wu_parity ^= 1u;
     wu_pending = false;
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     }
     tc::fence_proxy_async_smem();   // the tiles, written by the threads, read by the TMA unit
     tc::tc_fence_before();
-    __syncthreads();
+    const bool any_raw_bad = __syncthreads_or(raw_bad);
     if (tid == 0 && okw) {
 #pragma unroll
       for (int t = 0; t < L::kWuN / 64; ++t) {
@@ -311,7 +316,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       tc::bulk_commit();
       bulk_pending = true;
     }
-    return okw;
+    drain_ok = okw;
+    return any_raw_bad;
   };
 
   // This CTA's tasks are blockIdx.x + i * gridDim.x; (chunk, head) of the
@@ -388,14 +394,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2, r0 = 8 * rg;
     if (tid < C) sBeta[tid] = beta_cur;   // visible after the next CTA barrier
     const bool ok = tc::mbar_wait(bar, parity, kWaitLimit);
-    if (__syncthreads_or(!ok)) {   // a staging copy never landed: report, drain, stop
+    // The previous task's [w | u] (its CTA barrier also tells every thread
+    // whether a raw-row copy failed to land; no thread reads the rows before it).
+    if (wu_drain(!ok)) {   // a staging copy never landed: report, drain, stop
       if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
       tc::mbar_wait(bar, parity, kWaitLimit);
       failed = true;
       break;
     }
+    if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
     parity ^= 1u;
-    if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the previous task's [w | u]
     float2 G[8];
     {
       float2 run = make_float2(0.f, 0.f);
@@ -781,7 +789,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (tid == 0) {
+    if (tid == kWuIssuer) {   // lane 0 of warp 2, which has no part in the next drain: it catches up there
       const uint64_t dX = tc::desc_kmajor_sw128(tc::smem_u32(sX));
       const uint64_t dKV = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sKV), 8192);
       tc::mma_16bit_first(tmem, dX, dKV, kIdescWU);
@@ -794,10 +802,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     wu_rec = rec;
     // No barrier here: until the next task's first one the threads write only
     // sBeta, whose last readers (the A / P epilogue, the operand of [w | u])
-    // finished before the barrier above; thread 0, held while the tensor pipe
-    // takes the [w | u] products, joins there (a barrier here cost 7 %).
+    // finished before the barrier above; the issuing thread, held while the
+    // tensor pipe takes the [w | u] products, joins there (a barrier here cost 7 %).
   }
-  if (!wu_drain() && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);   // the last task's [w | u]
+  wu_drain(false);   // the last task's [w | u]
+  if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
   if (bulk_pending) tc::bulk_wait0();   // thread 0: every record store has completed
   (void)failed;
   tc::tc_fence_before();
