@@ -6,7 +6,9 @@ library never imports it) and follows the recurrence token by token as
 written on the page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读":
 §3.1 (the KDA update ``S_t = (I - beta k k^T) Diag(alpha) S_{t-1} + beta k v^T``,
 ``o_t = S_t^T q_t``), §3.2 (the order decay -> read -> write error -> read out)
-and §3.3 (``log alpha = -5 * Sigmoid(logit)``).  The arithmetic is in
+and §3.3 (``log alpha = -5 * Sigmoid(logit)``); optionally the unbounded
+``log alpha = -Softplus(logit)`` of the predecessor model (page "Kimi K3 架构篇：
+一文详解 2.8 万亿参数的巨型怪兽", "最被低估的一个细节：下界衰减").  The arithmetic is in
 ``kda_oracle.c``; this module compiles it with gcc and marshals numpy arrays.
 """
 from __future__ import annotations
@@ -24,6 +26,7 @@ _SRC = os.path.join(_HERE, "kda_oracle.c")
 _SO = os.path.join(_HERE, "libkda_oracle.so")
 
 F32, BF16, F64 = 0, 1, 2
+DECAY_BOUNDED, DECAY_SOFTPLUS = 0, 1
 _NP = {F32: np.float32, BF16: np.uint16, F64: np.float64}
 
 
@@ -53,6 +56,9 @@ def _lib():
         lib.kda_oracle_chains_snap.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                                i64, vp, vp]
         lib.kda_oracle_chains_snap.restype = ctypes.c_int
+        lib.kda_oracle_chains_map.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                              i64, vp, vp, i32]
+        lib.kda_oracle_chains_map.restype = ctypes.c_int
         lib.kda_oracle_max_threads.argtypes = []
         lib.kda_oracle_max_threads.restype = ctypes.c_int
         _handle = lib
@@ -71,7 +77,8 @@ def _arr(x, dtype_code):
 
 
 def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
-           row0: Sequence[int], n: Sequence[int], s0: Optional[np.ndarray] = None, snap_every: int = 0):
+           row0: Sequence[int], n: Sequence[int], s0: Optional[np.ndarray] = None, snap_every: int = 0,
+           decay_map: int = DECAY_BOUNDED):
     """Run independent chains over shared token arrays.
 
     ``q, k, g``: rows of ``d_k`` values, ``v``: rows of ``d_v`` (storage dtype:
@@ -81,7 +88,8 @@ def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
     Returns (list of ``[n[c], d_v]`` fp64 outputs, ``[nchains, d_k, d_v]`` fp64
     final states, threads used); with ``snap_every > 0`` a fourth item, the list
     of ``[n[c] // snap_every, d_k, d_v]`` fp64 states after every ``snap_every``
-    tokens of each chain."""
+    tokens of each chain.  ``decay_map``: ``DECAY_BOUNDED`` (-5 Sigmoid) or
+    ``DECAY_SOFTPLUS`` (-Softplus)."""
     q, k, g = _arr(q, dtype), _arr(k, dtype), _arr(g, dtype)
     v = _arr(v, dtype)
     beta = np.ascontiguousarray(beta, dtype=np.float32)
@@ -106,10 +114,10 @@ def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
     if nc > 1:
         soff[1:] = np.cumsum(counts[:-1])
     snaps = np.zeros((max(int(counts.sum()), 1), d_k, d_v), dtype=np.float64)
-    used = _lib().kda_oracle_chains_snap(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, dtype,
-                                         beta.ctypes.data, row_stride, d_k, d_v, nc, r0.ctypes.data,
-                                         nn.ctypes.data, s0p, o.ctypes.data, off.ctypes.data, s_out.ctypes.data,
-                                         snap_every, snaps.ctypes.data, soff.ctypes.data)
+    used = _lib().kda_oracle_chains_map(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, dtype,
+                                        beta.ctypes.data, row_stride, d_k, d_v, nc, r0.ctypes.data,
+                                        nn.ctypes.data, s0p, o.ctypes.data, off.ctypes.data, s_out.ctypes.data,
+                                        snap_every, snaps.ctypes.data, soff.ctypes.data, int(decay_map))
     if used < 0:
         raise ValueError("kda_oracle_chains: bad arguments")
     outs = [o[off[c]: off[c] + nn[c] * d_v].reshape(int(nn[c]), d_v) for c in range(nc)]
@@ -118,12 +126,12 @@ def chains(q, k, v, g, beta, dtype: int, d_k: int, d_v: int, row_stride: int,
     return outs, s_out, used
 
 
-def recurrence(q, k, v, g, beta, s0=None, dtype: int = F64):
+def recurrence(q, k, v, g, beta, s0=None, dtype: int = F64, decay_map: int = DECAY_BOUNDED):
     """One chain: ``q, k, g`` ``[n, d_k]``, ``v`` ``[n, d_v]``, ``beta`` ``[n]``,
     ``s0`` ``[d_k, d_v]`` or None.  Returns (o ``[n, d_v]``, S ``[d_k, d_v]``), fp64."""
     q = np.asarray(q)
     n, d_k = q.shape
     d_v = np.asarray(v).shape[1]
     outs, s_out, _ = chains(q, k, v, g, beta, dtype, d_k, d_v, 1, [0], [n],
-                            None if s0 is None else np.asarray(s0, dtype=np.float64)[None])
+                            None if s0 is None else np.asarray(s0, dtype=np.float64)[None], decay_map=decay_map)
     return outs[0], s_out[0]

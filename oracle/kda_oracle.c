@@ -10,6 +10,10 @@
  *     (lower-bounded decay): the per-key-channel log-decay is
  *     g_min * Sigmoid(logit) with g_min = -5, and alpha = exp(log-decay).
  *     The caller's logit already contains the per-head scale e^{A^h}.
+ *     Variant map (decay_map = 1): the predecessor model's unbounded map that
+ *     page "Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽" contrasts with the bound
+ *     (section "最被低估的一个细节：下界衰减"), log-decay = -Softplus(logit)
+ *     = -ln(1 + e^logit), which has no lower limit.
  *   - recurrence, same page §3.1 (KDA equation) and page "Kimi K3 架构篇：一文详解
  *     2.8 万亿参数的巨型怪兽", section "KDA 到底在算什么":
  *        S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
@@ -37,6 +41,9 @@
 #define ORACLE_BF16 1
 #define ORACLE_F64 2
 
+#define ORACLE_DECAY_BOUNDED 0
+#define ORACLE_DECAY_SOFTPLUS 1
+
 static double load_elem(const void* p, int dtype, int64_t i) {
   if (dtype == ORACLE_F64) return ((const double*)p)[i];
   if (dtype == ORACLE_F32) return (double)((const float*)p)[i];
@@ -47,8 +54,15 @@ static double load_elem(const void* p, int dtype, int64_t i) {
   return (double)f;
 }
 
-/* g_min * Sigmoid(x) with g_min = -5, then alpha = exp of it. */
-static double decay_alpha(double logit) {
+/* The log-decay of one channel, then alpha = exp of it:
+ *   bounded:  g_min * Sigmoid(x), g_min = -5;
+ *   softplus: -ln(1 + e^x), written max(x, 0) + ln(1 + e^{-|x|}) so that no
+ *             intermediate overflows (x = +inf gives alpha = 0, -inf gives 1). */
+static double decay_alpha(double logit, int decay_map) {
+  if (decay_map == ORACLE_DECAY_SOFTPLUS) {
+    const double softplus = (logit > 0.0 ? logit : 0.0) + log1p(exp(-fabs(logit)));
+    return exp(-softplus);
+  }
   const double sig = 1.0 / (1.0 + exp(-logit));
   return exp(-5.0 * sig);
 }
@@ -67,7 +81,7 @@ static double decay_alpha(double logit) {
 static void run_chain(const void* q, const void* k, const void* v, const void* g, int dtype,
                       const float* beta, int64_t row0, int64_t row_stride, int64_t n,
                       int32_t d_k, int32_t d_v, const double* s0, double* o, double* s_out,
-                      int64_t snap_every, double* snaps) {
+                      int64_t snap_every, double* snaps, int decay_map) {
   double* S = (double*)calloc((size_t)d_k * d_v, sizeof(double));
   double* kk = (double*)malloc(sizeof(double) * d_k);
   double* qq = (double*)malloc(sizeof(double) * d_k);
@@ -81,7 +95,7 @@ static void run_chain(const void* q, const void* k, const void* v, const void* g
     for (int32_t i = 0; i < d_k; ++i) {
       kk[i] = load_elem(k, dtype, row * d_k + i);
       qq[i] = load_elem(q, dtype, row * d_k + i);
-      alpha[i] = decay_alpha(load_elem(g, dtype, row * d_k + i));
+      alpha[i] = decay_alpha(load_elem(g, dtype, row * d_k + i), decay_map);
     }
     /* 1. decay: S_bar = Diag(alpha) S  (row i scaled by alpha_i) */
     for (int32_t i = 0; i < d_k; ++i)
@@ -120,15 +134,17 @@ static void run_chain(const void* q, const void* k, const void* v, const void* g
  * whose first row is row0[c] (rows advance by row_stride); its initial state is
  * s0 + c*d_k*d_v (s0 may be NULL), its outputs go to o + o_off[c] (n[c] x d_v)
  * and s_out + c*d_k*d_v (either may be NULL).  With snap_every > 0 its
- * n[c] / snap_every snapshots go to snaps + snap_off[c]*d_k*d_v.
+ * n[c] / snap_every snapshots go to snaps + snap_off[c]*d_k*d_v.  decay_map
+ * selects the gate (ORACLE_DECAY_BOUNDED or ORACLE_DECAY_SOFTPLUS).
  * Returns the number of threads used, or -1 on bad arguments.
  */
-int kda_oracle_chains_snap(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
-                           const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
-                           const int64_t* row0, const int64_t* n, const double* s0, double* o,
-                           const int64_t* o_off, double* s_out, int64_t snap_every, double* snaps,
-                           const int64_t* snap_off) {
+int kda_oracle_chains_map(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
+                          const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
+                          const int64_t* row0, const int64_t* n, const double* s0, double* o,
+                          const int64_t* o_off, double* s_out, int64_t snap_every, double* snaps,
+                          const int64_t* snap_off, int32_t decay_map) {
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return -1;
+  if (decay_map != ORACLE_DECAY_BOUNDED && decay_map != ORACLE_DECAY_SOFTPLUS) return -1;
   if (d_k <= 0 || d_v <= 0 || nchains < 0 || row_stride <= 0 || snap_every < 0) return -1;
   if (snap_every > 0 && snaps && !snap_off) return -1;
   int used = 1;
@@ -145,10 +161,19 @@ int kda_oracle_chains_snap(const void* q, const void* k, const void* v, const vo
       const int64_t dd = (int64_t)d_k * d_v;
       run_chain(q, k, v, g, dtype, beta, row0[c], row_stride, n[c], d_k, d_v, s0 ? s0 + c * dd : NULL,
                 o ? o + o_off[c] : NULL, s_out ? s_out + c * dd : NULL, snap_every,
-                (snap_every > 0 && snaps) ? snaps + snap_off[c] * dd : NULL);
+                (snap_every > 0 && snaps) ? snaps + snap_off[c] * dd : NULL, decay_map);
     }
   }
   return used;
+}
+
+int kda_oracle_chains_snap(const void* q, const void* k, const void* v, const void* g, int32_t dtype,
+                           const float* beta, int64_t row_stride, int32_t d_k, int32_t d_v, int32_t nchains,
+                           const int64_t* row0, const int64_t* n, const double* s0, double* o,
+                           const int64_t* o_off, double* s_out, int64_t snap_every, double* snaps,
+                           const int64_t* snap_off) {
+  return kda_oracle_chains_map(q, k, v, g, dtype, beta, row_stride, d_k, d_v, nchains, row0, n, s0, o, o_off,
+                               s_out, snap_every, snaps, snap_off, ORACLE_DECAY_BOUNDED);
 }
 
 int kda_oracle_chains(const void* q, const void* k, const void* v, const void* g, int32_t dtype,

@@ -349,3 +349,128 @@ def test_bf16_rounding_reading():
         assert o_excess(ob, o, "bf16").max() <= 1e-6 * rms
         assert (np.abs(ob - o) <= half_ulp_bf16(ob) * (1 + 2.0 ** -13)).all()
     assert worst_bare > 2e-2
+
+
+# ---- the unbounded -Softplus decay map (the predecessor model's gate that the
+# ---- second page contrasts with the lower bound, "最被低估的一个细节：下界衰减")
+
+def test_softplus_gate_special_values():
+    """log alpha = -ln(1 + e^x): logit 0 -> alpha = 1/2; ln(e - 1) -> 1/e;
+    +inf -> 0 (no lower limit); -inf -> 1.  Probed through beta = 0, where
+    S_1 = Diag(alpha) S_0."""
+    d = 4
+    s0 = np.arange(1.0, 1.0 + d * d).reshape(d, d)
+    g = np.array([[0.0, math.log(math.e - 1.0), np.inf, -np.inf]])
+    o, S = oracle.recurrence(np.eye(d)[[1]], np.zeros((1, d)), np.zeros((1, d)), g, np.zeros(1, np.float32), s0,
+                             decay_map=oracle.DECAY_SOFTPLUS)
+    expect = s0 * np.array([0.5, 1.0 / math.e, 0.0, 1.0])[:, None]
+    np.testing.assert_allclose(S, expect, rtol=1e-15, atol=0)
+    np.testing.assert_allclose(o[0], expect[1], rtol=1e-15, atol=0)
+
+
+def test_softplus_pure_decay_closed_form():
+    """beta = 0: S_t = Diag(exp(-sum_{tau<=t} Softplus(logit_tau))) S_0, with
+    Softplus from numpy's logaddexp(0, x)."""
+    rng = np.random.default_rng(21)
+    n, d_k, d_v = 40, 5, 7
+    q, k, v, g, _ = _rand_inputs(rng, n, d_k, d_v)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = oracle.recurrence(q, k, v, g, np.zeros(n, np.float32), s0, decay_map=oracle.DECAY_SOFTPLUS)
+    cum = np.cumsum(-np.logaddexp(0.0, g), axis=0)
+    for t in range(n):
+        St = np.exp(cum[t])[:, None] * s0
+        np.testing.assert_allclose(o[t], St.T @ q[t], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S, np.exp(cum[-1])[:, None] * s0, rtol=1e-12, atol=1e-14)
+
+
+def _brute_states_alpha(q, k, v, alpha, beta, s0):
+    """S_t (t = 1..n) from explicit M_t = (I - beta_t k_t k_t^T) Diag(alpha_t)."""
+    d_k = k.shape[1]
+    St, out = np.array(s0, dtype=np.float64), []
+    for t in range(len(q)):
+        M = (np.eye(d_k) - float(beta[t]) * np.outer(k[t], k[t])) @ np.diag(alpha[t])
+        St = M @ St + float(beta[t]) * np.outer(k[t], v[t])
+        out.append(St.copy())
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_softplus_brute_force_transition_product(seed):
+    """Tiny inputs, d_k != d_v: the oracle under the -Softplus map against
+    explicit transition products with alpha = 1 / (1 + e^x) (= e^{-Softplus(x)},
+    written without a logarithm), every o_t and the final state."""
+    rng = np.random.default_rng(400 + seed)
+    n, d_k, d_v = 8, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = oracle.recurrence(q, k, v, g, beta, s0, decay_map=oracle.DECAY_SOFTPLUS)
+    ref = _brute_states_alpha(q, k, v, 1.0 / (1.0 + np.exp(g)), beta, s0)
+    for t in range(n):
+        np.testing.assert_allclose(o[t], ref[t].T @ q[t], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(S, ref[-1], rtol=1e-12, atol=1e-13)
+
+
+def test_softplus_passes_the_tile_bound():
+    """All logits +40: each step decays by about e^{-40}, so 16 steps reach a
+    cumulative log-decay of -640, far past the -80 that the lower bound
+    guarantees for a 16-token tile (and past fp32's e^{-103}).  The fp64 oracle
+    stays finite and matches the closed form."""
+    n, d = 16, 4
+    s0 = np.full((d, d), 1.0e300)
+    g = np.full((n, d), 40.0)
+    o, S = oracle.recurrence(np.ones((n, d)), np.zeros((n, d)), np.zeros((n, d)), g, np.zeros(n, np.float32), s0,
+                             decay_map=oracle.DECAY_SOFTPLUS)
+    logdecay = -n * (40.0 + math.log1p(math.exp(-40.0)))
+    assert logdecay <= -640.0
+    assert np.isfinite(S).all() and np.isfinite(o).all()
+    np.testing.assert_allclose(S, math.exp(logdecay) * 1.0e300, rtol=1e-12)
+
+
+def test_decay_map_is_checked():
+    with pytest.raises(ValueError):
+        oracle.recurrence(np.ones((1, 2)), np.ones((1, 2)), np.ones((1, 2)), np.zeros((1, 2)),
+                          np.zeros(1, np.float32), decay_map=2)
+
+
+SOFTPLUS_MUTANTS = {
+    "positive part dropped": ("(logit > 0.0 ? logit : 0.0) + log1p", "0.0 + log1p"),
+    "tail sign": ("log1p(exp(-fabs(logit)))", "log1p(exp(fabs(logit)))"),
+    "tail without abs": ("log1p(exp(-fabs(logit)))", "log1p(exp(-logit))"),
+    "decay inverted": ("return exp(-softplus);", "return exp(softplus);"),
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(SOFTPLUS_MUTANTS))
+def test_softplus_planted_mistakes_fail_a_pin(mutant, tmp_path):
+    """A plausible mistake planted in the -Softplus branch of a compiled copy of
+    the oracle is rejected by the transition-product pin above."""
+    import ctypes
+    import subprocess
+
+    src = open(oracle._SRC).read()
+    old, new = SOFTPLUS_MUTANTS[mutant]
+    assert src.count(old) == 1, mutant
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fopenmp", "-fPIC", "-shared", str(mpath), "-o", str(so), "-lm"],
+                   check=True)
+    lib = ctypes.CDLL(str(so))
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    lib.kda_oracle_chains_map.argtypes = [vp, vp, vp, vp, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                          i64, vp, vp, i32]
+    lib.kda_oracle_chains_map.restype = ctypes.c_int
+    rng = np.random.default_rng(410)
+    n, d_k, d_v = 8, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, n, d_k, d_v, unit=False)
+    s0 = rng.normal(size=(d_k, d_v))
+    o, S = np.zeros((n, d_v)), np.zeros((d_k, d_v))
+    z, nn = np.zeros(1, np.int64), np.array([n], np.int64)
+    arrs = [np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, g)]
+    assert lib.kda_oracle_chains_map(*(a.ctypes.data for a in arrs), oracle.F64, beta.ctypes.data, 1, d_k, d_v, 1,
+                                     z.ctypes.data, nn.ctypes.data, s0.ctypes.data, o.ctypes.data, z.ctypes.data,
+                                     S.ctypes.data, 0, None, None, oracle.DECAY_SOFTPLUS) > 0
+    ref = _brute_states_alpha(q, k, v, 1.0 / (1.0 + np.exp(g)), beta, s0)
+    o_ref = np.stack([ref[t].T @ q[t] for t in range(n)])
+    err = max(np.abs(o - o_ref).max(), np.abs(S - ref[-1]).max())
+    assert err > 1e-6, f"mutant '{mutant}' was not caught (err {err:g})"
