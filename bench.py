@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-snapshots", action="store_true")
     ap.add_argument("--no-gated", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the decay-map ablation (diagonal tiles by position pairs, bounded and -Softplus maps)")
     ap.add_argument("--snapshot-interval", type=int, default=512)
     ap.add_argument("--decode-steps", type=int, default=100)
     ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD, "prefill_b8_h96_t8192_d128",
@@ -397,6 +399,53 @@ def bench_gated(args, r, steps):
             "note": "fused into the chain where its CTAs hold all d_v columns of a head, else a pass of its own over o"}
 
 
+def bench_decay_ablation(args, r, steps):
+    """The ablation of the lower-bounded decay on the same workload: the
+    diagonal 16x16 tiles of the intra-chunk matrices formed pair by pair on the
+    CUDA cores (one exponential per position pair and key channel) instead of
+    on the tensor cores, first under the bounded map itself (the cost of the
+    slow path alone), then under the unbounded -Softplus map that needs it.
+    Whole-call and per-kernel times with CUDA events on the launch stream."""
+    import torch
+
+    import linear_attention_recurrence_chunk_gb300 as kda
+
+    lib = kda.load_library()
+    w, t = r["w"], r["t"]
+    stream = torch.cuda.current_stream()
+    plain_ms = r["elapsed_ms"] / args.steps
+    plain_prep = statistics.mean(r["per_kernel"]["chunk_prep_tc"])
+    out = {"tensor_core_diagonal": {"ms_per_step": plain_ms, "prep_ms": plain_prep}}
+    for name, dmap in (("bounded_pairs", kda.DECAY_BOUNDED), ("softplus_pairs", kda.DECAY_SOFTPLUS)):
+        def step():
+            kda.kda_chunk_fwd_decay_variant(t["q"], t["k"], t["v"], t["g"], t["beta"], decay_map=dmap,
+                                            diag_by_pairs=True, initial_state=t["s0"], cu_seqlens=t["cu"],
+                                            o=r["o"], final_state=r["sf"], workspace=r["wsp"], stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        st, code = kda.kda_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {code} in the {name} leg")
+        _prof(lib, True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _prof(lib, False)
+        ms = e0.elapsed_time(e1) / steps
+        _, recs = _collect(lib)
+        prep = [v for nm, v in recs if nm.startswith("chunk_prep_tc")]
+        prep_ms = statistics.mean(prep) if prep else None
+        out[name] = {"ms_per_step": ms, "prep_ms": prep_ms, "value": w.tokens / (ms / 1e3), "unit": "tokens/s",
+                     "steps": steps, "slowdown_vs_tensor_core": ms / plain_ms,
+                     "prep_slowdown_vs_tensor_core": (prep_ms / plain_prep) if prep_ms else None}
+    return out
+
+
 def bench_e2e(args, w, wsp, steps):
     """Same metric through the Python API from pinned host buffers: every step
     copies its inputs host -> device, runs the call and copies o and the final
@@ -658,6 +707,8 @@ def main():
         line["snapshots"] = bench_snapshots(args, r, max(3, steps // 10))
     if not args.no_gated:
         line["gated"] = bench_gated(args, r, max(3, steps // 10))
+    if not args.no_ablation:
+        line["decay_ablation"] = bench_decay_ablation(args, r, max(3, steps // 10))
     if not args.no_e2e:
         line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
         if ws_size > 1:

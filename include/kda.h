@@ -65,6 +65,15 @@ typedef enum {
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
+/* Decay map of the gate logits g (kda_chunk_fwd_decay_variant):
+ *  KDA_DECAY_BOUNDED   log alpha = -5 Sigmoid(g), the lower-bounded decay of page
+ *                      "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读" §3.3 (what
+ *                      every other entry point applies);
+ *  KDA_DECAY_SOFTPLUS  log alpha = -Softplus(g) = -ln(1 + e^g), the unbounded map of
+ *                      the predecessor model that page "Kimi K3 架构篇：一文详解 2.8 万亿参数的
+ *                      巨型怪兽" contrasts with the bound ("最被低估的一个细节：下界衰减"). */
+typedef enum { KDA_DECAY_BOUNDED = 0, KDA_DECAY_SOFTPLUS = 1 } kda_decay_map;
+
 /* Human-readable name of a status code (static string, never NULL). */
 KDA_API const char* kda_status_string(kda_status s);
 
@@ -162,7 +171,32 @@ KDA_API kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void*
                                        size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * One decode step for N independent sequences (one new token each), the/*
+ * Chunked prefill under a chosen decay map and diagonal-block path: the
+ * ablation of the lower bound (page "Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽",
+ * "最被低估的一个细节：下界衰减": without a lower bound the factors e^{-G} inside a
+ * 16-token tile leave the floating-point range, so the diagonal tiles have to be
+ * formed pair by pair instead of on the tensor cores).  Arguments, layouts,
+ * results and errors are those of kda_chunk_fwd, plus:
+ *  decay_map      KDA_DECAY_BOUNDED or KDA_DECAY_SOFTPLUS (else KDA_ERR_INVALID_ARG);
+ *  diag_by_pairs  0: the diagonal 16x16 blocks of the intra-chunk matrices on the
+ *                 tensor cores (valid only with KDA_DECAY_BOUNDED, else
+ *                 KDA_ERR_UNSUPPORTED); 1: each entry of those blocks summed over
+ *                 the key channels on the CUDA cores with one exponential
+ *                 e^{G_r - G_i} <= 1 per position pair and channel (any map);
+ *                 other values: KDA_ERR_INVALID_ARG.
+ * Supported on the bf16 path with d_k = 128 (d_v = 64 or 128); other head sizes
+ * or fp32 inputs return KDA_ERR_UNSUPPORTED.  With KDA_DECAY_BOUNDED and
+ * diag_by_pairs = 0 it is kda_chunk_fwd.  Logits above 8.8e29 are taken as
+ * 8.8e29 under KDA_DECAY_SOFTPLUS (the decay factors they feed are 0 either way).
+ */
+KDA_API kda_status kda_chunk_fwd_decay_variant(const void* q, const void* k, const void* v, const void* g,
+                                               const float* beta, const float* initial_state,
+                                               const int32_t* cu_seqlens, int32_t num_seqs, int64_t B, int64_t T,
+                                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
+                                               float* final_state, int32_t decay_map, int32_t diag_by_pairs,
+                                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * One decode step for N independent sequences (one new token each), the
  * single-token interface of page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读"
  * §3.2 restricted to the recurrence: (q, k, v, g, beta, S_{t-1}) -> (o_t, S_t).

@@ -18,6 +18,10 @@ Functions keep the C names:
 * ``kda_chunk_fwd_gated(q, k, v, g, beta, out_gate, norm_weight=None, ...)`` ->
   ``(o, final_state)``: the same with the output epilogue (Sigmoid gate times
   the per-head RMSNorm of o) applied before o is written (same page §3.2).
+* ``kda_chunk_fwd_decay_variant(q, k, v, g, beta, decay_map, diag_by_pairs, ...)``
+  -> ``(o, final_state)``: the same under the unbounded -Softplus decay map or
+  with the diagonal tiles formed by position pairs, the ablation of the lower
+  bound (page "Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽", "最被低估的一个细节：下界衰减").
 * ``kda_decode_step(q, k, v, g, beta, state, o=None)`` -> ``o``: one token per
   sequence (same page §3.2), state updated in place.
 * ``kda_decode_layer_step(q_in, k_in, v_in, z, A_log, beta_logit, conv_cache,
@@ -37,9 +41,11 @@ import torch
 
 from . import _build
 
-__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_chunk_fwd_gated", "kda_decode_step", "kda_decode_layer_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
+__all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_chunk_fwd_gated", "kda_chunk_fwd_decay_variant",
+           "DECAY_BOUNDED", "DECAY_SOFTPLUS", "kda_decode_step", "kda_decode_layer_step", "kda_chunk_fwd_workspace_size", "kda_device_error",
            "kda_check_wait_timeout", "KdaError", "library_path", "load_library", "STATUS"]
 
+DECAY_BOUNDED, DECAY_SOFTPLUS = 0, 1   # kda_decay_map
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
           4: "KDA_ERR_DEVICE_TIMEOUT"}
 _DT = {torch.float32: 0, torch.bfloat16: 1}
@@ -82,6 +88,9 @@ def load_library():
     lib.kda_chunk_fwd_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32, ctypes.c_int,
                                         vp, vp, vp, vp, ctypes.c_float, vp, sz, vp]
     lib.kda_chunk_fwd_gated.restype = ctypes.c_int
+    lib.kda_chunk_fwd_decay_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i64, i32, i32, i32,
+                                                ctypes.c_int, vp, vp, i32, i32, vp, sz, vp]
+    lib.kda_chunk_fwd_decay_variant.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp, vp]
     lib.kda_decode_step.restype = ctypes.c_int
     f32 = ctypes.c_float
@@ -218,6 +227,39 @@ def kda_chunk_fwd_gated(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: to
                                  _ptr(final_state), _ptr(out_gate), _ptr(norm_weight), float(eps_rms),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "kda_chunk_fwd_gated")
+    return o, final_state
+
+
+def kda_chunk_fwd_decay_variant(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                                beta: torch.Tensor, decay_map: int = DECAY_BOUNDED, diag_by_pairs: bool = True,
+                                initial_state: Optional[torch.Tensor] = None,
+                                cu_seqlens: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                                o: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked prefill under ``decay_map`` (``DECAY_BOUNDED``: -5 Sigmoid,
+    ``DECAY_SOFTPLUS``: -Softplus) with the diagonal 16x16 tiles either on the
+    tensor cores (``diag_by_pairs=False``, bounded map only) or formed pair by
+    pair on the CUDA cores.  Arguments otherwise as ``kda_chunk_fwd``."""
+    lib = load_library()
+    B, T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    num_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if output_final_state and final_state is None:
+        final_state = torch.empty((num_seqs, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    if not output_final_state:
+        final_state = None
+    ws_bytes = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd_decay_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                         _ptr(cu_seqlens), num_seqs, B, T, H, d_k, d_v, _dtype_code(q), _ptr(o),
+                                         _ptr(final_state), int(decay_map), int(bool(diag_by_pairs)),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream))
+    _check(st, "kda_chunk_fwd_decay_variant")
     return o, final_state
 
 

@@ -112,7 +112,8 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
                           int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
                           float* final_state, float* snapshots, int32_t snapshot_interval,
                           int64_t snapshot_capacity, const void* out_gate, const float* norm_weight, float eps_rms,
-                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                          int32_t decay_map = KDA_DECAY_BOUNDED, int32_t diag_pairs = 0) {
   const bool varlen = cu_seqlens != nullptr;
   kda_status st = check_chunk_shape(B, T, H, d_k, d_v, num_seqs, dt, varlen);
   if (st != KDA_OK) return st;
@@ -178,6 +179,15 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
     }
   }
 
+  // Decay-map ablation: on the bf16 tensor-core path (d_k = 128) only; the
+  // unbounded map needs the pair path for the diagonal blocks.
+  if (decay_map != KDA_DECAY_BOUNDED && decay_map != KDA_DECAY_SOFTPLUS) return KDA_ERR_INVALID_ARG;
+  if (diag_pairs != 0 && diag_pairs != 1) return KDA_ERR_INVALID_ARG;
+  if (decay_map != KDA_DECAY_BOUNDED || diag_pairs) {
+    if (!kda::tc_path_supported(d_k, d_v, dt)) return KDA_ERR_UNSUPPORTED;
+    if (decay_map == KDA_DECAY_SOFTPLUS && !diag_pairs) return KDA_ERR_UNSUPPORTED;
+  }
+
   if (num_seqs == 0) return KDA_OK;
 
   int32_t* dev_err = nullptr;
@@ -192,6 +202,8 @@ kda_status chunk_fwd_impl(const void* q, const void* k, const void* v, const voi
   p.out_gate = out_gate;
   p.norm_weight = norm_weight;
   p.eps_rms = eps_rms;
+  p.decay_map = decay_map;
+  p.diag_pairs = diag_pairs;
   return kda::launch_chunk_fwd(p, ws, workspace, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -216,6 +228,16 @@ kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, cons
   return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
                         final_state, nullptr, 0, 0, out_gate, norm_weight, eps_rms, workspace, workspace_bytes,
                         stream);
+}
+
+kda_status kda_chunk_fwd_decay_variant(const void* q, const void* k, const void* v, const void* g, const float* beta,
+                                       const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs,
+                                       int64_t B, int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt,
+                                       void* o, float* final_state, int32_t decay_map, int32_t diag_by_pairs,
+                                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
+                        final_state, nullptr, 0, 0, nullptr, nullptr, 0.f, workspace, workspace_bytes, stream,
+                        decay_map, diag_by_pairs);
 }
 
 kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const void* v, const void* g, const float* beta,

@@ -115,6 +115,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// log2 of the unbounded decay, -Softplus(x) / ln 2 = -log2(1 + 2^y) with
+// y = x log2(e), as -(max(y, 0) + log2(1 + 2^{-|y|})) so that nothing
+// overflows; y is capped at 2^100 (logits above 8.8e29), which keeps a chunk's
+// sum finite (the factors it feeds are then 0 either way).
+__device__ __forceinline__ float fast_log2_softplus_decay(float x) {
+  float y = x * 1.4426950408889634f;
+  y = y > 1.2676506e30f ? 1.2676506e30f : y;   // NaN passes through
+  return -(fmaxf(y, 0.f) + lg2_approx(1.f + ex2_approx(-fabsf(y))));
+}
+template <bool kSoftplus>
+__device__ __forceinline__ float log2_decay(float x) {
+  return kSoftplus ? fast_log2_softplus_decay(x) : fast_log2_decay(x);
+}
 
 // bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
@@ -155,8 +173,24 @@ __device__ __forceinline__ uint32_t kv_off(int k, int n) {
 // --------------------------------------------------------------- prep kernel
 constexpr int kPrepTcThreads = 512;
 
-template <int DV>
+// Variants of the prep kernel (the decay-map ablation):
+//   kPrepBounded       -5 Sigmoid gate, diagonal 16x16 blocks of A and P on the
+//                      tensor cores with the sub-tile-start reference, whose
+//                      factors e^{G_s - G_i} stay below e^80 only because of the
+//                      lower bound (page "Kimi K3：架构、训练与百万 Token Agentic RL 技术解读",
+//                      §3.3 "lower-bounded decay");
+//   kPrepBoundedPairs  the same gate, diagonal blocks by position pairs;
+//   kPrepSoftplusPairs the unbounded -Softplus gate of the predecessor model
+//                      (page "Kimi K3 架构篇：一文详解 2.8 万亿参数的巨型怪兽", section
+//                      "最被低估的一个细节：下界衰减"), which only the pair path can take.
+// The pair path forms each diagonal-block entry as a sum over the key channels
+// of k_r k_i e^{G_r - G_i} (and q_r k_i e^{G_r - G_i}) on the CUDA cores, one
+// exponential per pair and channel, with every exponent <= 0.
+constexpr int kPrepBounded = 0, kPrepBoundedPairs = 1, kPrepSoftplusPairs = 2;
+
+template <int DV, int kVariant = kPrepBounded>
 struct PrepTcSmem {
+  static constexpr bool kPairs = kVariant != kPrepBounded;
   static constexpr int LDX = C + 8;           // fp16 row stride of A's off-diagonal blocks
   static constexpr int kWuN = DK + DV;        // columns of [w | u]
   static constexpr int LDA = C + 1;           // fp32 row stride of A's diagonal blocks
@@ -201,7 +235,21 @@ struct PrepTcSmem {
                     (oRawV % 1024) == 0,
                 "TMA, tcgen05 operand and mbarrier alignment");
   static_assert(kAlloc <= 232448, "fits the 227 KB shared-memory limit");
+  // The pair path keeps the per-token decays (fp32 [64][DK], rows 0-31 and 32-63)
+  // in column-operand rows 0-127 of the two channel atoms, which its product
+  // does not read.
+  static constexpr size_t oAlpha0 = oCol, oAlpha1 = oCol + kColAtom;
+  static_assert(32 * DK * 4 <= 128 * 128, "half of the decays fits 128 operand rows");
 };
+
+// (r, i) of the s-th strictly lower pair of a 16x16 block (0 <= s < 120), the
+// order the pair path enumerates them in: rows r = 1..15, and in each row the
+// columns i = r-1 down to 0, s = r (r - 1) / 2 + (r - 1 - i).
+__device__ __forceinline__ void pair_unrank(int s, int& r, int& i) {
+  r = 1;
+  while ((r + 1) * r / 2 <= s) ++r;
+  i = r - 1 - (s - r * (r - 1) / 2);
+}
 
 // Row (in the column operand) of column i of later sub-tile a' = 1..3, minus 128.
 __device__ __forceinline__ int later_row0(int a2) { return a2 == 1 ? 0 : (a2 == 2 ? 16 : 48); }
@@ -213,7 +261,7 @@ __device__ __forceinline__ uint32_t opnd_off(int rows, int row, int ch) {
 }
 
 
-template <int DV>
+template <int DV, int kVariant>
 __global__ void __launch_bounds__(kPrepTcThreads, 1)
     chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
@@ -221,8 +269,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                   const __grid_constant__ CUtensorMap tmPs,
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
-  using L = PrepTcSmem<DV>;
+  using L = PrepTcSmem<DV, kVariant>;
   constexpr int LDX = L::LDX, LDA = L::LDA;
+  constexpr bool kPairs = L::kPairs, kSoftplus = kVariant == kPrepSoftplusPairs;
+  // TMEM column of the first block below the diagonal (the pair path's
+  // product holds those blocks only)
+  constexpr int kLaterCol = kPairs ? 0 : 2 * C;
   constexpr int NTH = kPrepTcThreads;
   // TMEM: the A / P accumulators (columns 0-287) and, after them, the [w | u]
   // accumulator (columns 0-255, rows 0-63 in lanes 0-63)
@@ -346,9 +398,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   auto arm = [&](int4 ci) {
     if (ci.y > 0 && tid == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)C * (3 * DK + DV) * 2);
   };
-  auto issue = [&](int32_t ht, int4 ci) {
+  // `which_mask`: bit t selects tensor t (g, k, q, v); the pair path stages g
+  // and v a task ahead as usual, k and q once it has read the current ones.
+  auto issue = [&](int32_t ht, int4 ci, unsigned which_mask = 15u) {
     if (ci.y <= 0 || warp < 12 || warp >= 16 || lane != 0) return;
     const int which = warp - 12;
+    if (!((which_mask >> which) & 1u)) return;
     const CUtensorMap* m = which == 0 ? &tmG : (which == 1 ? &tmK : (which == 2 ? &tmQ : &tmV));
     tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, ht, ci.z, bar);
   };
@@ -411,8 +466,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       for (int rr = 0; rr < 8; ++rr) {
         const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
         if (r0 + rr < len) {
-          run.x += fast_log2_decay(__low2float(x));
-          run.y += fast_log2_decay(__high2float(x));
+          run.x += log2_decay<kSoftplus>(__low2float(x));
+          run.y += log2_decay<kSoftplus>(__high2float(x));
         }
         G[rr] = run;
       }
@@ -437,7 +492,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       bulk_pending = false;
     }
     __syncthreads();   // every raw read is done; the group sums are visible
-    issue(h_next, ci_next);
+    issue(h_next, ci_next, kPairs ? 0x9u : 15u);   // the pair path reads k and q until its epilogue
 
     // 2. Offsets from the group sums: G_s(a') = cumulative decay before sub-tile
     //    a', G_last; then the per-thread factors e^{G_s(a') - G_s(a)}, a' >= a.
@@ -453,6 +508,16 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         acc.y += t2.y;
       }
       gl = acc;
+      if constexpr (kPairs) {   // the per-token decay alpha_r = 2^{G_r - G_{r-1}} for the pair path, from the
+                                // thread's own partial sums (small exponents)
+        float* adst = reinterpret_cast<float*>(smem + (rg < 4 ? L::oAlpha0 : L::oAlpha1)) + (r0 & 31) * DK + c;
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const float2 prev = rr ? G[rr - 1] : make_float2(0.f, 0.f);
+          *reinterpret_cast<float2*>(adst + rr * DK) =
+              make_float2(ex2_approx(G[rr].x - prev.x), ex2_approx(G[rr].y - prev.y));
+        }
+      }
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         G[rr].x += excl.x;
@@ -466,8 +531,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     float2 om[4];
 #pragma unroll
     for (int a2 = 0; a2 < 4; ++a2)
-      om[a2] = a2 > a ? make_float2(ex2_approx(gsA[a2].x - gs.x), ex2_approx(gsA[a2].y - gs.y))
-                      : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
+      om[a2] = (!kPairs && a2 > a) ? make_float2(ex2_approx(gsA[a2].x - gs.x), ex2_approx(gsA[a2].y - gs.y))
+                                   : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
     if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(ex2_approx(gl.x), ex2_approx(gl.y));
 
     // 3. The operands of the A / P products (every 16-bit operand is stored as
@@ -477,10 +542,20 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       const int r = r0 + rr;
       const float2 gr = G[rr];
       const float e0 = ex2_approx(gr.x - gs.x), e1 = ex2_approx(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]: normal
-      const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
       const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
       const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
       *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, r, c)) = pack_bf16x2(k0 * e0, k1 * e1);
+      if constexpr (kPairs) {   // blocks below the diagonal only: every factor e^{G_a - G_b} <= 1, one ex2 each
+        *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, C + r, c)) = pack_bf16x2(q0 * e0, q1 * e1);
+#pragma unroll
+        for (int a2 = 1; a2 < 4; ++a2) {
+          if (a2 > a)
+            *reinterpret_cast<uint32_t*>(sCol + opnd_off(L::kColRows, 2 * C + later_row0(a2) + r, c)) =
+                pack_bf16x2(k0 * ex2_approx(gsA[a2].x - gr.x), k1 * ex2_approx(gsA[a2].y - gr.y));
+        }
+        continue;
+      }
+      const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
       uint32_t hi, lo;
       split_bf16x2(q0 * e0, q1 * e1, hi, lo);
       *reinterpret_cast<uint32_t*>(sRow + opnd_off(L::kRowRows, C + r, c)) = hi;
@@ -508,8 +583,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     //    diagonal blocks, the low-part products D1[64 + r][64 + i] + D2[64 + r][i].
     if (tid == 0) {
       const uint64_t dR = tc::desc_kmajor_sw128(tc::smem_u32(sRow));
-      const uint64_t dC = tc::desc_kmajor_sw128(tc::smem_u32(sCol));
-      constexpr uint32_t kId1 = tc::idesc_bf16_f32(128, L::kColRows), kId2 = tc::idesc_bf16_f32(128, C);
+      // the pair path multiplies by the later sub-tiles' rows only (128-223: N = 96)
+      const uint64_t dC = tc::desc_kmajor_sw128(tc::smem_u32(sCol + (kPairs ? 2 * C * 128 : 0)));
+      constexpr uint32_t kId1 = tc::idesc_bf16_f32(128, kPairs ? L::kColRows - 2 * C : L::kColRows),
+                         kId2 = tc::idesc_bf16_f32(128, C);
 #pragma unroll
       for (int kk = 0; kk < DK / 16; ++kk) {
         const uint64_t oR = (((kk >> 2) * L::kRowAtom) + (kk & 3) * 32) >> 4;
@@ -520,7 +597,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
           tc::mma_16bit_acc(tmem, dR + oR, dC + oC, kId1);
       }
 #pragma unroll
-      for (int kk = 0; kk < DK / 16; ++kk) {
+      for (int kk = 0; kk < (kPairs ? 0 : DK / 16); ++kk) {
         const uint64_t oR = (((kk >> 2) * L::kRowAtom) + C * 128 + (kk & 3) * 32) >> 4;
         const uint64_t oC = (((kk >> 2) * L::kColAtom) + (kk & 3) * 32) >> 4;
         if (kk == 0)
@@ -571,6 +648,122 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         *reinterpret_cast<uint4*>(sKV + kv_off(r, DK + c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
+    // 4b. The pair path: the diagonal 16x16 blocks of A and P from the raw k, q
+    //     and the per-token decays, on the CUDA cores while the products run.
+    //     Warp w takes a quarter (w % 4) of the 256 entries of sub-tile w / 4:
+    //     entries 2s and 2s + 1 are A and P of the s-th strictly lower pair
+    //     (r, i), entries 240 + d the P diagonal (d, d).  A lane sums over its 4
+    //     key channels, with the pair's decay e^{G_r - G_i} = prod_{i<m<=r} alpha_m
+    //     carried along the row as i descends (one product per pair, every
+    //     factor <= 1, so no exponent can leave the range whatever the map);
+    //     the warp then reduces over lanes in halving steps (each lane keeps half
+    //     of the entries it still holds, plus its partner's copy of them), so
+    //     lane l ends with the warp's entries 2l and 2l + 1.
+    float pv[2] = {0.f, 0.f};
+    if constexpr (kPairs) {
+      const int sa = warp >> 2, part = warp & 3, c4 = 4 * lane, row0 = 16 * sa;
+      auto alpha_row = [&](int row) -> float4 {   // row within the sub-tile
+        const int rc = row0 + row;
+        const float* base = reinterpret_cast<const float*>(smem + (rc < 32 ? L::oAlpha0 : L::oAlpha1));
+        return *reinterpret_cast<const float4*>(base + (rc & 31) * DK + c4);
+      };
+      auto unpack = [](uint2 w, float (&x)[4]) {
+        x[0] = __uint_as_float(w.x << 16);
+        x[1] = __uint_as_float(w.x & 0xffff0000u);
+        x[2] = __uint_as_float(w.y << 16);
+        x[3] = __uint_as_float(w.y & 0xffff0000u);
+      };
+      auto ld_bf4 = [&](const bf16* base, int row) -> uint2 {
+        return *reinterpret_cast<const uint2*>(base + (row0 + row) * DK + c4);
+      };
+      // A cursor: pair (r, i), k and q of row r (as floats), and e = e^{G_r - G_i}
+      // per channel.
+      struct Cursor {
+        int r, i;
+        float k[4], q[4];
+        float4 e;
+      };
+      auto start = [&](Cursor& cu, int sidx) {
+        pair_unrank(sidx, cu.r, cu.i);
+        unpack(ld_bf4(rawK, cu.r), cu.k);
+        unpack(ld_bf4(rawQ, cu.r), cu.q);
+        cu.e = alpha_row(cu.r);
+        for (int m = cu.r - 1; m > cu.i; --m) {   // a start inside the row
+          const float4 am = alpha_row(m);
+          cu.e = make_float4(cu.e.x * am.x, cu.e.y * am.y, cu.e.z * am.z, cu.e.w * am.w);
+        }
+      };
+      auto advance = [&](Cursor& cu) {   // warp-uniform: every lane walks the same pairs
+        if (cu.i == 0) {                  // next row, first pair (r + 1, r)
+          ++cu.r;
+          cu.i = cu.r - 1;
+          unpack(ld_bf4(rawK, cu.r), cu.k);
+          unpack(ld_bf4(rawQ, cu.r), cu.q);
+          cu.e = alpha_row(cu.r);
+        } else {                          // (r, i - 1): one more factor alpha_i
+          const float4 am = alpha_row(cu.i);
+          cu.e = make_float4(cu.e.x * am.x, cu.e.y * am.y, cu.e.z * am.z, cu.e.w * am.w);
+          --cu.i;
+        }
+      };
+      auto term = [&](const Cursor& cu, float& av, float& pw) {
+        float ki[4];
+        unpack(ld_bf4(rawK, cu.i), ki);
+        const float e[4] = {cu.e.x, cu.e.y, cu.e.z, cu.e.w};
+        av = 0.f;
+        pw = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const float t = ki[ch] * e[ch];
+          av = fmaf(cu.k[ch], t, av);
+          pw = fmaf(cu.q[ch], t, pw);
+        }
+      };
+      auto diag = [&](int d) -> float {   // P (d, d): the factor is e^0
+        float kr[4], qr[4];
+        unpack(ld_bf4(rawK, d), kr);
+        unpack(ld_bf4(rawQ, d), qr);
+        return fmaf(qr[3], kr[3], fmaf(qr[2], kr[2], fmaf(qr[1], kr[1], qr[0] * kr[0])));
+      };
+      // pairs 32 part + m (lower half of the entries) and 32 part + 16 + m (upper half)
+      const bool hi_pairs = part < 3;   // part 3: 8 upper pairs (s = 112..119), then the P diagonal
+      Cursor lo, hi;
+      start(lo, 32 * part);
+      start(hi, 32 * part + 16);
+      const bool up = (lane & 16) != 0;
+      float keep[32];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        float a_lo, p_lo, a_hi, p_hi;
+        term(lo, a_lo, p_lo);
+        if (hi_pairs || m < 8) {
+          term(hi, a_hi, p_hi);
+        } else {
+          a_hi = diag(2 * (m - 8));
+          p_hi = diag(2 * (m - 8) + 1);
+        }
+        const float xa = __shfl_xor_sync(0xffffffffu, up ? a_lo : a_hi, 16);
+        const float xp = __shfl_xor_sync(0xffffffffu, up ? p_lo : p_hi, 16);
+        keep[2 * m] = (up ? a_hi : a_lo) + xa;
+        keep[2 * m + 1] = (up ? p_hi : p_lo) + xp;
+        if (m < 15) {
+          advance(lo);
+          if (hi_pairs || m < 7) advance(hi);
+        }
+      }
+#pragma unroll
+      for (int msk = 8, n = 32; msk >= 1; msk >>= 1, n >>= 1) {
+        const bool hb = (lane & msk) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+          const float x = __shfl_xor_sync(0xffffffffu, hb ? keep[j] : keep[n / 2 + j], msk);
+          keep[j] = (hb ? keep[n / 2 + j] : keep[j]) + x;
+        }
+      }
+      pv[0] = keep[0];
+      pv[1] = keep[1];
+    }
+
     // 5. A and P out of TMEM: A to shared memory, P to the record tile.
     {
       const bool okap = tc::mbar_wait(bar + 2, ap_parity, kWaitLimit);
@@ -587,8 +780,8 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         const int ap = 2 * (q & 1) + part;   // the sub-tile of lanes 16 part .. 16 part + 15
         float v[16];
         if (q < 2) {
-          if (b > ap) continue;
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, b == ap ? 16 * b : 2 * C + later_row0(ap) + 16 * b), v);
+          if (b > ap || (kPairs && b == ap)) continue;   // the pair path writes the diagonal blocks
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, b == ap ? 16 * b : kLaterCol + later_row0(ap) + 16 * b), v);
           if (ar != ap) continue;
           const float br = sBeta[rr];
           if (b == ap) {   // diagonal block, fp32 (only its strictly lower part is read)
@@ -606,6 +799,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
           } else if (b == ap) {
+            if constexpr (kPairs) continue;
             float w2[16];
             tc::tmem_ld16(tc::tmem_addr(tmem, tl, 16 * b), v);
             tc::tmem_ld16(tc::tmem_addr(tmem, tl, C + 16 * b), w2);
@@ -615,7 +809,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = i <= (rr & 15) ? v[i] + w2[i] : 0.f;   // inclusive lower triangle
           } else {
-            tc::tmem_ld16(tc::tmem_addr(tmem, tl, 2 * C + later_row0(ap) + 16 * b), v);
+            tc::tmem_ld16(tc::tmem_addr(tmem, tl, kLaterCol + later_row0(ap) + 16 * b), v);
           }
           if (ar != ap) continue;
 #pragma unroll
@@ -626,6 +820,21 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         }
       }
     }
+    if constexpr (kPairs) {   // the pair path's entries: A (beta-weighted, fp32) and P (fp16, zero above)
+      const int sa = warp >> 2, part = warp & 3;
+      if (part < 3 || lane < 24) {
+        int r, i;
+        pair_unrank(32 * part + lane, r, i);
+        const int R = 16 * sa + r, I = 16 * sa + i;
+        sA[R * LDA + I] = sBeta[R] * pv[0];
+        *reinterpret_cast<f16*>(sPst + xs_off(R, I)) = __float2half_rn(pv[1]);
+        *reinterpret_cast<f16*>(sPst + xs_off(I, R)) = __float2half_rn(0.f);
+      } else {
+        const int R = 16 * sa + 2 * (lane - 24);
+        *reinterpret_cast<f16*>(sPst + xs_off(R, R)) = __float2half_rn(pv[0]);
+        *reinterpret_cast<f16*>(sPst + xs_off(R + 1, R + 1)) = __float2half_rn(pv[1]);
+      }
+    }
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     __syncthreads();
@@ -634,6 +843,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       tc::bulk_commit();
       bulk_pending = true;
     }
+    if constexpr (kPairs) issue(h_next, ci_next, 0x6u);   // k and q of this task are no longer read
 
     // 6. X = (I + A)^{-1}, in fp16 (the precision w and u are formed in):
     //    diagonal 16x16 blocks (only their strictly lower parts are read) by
@@ -1602,19 +1812,29 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
         !make_map(&mUs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mPs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    const size_t smem = PrepTcSmem<DV>::kAlloc;
-    e = cudaFuncSetAttribute(chunk_prep_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
     const int grid = (int)std::min<int64_t>(n_tasks, sms);
-    prof_begin(stream, "chunk_prep_tc");
-    chunk_prep_tc<DV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, mWs, mUs, mPs, p.beta, p.num_seqs, p.H, map, rec,
-                                                              n_tasks, p.dev_err);
-    prof_end(stream);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto prep = [&](auto variant_tag, const char* name) -> cudaError_t {
+      constexpr int kV = decltype(variant_tag)::value;
+      const size_t smem = PrepTcSmem<DV, kV>::kAlloc;
+      cudaError_t err = cudaFuncSetAttribute(chunk_prep_tc<DV, kV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (err != cudaSuccess) return err;
+      prof_begin(stream, name);
+      chunk_prep_tc<DV, kV><<<grid, kPrepTcThreads, smem, stream>>>(mG, mK, mQ, mV, mWs, mUs, mPs, p.beta, p.num_seqs,
+                                                                    p.H, map, rec, n_tasks, p.dev_err);
+      prof_end(stream);
+      return cudaGetLastError();
+    };
+    if (p.decay_map == KDA_DECAY_SOFTPLUS)
+      e = prep(std::integral_constant<int, kPrepSoftplusPairs>{}, "chunk_prep_tc_softplus_pairs");
+    else if (p.diag_pairs)
+      e = prep(std::integral_constant<int, kPrepBoundedPairs>{}, "chunk_prep_tc_pairs");
+    else
+      e = prep(std::integral_constant<int, kPrepBounded>{}, "chunk_prep_tc");
+    if (e != cudaSuccess) return e;
   }
   // Chain variant: 32 value columns per CTA (the most CTAs, for few long
   // chains) unless that grid exceeds one wave of the GPU; then one CTA per

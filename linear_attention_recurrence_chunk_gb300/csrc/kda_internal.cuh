@@ -104,6 +104,8 @@ struct ChunkProblem {
   const void* out_gate;       // output epilogue: gate logits [tokens][H][d_v] or nullptr (none)
   const float* norm_weight;   // its RMSNorm weight [H][d_v] or nullptr (ones)
   float eps_rms;
+  int32_t decay_map;     // KDA_DECAY_BOUNDED or KDA_DECAY_SOFTPLUS (tensor-core path only)
+  int32_t diag_pairs;    // nonzero: diagonal blocks of A and P by position pairs (tensor-core path only)
   int32_t* dev_err;
 };
 

@@ -32,9 +32,10 @@ def prefill_device_inputs(w: ks.PrefillWorkload, device="cuda"):
     return prefill_inputs(w, device)
 
 
-def oracle_chains(w: ks.PrefillWorkload, pairs, ntok=None):
+def oracle_chains(w: ks.PrefillWorkload, pairs, ntok=None, decay_map=oracle.DECAY_BOUNDED):
     """Oracle (o [n, d_v], S [d_k, d_v]) for each (seq, head) in ``pairs``
-    (first ``ntok`` tokens of each sequence if given), OpenMP across chains."""
+    (first ``ntok`` tokens of each sequence if given), OpenMP across chains,
+    under the given decay map."""
     ins = [w.chain_inputs(s, h, ntok) for s, h in pairs]
     n = [len(x["beta"]) for x in ins]
     cat = {k: np.concatenate([x[k] for x in ins]) for k in ("q", "k", "v", "g", "beta")}
@@ -43,7 +44,7 @@ def oracle_chains(w: ks.PrefillWorkload, pairs, ntok=None):
         s0 = np.stack([x["s0"] for x in ins]).astype(np.float64)
     row0 = np.concatenate([[0], np.cumsum(n)[:-1]])
     outs, states, _ = oracle.chains(cat["q"], cat["k"], cat["v"], cat["g"], cat["beta"], ORACLE_DT[w.dtype],
-                                    w.d_k, w.d_v, 1, row0, n, s0)
+                                    w.d_k, w.d_v, 1, row0, n, s0, decay_map=decay_map)
     return outs, states
 
 

@@ -142,6 +142,30 @@ def test_chunk_fwd_gated_rejects_bad_arguments_on_host():
     assert _gated(lib, B=0, num_seqs=0) == 0                    # nothing to do, no CUDA call
 
 
+def _variant(lib, **kw):
+    args = dict(q=FAKE, k=FAKE + (1 << 30), v=FAKE + (2 << 30), g=FAKE + (3 << 30), beta=FAKE + (4 << 30),
+                s0=None, cu=None, num_seqs=1, B=1, T=64, H=2, dk=128, dv=128, dt=1, o=FAKE + (5 << 30),
+                sf=None, dmap=1, pairs=1, ws=FAKE + (6 << 30), wsb=1 << 40)
+    args.update(kw)
+    return lib.kda_chunk_fwd_decay_variant(args["q"], args["k"], args["v"], args["g"], args["beta"], args["s0"],
+                                           args["cu"], args["num_seqs"], args["B"], args["T"], args["H"], args["dk"],
+                                           args["dv"], args["dt"], args["o"], args["sf"], args["dmap"],
+                                           args["pairs"], args["ws"], args["wsb"], None)
+
+
+def test_chunk_fwd_decay_variant_rejects_bad_arguments_on_host():
+    lib = kda.load_library()
+    assert _variant(lib, dmap=2) == 1 and _variant(lib, dmap=-1) == 1   # no such decay map
+    assert _variant(lib, pairs=2) == 1
+    assert _variant(lib, dmap=1, pairs=0) == 2                  # the unbounded map needs the pair path
+    assert _variant(lib, dt=0) == 2                             # fp32: not on the tensor-core path
+    assert _variant(lib, dk=64) == 2
+    assert _variant(lib, dmap=0, pairs=1, dv=96) == 2
+    assert _variant(lib, q=None) == 1                           # the kda_chunk_fwd checks still apply
+    assert _variant(lib, dmap=2, B=0, num_seqs=0) == 1          # checked before the empty-batch return
+    assert _variant(lib, B=0, num_seqs=0) == 0                  # nothing to do, no CUDA call
+
+
 def test_decode_rejects_bad_arguments_on_host():
     lib = kda.load_library()
     f = lib.kda_decode_step
