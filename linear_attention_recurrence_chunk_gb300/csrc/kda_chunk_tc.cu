@@ -227,9 +227,8 @@ struct PrepTcSmem {
   static constexpr size_t oXb = (oA + (size_t)C * LDA * 4 + 1023) / 1024 * 1024;
   static constexpr size_t oAh = oXb + (size_t)2 * C * C * 2;         // fp16 [64][LDX]  A, blocks below them
   static constexpr size_t oYh = oAh + (size_t)C * LDX * 2;           // fp16 [7][16][24] scratch blocks of the inverse
-  static constexpr size_t oWst = oRow;                               // [w | u] tiles of the previous task (8 KB each)
   static_assert(oYh + 7 * 16 * 24 * 2 <= oKV, "aliases fit in the operand area");
-  static_assert(oWst + (size_t)(kWuN / 64) * 8192 <= oKV, "the [w | u] tiles fit the operand area");
+  static_assert(oKV + (size_t)(kWuN / 64) * 8192 <= oPst, "the [w | u] tiles fit the area of its operand");
   static_assert((oRow % 1024) == 0 && (oCol % 1024) == 0 && (kRowAtom % 1024) == 0 && (kColAtom % 1024) == 0 &&
                     (oXb % 1024) == 0 && (oKV % 1024) == 0 && (oPst % 1024) == 0 && (oBar % 8) == 0 &&
                     (oRawV % 1024) == 0,
@@ -321,11 +320,12 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   const uint32_t tmem = *reinterpret_cast<const uint32_t*>(smem + L::oTmem);
 
   // [w | u] of a task is multiplied on the tensor cores after its inverse and
-  // read out of TMEM at the start of the next task (or after the last one):
-  // the warps of lane quarters 0 and 1 take rows 32(w%4)..+31 and columns
-  // 64(w/4)..+63 into 64-column tiles (128-byte swizzle) in the then free
-  // operand area, which thread 0 stores to the record with TMA; the tiles are
-  // released (bulk read wait) before the operand area is rewritten.
+  // read out of TMEM in the next task, after its gate and scan (or after the
+  // last task): the warps of lane quarters 0 and 1 take rows 32(w%4)..+31 and
+  // columns 64(w/4)..+63 into 64-column tiles (128-byte swizzle) in the area of
+  // the product's own B operand, free once the product is done, which thread 0
+  // stores to the record with TMA; the tiles are released (bulk read wait)
+  // before that area is rewritten.
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
   uint32_t wu_parity = 0, ap_parity = 0;
   int64_t wu_rec = 0;
@@ -339,17 +339,18 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     wu_parity ^= 1u;
     wu_pending = false;
     tc::tc_fence_after();
-    uint8_t* stg = smem + L::oWst;   // tile t (columns 64t..64t+63) at stg + 8 KB * t
+    uint8_t* stg = smem + L::oKV;   // tile t (columns 64t..64t+63) at stg + 8 KB * t, in the product's own
+                                    // operand area (rewritten only after the pre-product barrier)
     const int qw = warp & 3, cg = warp >> 2;
     if (qw < 2 && 64 * cg < L::kWuN) {
       const int r = 32 * qw + lane;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[32];
-        tc::tmem_ld32(tc::tmem_addr(tmem, (uint32_t)(32 * qw), (uint32_t)(64 * cg + 32 * hf)), v);
+      for (int qt = 0; qt < 4; ++qt) {   // 16 columns at a time (the gate/scan registers are live here)
+        float v[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, (uint32_t)(32 * qw), (uint32_t)(64 * cg + 16 * qt)), v);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(stg + cg * 8192 + xs_off(r, 32 * hf + 8 * j)) =
+        for (int j = 0; j < 2; ++j)
+          *reinterpret_cast<uint4*>(stg + cg * 8192 + xs_off(r, 16 * qt + 8 * j)) =
               make_uint4(pack_f16x2(v[8 * j + 0], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
                          pack_f16x2(v[8 * j + 4], v[8 * j + 5]), pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
       }
@@ -448,28 +449,30 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     //    the raw k, q, v of the thread are read before the area is reused.
     const int rg = tid >> 6, a = rg >> 1, c = (tid & 63) * 2, r0 = 8 * rg;
     if (tid < C) sBeta[tid] = beta_cur;   // visible after the next CTA barrier
+    // (A copy that never landed leaves stale rows here; the CTA barrier of the
+    // drain below tells every thread, and nothing read from them is used.)
     const bool ok = tc::mbar_wait(bar, parity, kWaitLimit);
-    // The previous task's [w | u] (its CTA barrier also tells every thread
-    // whether a raw-row copy failed to land; no thread reads the rows before it).
-    if (wu_drain(!ok)) {   // a staging copy never landed: report, drain, stop
-      if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
-      tc::mbar_wait(bar, parity, kWaitLimit);
-      failed = true;
-      break;
-    }
-    if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
-    parity ^= 1u;
     float2 G[8];
     {
       float2 run = make_float2(0.f, 0.f);
+      if (r0 + 8 <= len) {   // every row of the thread is a token (warp-uniform)
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
-        if (r0 + rr < len) {
+        for (int rr = 0; rr < 8; ++rr) {
+          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
           run.x += log2_decay<kSoftplus>(__low2float(x));
           run.y += log2_decay<kSoftplus>(__high2float(x));
+          G[rr] = run;
         }
-        G[rr] = run;
+      } else {               // rows past the sequence end carry no decay
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * DK + c);
+          if (r0 + rr < len) {
+            run.x += log2_decay<kSoftplus>(__low2float(x));
+            run.y += log2_decay<kSoftplus>(__high2float(x));
+          }
+          G[rr] = run;
+        }
       }
       *reinterpret_cast<float2*>(sTot + rg * DK + c) = run;
     }
@@ -487,11 +490,17 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       vraw[e2] = *reinterpret_cast<const uint4*>(rawV + (idx / (DV / 8)) * DV + (idx % (DV / 8)) * 8);
     }
     arm(ci_next);
-    if (bulk_pending) {   // thread 0: the P and [w | u] tiles stored so far have been read by the TMA unit
-      tc::bulk_wait_read0();
-      bulk_pending = false;
+    // The previous task's [w | u], whose product ran during the steps above.
+    // The drain's CTA barrier also ends every raw read, makes the group sums
+    // visible and tells every thread whether a raw-row copy failed to land.
+    if (wu_drain(!ok)) {   // a staging copy never landed: report, drain, stop
+      if (tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      tc::mbar_wait(bar, parity, kWaitLimit);
+      failed = true;
+      break;
     }
-    __syncthreads();   // every raw read is done; the group sums are visible
+    if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    parity ^= 1u;
     issue(h_next, ci_next, kPairs ? 0x9u : 15u);   // the pair path reads k and q until its epilogue
 
     // 2. Offsets from the group sums: G_s(a') = cumulative decay before sub-tile
@@ -571,6 +580,10 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
               pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
       }
     }
+    if (bulk_pending) {   // thread 0: the P and [w | u] tiles stored so far have been read by the TMA unit
+      tc::bulk_wait_read0();   // (both areas are rewritten after the barrier below)
+      bulk_pending = false;
+    }
     tc::fence_proxy_async_smem();   // the operands, written by the threads, read by the MMAs
     tc::tc_fence_before();
     __syncthreads();
@@ -613,6 +626,9 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     // start (2^G and 2^{G_last - G} directly).
     {
       uint32_t kt0[4], kt1[4];   // K~^T rows c and c+1, tokens r0..r0+7, fp16 pairs
+      float bw[8];   // beta of the thread's rows (two broadcast loads)
+      *reinterpret_cast<float4*>(bw) = *reinterpret_cast<const float4*>(sBeta + r0);
+      *reinterpret_cast<float4*>(bw + 4) = *reinterpret_cast<const float4*>(sBeta + r0 + 4);
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = r0 + rr;
@@ -621,7 +637,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
         const float el0 = ex2_approx(gl.x - gr.x), el1 = ex2_approx(gl.y - gr.y);   // e^{G_last - G_r}
         const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
         const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
-        const float br = sBeta[r];
+        const float br = bw[rr];
         *reinterpret_cast<uint32_t*>(sKV + kv_off(r, c)) = pack_f16x2(br * k0 * eg0, br * k1 * eg1);
         *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * eg0, q1 * eg1);
         const __half2 kt = __floats2half2_rn(k0 * el0, k1 * el1);
@@ -838,7 +854,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     __syncthreads();
-    if (tid == 0) {   // P to the record (the tile is released at the next task's first CTA barrier)
+    if (tid == 0) {   // P to the record (the tile is released before the next task's product barrier)
       tc::tma_store_2d(&tmPs, 0, (int32_t)(rec * C), sPst);
       tc::bulk_commit();
       bulk_pending = true;
