@@ -1,0 +1,127 @@
+"""The rounding scheme of the tensor-core prefill path, emulated in numpy and
+checked against the fp64 oracle on the CPU: what each intermediate is rounded
+to decides whether the bf16 tolerance (2e-2 rms(o), with each stored value's
+half-ulp on top) holds, so the choices are pinned here rather than only on the
+GPU.
+
+The emulated path follows the chunked algebra (pinned against the oracle in
+test_chunk_algebra.py) with the kernels' operands and records:
+  - A / P products: bf16 operands referenced to the 16-token sub-tile start,
+    fp32 accumulation; the diagonal sub-tiles of P as hi + lo bf16 parts of
+    both operands (three products), those of A from the high parts; A's
+    diagonal blocks kept in fp32, its other blocks and P stored in fp16;
+  - X = (I + A)^{-1}, the [w | u] operand and w, u, q e^G, (k e^{G_last-G})^T
+    in fp16 (P V_new and w S are the error-sensitive products: V_new is
+    O(|v|) while o is an order of magnitude smaller);
+  - the chain: fp32 master state, its fp16 copy and V_new in fp16 as MMA
+    operands, o rounded to bf16.
+X is formed exactly from the rounded A and then rounded; the kernel's fp16
+products for X's blocks below the diagonal also round their intermediate
+16x16 blocks, which this does not model.
+Two alternatives are shown to miss the bound: every intermediate in bf16,
+and the scheme without the hi / lo split of P's diagonal sub-tiles.
+"""
+import numpy as np
+import pytest
+
+import kda_synth as ks
+import oracle
+from kda_testutil import o_excess
+
+C, SUB = 64, 16
+
+
+def _bf16(x):
+    return ks.bf16_bits_to_f64(ks.f32_to_bf16_bits(np.asarray(x, dtype=np.float32)))
+
+
+def _f16(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def _split(x):
+    hi = _bf16(x)
+    return hi, _bf16(x - hi)
+
+
+def emulate(q, k, v, g, beta, s0, scheme):
+    """o [T, d_v] (bf16 values) and S [d_k, d_v] under the given scheme:
+    'kernel', 'no_split' (P's diagonal sub-tiles single bf16) or 'bf16' (every
+    intermediate bf16, no split)."""
+    T, d_k = q.shape
+    rec = _bf16 if scheme == "bf16" else _f16
+    S = np.array(s0, dtype=np.float64)
+    outs = []
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        kk, qq, vv, bb = (np.zeros((C,) + x.shape[1:]) for x in (k, q, v, beta))
+        kk[:L], qq[:L], vv[:L], bb[:L] = k[c0:c0 + L], q[c0:c0 + L], v[c0:c0 + L], beta[c0:c0 + L]
+        ld = np.zeros((C, d_k))
+        ld[:L] = -5.0 / (1.0 + np.exp(-g[c0:c0 + L]))
+        G = np.cumsum(ld, axis=0)
+        Gs = np.stack([G[SUB * a - 1] if a else np.zeros(d_k) for a in range(C // SUB)])   # decay before sub-tile a
+        A = np.zeros((C, C))
+        P = np.zeros((C, C))
+        for a in range(C // SUB):
+            rows = slice(SUB * a, SUB * a + SUB)
+            rk = _bf16(kk[rows] * np.exp(G[rows] - Gs[a]))            # row operands, factors <= 1
+            rq_hi, rq_lo = _split(qq[rows] * np.exp(G[rows] - Gs[a]))
+            cd_hi, cd_lo = _split(kk[rows] * np.exp(Gs[a] - G[rows]))   # own sub-tile, factors >= 1
+            if scheme != "kernel":
+                rq_hi, rq_lo = _bf16(qq[rows] * np.exp(G[rows] - Gs[a])), 0.0 * rq_lo
+                cd_lo = 0.0 * cd_lo
+            A[rows, rows] = _f32(rk @ cd_hi.T)
+            P[rows, rows] = _f32(rq_hi @ cd_hi.T + rq_hi @ cd_lo.T + rq_lo @ cd_hi.T)
+            for b in range(a):   # earlier sub-tiles, referenced to the start of sub-tile a: factors <= 1
+                cols = slice(SUB * b, SUB * b + SUB)
+                cl = _bf16(kk[cols] * np.exp(Gs[a] - G[cols]))
+                A[rows, cols] = _f32(rk @ cl.T)
+                P[rows, cols] = _f32(_bf16(qq[rows] * np.exp(G[rows] - Gs[a])) @ cl.T)
+        A = np.tril(A, -1) * bb[:, None]
+        diag = np.kron(np.eye(C // SUB), np.ones((SUB, SUB))).astype(bool)
+        A = np.where(diag, A, rec(A))           # diagonal blocks fp32, the rest in the record precision
+        P = rec(np.tril(P))
+        X = rec(np.linalg.inv(np.eye(C) + A))
+        w = rec(X @ rec(bb[:, None] * kk * np.exp(G)))
+        u = rec(X @ rec(bb[:, None] * vv))
+        qh = rec(qq * np.exp(G))
+        kt = rec(kk * np.exp(G[-1] - G))
+        gam = np.exp(G[-1])
+        Sop = rec(S)
+        vn = rec(u - w @ Sop)
+        o = _bf16(qh @ Sop + P @ vn)
+        S = _f32(gam[:, None] * S + kt.T @ vn)
+        outs.append(o[:L])
+    return np.concatenate(outs), S
+
+
+def _worst(scheme, cases=((5, 0.05, 300), (7, 0.01, 640))):
+    worst_o, worst_s = 0.0, 0.0
+    for seed, s0_std, T in cases:
+        w = ks.PrefillWorkload("prec", "bf16", 1, T, 2, 128, 128, seed=seed, s0_std=s0_std)
+        for h in range(w.H):
+            ci = w.chain_inputs(0, h)
+            f = ks.bf16_bits_to_f64
+            s0 = ci["s0"].astype(np.float64)
+            o_ref, s_ref = oracle.recurrence(ci["q"], ci["k"], ci["v"], ci["g"], ci["beta"], s0, dtype=oracle.BF16)
+            o, S = emulate(f(ci["q"]), f(ci["k"]), f(ci["v"]), f(ci["g"]), ci["beta"].astype(np.float64), s0, scheme)
+            rms = np.sqrt(np.mean(o_ref ** 2))
+            worst_o = max(worst_o, float(o_excess(o, o_ref, "bf16").max() / rms))
+            worst_s = max(worst_s, float(np.linalg.norm(S - s_ref) / np.linalg.norm(s_ref)))
+    return worst_o, worst_s
+
+
+def test_kernel_scheme_meets_the_bf16_bound_with_margin():
+    o_err, s_err = _worst("kernel")
+    assert o_err <= 0.5 * 2e-2, o_err
+    assert s_err <= 1e-2, s_err
+
+
+@pytest.mark.parametrize("scheme", ["bf16", "no_split"])
+def test_rejected_schemes_miss_the_bound(scheme):
+    o_err, _ = _worst(scheme)
+    assert o_err > 2e-2, (scheme, o_err)
