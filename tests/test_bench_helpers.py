@@ -50,3 +50,22 @@ def test_single_rank_helpers():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.min_over_ranks(2.0, 1) == 2.0
     assert abs(bench.job_throughput(1000.0, 4, 2.0, 1) - 1000.0 * 4 / 0.002) < 1e-6
+
+
+def test_algorithmic_bytes_of_the_prefill_workloads():
+    """The roofline numerators: q, k, g, v, o at 2 bytes and beta at 4 per
+    head-token (1284 B at d = 128), plus 128 KiB per (sequence, head) for each
+    state read or written; the prep kernel is charged its inputs (1028 B per
+    head-token), the chain kernels o and the states."""
+    import kda_synth as ks
+
+    wl = ks.workloads()
+    w1 = wl["prefill_b1_h32_t65536_d128"]            # S0 given: read and written
+    ht = 65536 * 32
+    assert bench.prefill_alg_bytes(w1, "path") == ht * 1284 + 2 * 32 * 128 * 128 * 4 == 2_696_937_472
+    assert bench.prefill_alg_bytes(w1, "chunk_prep_tc") == ht * 1028
+    assert bench.prefill_alg_bytes(w1, "chunk_chain_tc") == ht * 256 + 2 * 32 * 128 * 128 * 4
+    w2 = wl["prefill_b8_h96_t8192_d128"]             # no S0: final states written only
+    assert bench.prefill_alg_bytes(w2, "path") == 8 * 8192 * 96 * 1284 + 8 * 96 * 128 * 128 * 4
+    w4 = wl["varlen_12seq_1m_h32_d128"]
+    assert abs(bench.prefill_alg_bytes(w4, "path") - 4.31e10) / 4.31e10 < 0.01
