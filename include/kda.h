@@ -244,7 +244,6 @@ KDA_API kda_status kda_decode_layer_step(const void* q_in, const void* k_in, con
                                          kda_dtype dt, void* o, cudaStream_t stream);
 
 /*
- * Reads and clears this device's error word/*
  * Reads and clears this device's error word (on the current device), after
  * waiting for `stream`.  *code receives the raw word (0 = none).  Returns
  * KDA_OK when it was 0, KDA_ERR_INVALID_ARG for a malformed cu_seqlens,
