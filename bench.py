@@ -225,6 +225,60 @@ def get_workload(name):
     return ks.workloads()[name]
 
 
+def global_workload(w, ws: int):
+    """The whole job at ``ws`` ranks under weak scaling: ``ws`` copies of the
+    workload's shape as one batch of sequences (B x ws sequences, or the varlen
+    length list repeated ws times), each with its own seeded values."""
+    import dataclasses
+
+    if ws == 1:
+        return w
+    if w.seq_lens is None:
+        return dataclasses.replace(w, name=f"{w.name}_x{ws}", B=w.B * ws)
+    lens = np.tile(np.asarray(w.seq_lens), ws)
+    return dataclasses.replace(w, name=f"{w.name}_x{ws}", T=int(lens.sum()), seq_lens=lens)
+
+
+def shard_sequences(num_seqs: int, ws: int):
+    """(first sequence, count) of each rank: contiguous blocks, sizes differing
+    by at most one, every sequence (with all its heads) on exactly one rank."""
+    base, extra = divmod(num_seqs, ws)
+    out, first = [], 0
+    for r in range(ws):
+        n = base + (1 if r < extra else 0)
+        out.append((first, n))
+        first += n
+    return out
+
+
+def rank_workload(w, rank: int, ws: int):
+    """This rank's part of the whole job: its block of sequences, all heads."""
+    if ws == 1:
+        return w
+    wg = global_workload(w, ws)
+    first, n = shard_sequences(wg.num_seqs, ws)[rank]
+    return wg.shard(first, n, name=f"{wg.name}[seqs {first}:{first + n}]")
+
+
+def maybe_spawn(args) -> bool:
+    """``--gpus N`` (N > 1) without a launcher: start N local ranks under
+    torch.distributed.run on 127.0.0.1 with the same arguments and wait for
+    them.  Returns True when it did (this process then only relays)."""
+    if args.gpus <= 1 or "WORLD_SIZE" in os.environ:
+        return False
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    rc = subprocess.call(cmd)
+    if rc != 0:
+        sys.exit(rc)
+    return True
+
+
 def dist_setup(args):
     import torch
 
@@ -277,7 +331,8 @@ def bench_prefill(args, ws_size, local):
     import linear_attention_recurrence_chunk_gb300 as kda
     from kda_synth.torchio import prefill_inputs
 
-    w = get_workload(args.workload)
+    ws_rank = int(os.environ.get("RANK", "0"))
+    w = rank_workload(get_workload(args.workload), ws_rank, ws_size)
     t = prefill_inputs(w, "cuda")
     lib = kda.load_library()
     stream = torch.cuda.current_stream()
@@ -322,6 +377,28 @@ def bench_prefill(args, ws_size, local):
             "per_kernel": per_kernel, "clocks": clocks, "o": o, "sf": sf, "wsp": wsp}
 
 
+def timed_steps(step, steps: int, stream):
+    """Runs ``steps`` calls of ``step`` with a CUDA event before each and after
+    the last, on the launch stream.  Returns (mean ms per step, spread) where
+    spread holds the per-step min / median / max."""
+    import torch
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total = ev[0].elapsed_time(ev[steps])
+    return total / steps, {"min_ms": min(per), "median_ms": statistics.median(per), "max_ms": max(per)}
+
+
+def side_leg_steps(steps: int) -> int:
+    """Timed steps of each side leg: at least 20."""
+    return max(20, steps // 10)
+
+
 def bench_snapshots(args, r, steps):
     """The same prefill with the state kept every ``--snapshot-interval`` tokens
     (the prefix-cache snapshots, 512 tokens on the pages), timed with CUDA
@@ -347,18 +424,13 @@ def bench_snapshots(args, r, steps):
     st, code = kda.kda_device_error()
     if st != 0:
         raise RuntimeError(f"device error {code} in the snapshot leg")
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms, spread = timed_steps(step, steps, stream)
     plain_ms = r["elapsed_ms"] / args.steps
     del snaps
     return {"interval_tokens": every, "snapshots_per_step": slots * w.H,
             "snapshot_bytes_per_step": slots * w.H * w.d_k * w.d_v * 4, "value": w.tokens / (ms / 1e3),
-            "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "slowdown_vs_plain": ms / plain_ms}
+            "unit": "tokens/s", "ms_per_step": ms, "steps": steps, "spread": spread,
+            "slowdown_vs_plain": ms / plain_ms}
 
 
 def bench_gated(args, r, steps):
@@ -386,16 +458,10 @@ def bench_gated(args, r, steps):
     st, code = kda.kda_device_error()
     if st != 0:
         raise RuntimeError(f"device error {code} in the gated leg")
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms, spread = timed_steps(step, steps, stream)
     del gate, nw
     return {"value": w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
+            "spread": spread, "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
             "note": "fused into the chain where its CTAs hold all d_v columns of a head, else a pass of its own over o"}
 
 
@@ -429,19 +495,13 @@ def bench_decay_ablation(args, r, steps):
         if st != 0:
             raise RuntimeError(f"device error {code} in the {name} leg")
         _prof(lib, True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+        ms, spread = timed_steps(step, steps, stream)
         _prof(lib, False)
-        ms = e0.elapsed_time(e1) / steps
         _, recs = _collect(lib)
         prep = [v for nm, v in recs if nm.startswith("chunk_prep_tc")]
         prep_ms = statistics.mean(prep) if prep else None
         out[name] = {"ms_per_step": ms, "prep_ms": prep_ms, "value": w.tokens / (ms / 1e3), "unit": "tokens/s",
-                     "steps": steps, "slowdown_vs_tensor_core": ms / plain_ms,
+                     "steps": steps, "spread": spread, "slowdown_vs_tensor_core": ms / plain_ms,
                      "prep_slowdown_vs_tensor_core": (prep_ms / plain_prep) if prep_ms else None}
     return out
 
@@ -496,17 +556,29 @@ def bench_e2e(args, w, wsp, steps):
     for i in range(2):
         step(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    block = 5   # steps per spread sample
+    e0 = torch.cuda.Event(enable_timing=True)
+    marks = []
     t0 = time.perf_counter()
     e0.record(s_in)   # before the first timed copy in ...
     for i in range(steps):
         step(i)
-    e1.record(s_out)  # ... after the last copy out, which follows every earlier step on the device
+        if (i + 1) % block == 0 or i + 1 == steps:   # ... after a copy out, which follows every earlier step
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(s_out)
+            marks.append((i + 1, e))
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
-    ms = e0.elapsed_time(e1)
+    ms = e0.elapsed_time(marks[-1][1])
+    per_block, prev_n, prev_t = [], 0, 0.0
+    for n_, e in marks:
+        t_ = e0.elapsed_time(e)
+        per_block.append((t_ - prev_t) / (n_ - prev_n))
+        prev_n, prev_t = n_, t_
     return {"value": w.tokens * steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": ms / steps,
+            "spread": {"blocks_of_steps": block, "min_ms": min(per_block), "median_ms": statistics.median(per_block),
+                       "max_ms": max(per_block)},
             "wall_s": round(wall, 3), "pipelined": "next step's inputs copied while the current one computes"}
 
 
@@ -662,6 +734,8 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if maybe_spawn(args):
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -692,9 +766,13 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_size, "steps": steps,
         "warmup": args.warmup, "ms_per_step": r["max_ms"] / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "d_k": w.d_k, "d_v": w.d_v,
+        "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "d_k": w.d_k, "d_v": w.d_v,
                    "state": "fp32, S0 ~ N(0, 0.01)", "chunk": 64,
-                   "l2": "no flush: 2.1 GB of inputs per step, larger than L2"},
+                   "l2": "no flush: 2.1 GB of inputs per step, larger than L2",
+                   "parallelism": ("single GPU" if ws_size == 1 else
+                                   f"dp{ws_size}: the job is {ws_size} x the workload's sequences; each rank runs "
+                                   f"its own block of sequences (all heads), no collective on the data path"),
+                   "global_sequences": w.num_seqs * ws_size},
         "roofline": roof,
         "path_roofline": {"bound": "hbm", "achieved": path_ach, "peak": peak, "unit": "GB/s",
                           "frac": path_ach / peak, "alg_bytes_per_step": path_alg},
@@ -704,13 +782,13 @@ def main():
         "clocks": r["clocks"],
     }
     if not args.no_snapshots:
-        line["snapshots"] = bench_snapshots(args, r, max(3, steps // 10))
+        line["snapshots"] = bench_snapshots(args, r, side_leg_steps(steps))
     if not args.no_gated:
-        line["gated"] = bench_gated(args, r, max(3, steps // 10))
+        line["gated"] = bench_gated(args, r, side_leg_steps(steps))
     if not args.no_ablation:
-        line["decay_ablation"] = bench_decay_ablation(args, r, max(3, steps // 10))
+        line["decay_ablation"] = bench_decay_ablation(args, r, side_leg_steps(steps))
     if not args.no_e2e:
-        line["e2e"] = bench_e2e(args, w, r["wsp"], max(3, steps // 20))
+        line["e2e"] = bench_e2e(args, w, r["wsp"], side_leg_steps(steps))
         if ws_size > 1:
             line["e2e"]["value"] = min_over_ranks(line["e2e"]["value"], ws_size) * ws_size
     del r

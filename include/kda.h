@@ -26,9 +26,10 @@
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
  *    errors are detected on the host and returned before anything is launched.
  *    A launch failure returns KDA_ERR_CUDA.  Conditions only the device can see
- *    (a malformed cu_seqlens array, a bounded device-side wait that ran out)
- *    set a per-device error word instead; read and clear it with
- *    kda_device_error() after the work has finished.
+ *    (a malformed cu_seqlens array, a bounded device-side wait that ran out,
+ *    an inf or NaN in the tensor-core prefill's outputs) set a per-device error
+ *    word instead; read and clear it with kda_device_error() after the work has
+ *    finished.
  *  - q and k are used as given (any L2 normalisation happens upstream); g is
  *    the raw decay logit (any per-head scale is already folded into it); beta is
  *    the write strength, already in (0, 1), as fp32.  No 1/sqrt(d_k) factor is
@@ -60,7 +61,8 @@ typedef enum {
   KDA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment, alias or workspace */
   KDA_ERR_UNSUPPORTED = 2,    /* valid request outside what the kernels cover (head size) */
   KDA_ERR_CUDA = 3,           /* a CUDA runtime call or a launch failed */
-  KDA_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (see kda_device_error) */
+  KDA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait gave up (see kda_device_error) */
+  KDA_ERR_NONFINITE = 5       /* an output or final state came out inf / NaN (see kda_device_error) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -110,6 +112,16 @@ KDA_API size_t kda_chunk_fwd_workspace_size(int64_t B, int64_t T, int32_t H, int
  *  bytes, 256-byte aligned, owned by the caller; its contents on entry do not
  *  matter and on return are unspecified.  Two calls in flight at once need two
  *  workspaces.
+ *  Range of the bf16 path with d_k = 128 (the tensor-core path): the chain's
+ *  intermediates u = (I + A)^{-1} Diag(beta) V, V_new = u - w S, beta v and the
+ *  copy of the state the tensor cores multiply are held in fp16, whose largest
+ *  finite value is 65504.  On inputs like the benchmark's (unit-norm q, k)
+ *  |u| and |V_new| reach about 1-2x max|v| and the state about |S_0| plus
+ *  max|v|, so |v| and |S| must stay below about 3e4 (2e4 leaves margin).
+ *  Beyond that a value becomes inf; the chain then reports
+ *  KDA_ERR_NONFINITE through kda_device_error() (it checks every o and final
+ *  state value it writes), and o / final_state hold inf or NaN.  fp32 inputs
+ *  and d_k = 64 run in fp32 throughout and have no such limit.
  */
 KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const void* g, const float* beta,
                          const float* initial_state, const int32_t* cu_seqlens, int32_t num_seqs,
@@ -247,8 +259,11 @@ KDA_API kda_status kda_decode_layer_step(const void* q_in, const void* k_in, con
  * Reads and clears this device's error word (on the current device), after
  * waiting for `stream`.  *code receives the raw word (0 = none).  Returns
  * KDA_OK when it was 0, KDA_ERR_INVALID_ARG for a malformed cu_seqlens,
- * KDA_ERR_DEVICE_TIMEOUT for a device-side wait that ran out, KDA_ERR_CUDA if
- * the read itself failed.
+ * KDA_ERR_DEVICE_TIMEOUT for a device-side wait that ran out,
+ * KDA_ERR_NONFINITE when a tensor-core prefill wrote an inf or NaN output or
+ * final state (the fp16 range of kda_chunk_fwd exceeded, or non-finite
+ * inputs), KDA_ERR_CUDA if the read itself failed.  The word keeps the first
+ * non-finite report and the last of the other codes.
  */
 KDA_API kda_status kda_device_error(cudaStream_t stream, int32_t* code);
 
@@ -277,10 +292,16 @@ KDA_API kda_status kda_check_wait_timeout(int64_t limit_cycles, cudaStream_t str
  * provides every input and output.
  *  - A problem whose kda_chunk_fwd_workspace_size(...) exceeds
  *    KDA_NOALLOC_SCRATCH_BYTES is rejected with KDA_ERR_INVALID_ARG before
- *    anything is launched.
+ *    anything is launched.  The 64 MiB hold about 55,000 head-tokens on the
+ *    bf16 tensor-core path (d_k = d_v = 128: one sequence of ~1,700 tokens at
+ *    H = 32, ~57,000 at H = 1; each 64-token chunk of each head takes ~74 KB)
+ *    and about 27,000 on the fp32 path at d = 128 (~830 tokens at H = 32).
+ *    Larger problems need kda_chunk_fwd with a caller workspace.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (on the current device) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The cache assumes the device's
+ *    primary context for the life of the process: do not use this entry
+ *    point on a device after cudaDeviceReset.
  *  - Nothing is allocated or freed by the call.
  *  - All calls share the one array: calls whose work overlaps on the GPU
  *    (other streams, other host threads) race on it and must not overlap.

@@ -165,6 +165,11 @@ class PrefillWorkload:
     s0_std: Optional[float]          # None: no initial state (zeros)
     seq_lens: Optional[np.ndarray] = None
     extra: dict = field(default_factory=dict)
+    # A shard of a larger workload (see ``shard``): this workload's token 0 and
+    # sequence 0 are token ``tok_base`` and sequence ``seq_base`` of the
+    # generator streams, so its values are exactly that slice of the whole.
+    tok_base: int = 0
+    seq_base: int = 0
 
     @property
     def dcode(self) -> int:
@@ -196,6 +201,7 @@ class PrefillWorkload:
         [tok0, tok0 + ntok) of all heads (s0: all states) into ``out``."""
         ntok = self.tokens - tok0 if ntok is None else ntok
         H = self.H
+        tok0 = tok0 + self.tok_base
         if name == "q":
             return rows(self.seed, STREAM_Q, tok0 * H, 1, ntok * H, self.d_k, 1.0, True, self.dcode, out)
         if name == "k":
@@ -209,7 +215,8 @@ class PrefillWorkload:
         if name == "s0":
             assert self.s0_std is not None
             n = self.num_seqs * H * self.d_k
-            return rows(self.seed, STREAM_S0, 0, 1, n, self.d_v, self.s0_std, False, F32, out)
+            return rows(self.seed, STREAM_S0, self.seq_base * H * self.d_k, 1, n, self.d_v, self.s0_std, False, F32,
+                        out)
         raise KeyError(name)
 
     # ---- one (sequence, head) chain, for the oracle -----------------------
@@ -220,6 +227,7 @@ class PrefillWorkload:
         tok0, L = self.seq_bounds(s)
         n = L if ntok is None else min(ntok, L)
         H = self.H
+        tok0 += self.tok_base
         out = {
             "q": rows(self.seed, STREAM_Q, tok0 * H + h, H, n, self.d_k, 1.0, True, self.dcode),
             "k": rows(self.seed, STREAM_K, tok0 * H + h, H, n, self.d_k, 1.0, True, self.dcode),
@@ -229,9 +237,25 @@ class PrefillWorkload:
             "s0": None,
         }
         if self.s0_std is not None:
-            out["s0"] = rows(self.seed, STREAM_S0, (s * H + h) * self.d_k, 1, self.d_k, self.d_v, self.s0_std,
-                             False, F32)
+            out["s0"] = rows(self.seed, STREAM_S0, ((self.seq_base + s) * H + h) * self.d_k, 1, self.d_k, self.d_v,
+                             self.s0_std, False, F32)
         return out
+
+    def shard(self, first_seq: int, count: int, name: Optional[str] = None) -> "PrefillWorkload":
+        """Sequences [first_seq, first_seq + count) of this workload (all their
+        heads) as a workload of their own, with exactly the same values."""
+        assert 0 <= first_seq and count >= 0 and first_seq + count <= self.num_seqs
+        import dataclasses
+
+        tok0, _ = self.seq_bounds(first_seq) if count else (0, 0)
+        if self.seq_lens is None:
+            B, T, lens = count, self.T, None
+        else:
+            lens = np.asarray(self.seq_lens[first_seq: first_seq + count])
+            B, T = 1, int(lens.sum())
+        return dataclasses.replace(self, name=name or f"{self.name}[{first_seq}:{first_seq + count}]", B=B, T=T,
+                                   seq_lens=lens, tok_base=self.tok_base + tok0,
+                                   seq_base=self.seq_base + first_seq, extra=dict(self.extra))
 
 
 @dataclass

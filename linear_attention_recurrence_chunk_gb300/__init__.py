@@ -47,7 +47,7 @@ __all__ = ["kda_chunk_fwd", "kda_chunk_fwd_snapshots", "kda_chunk_fwd_gated", "k
 
 DECAY_BOUNDED, DECAY_SOFTPLUS = 0, 1   # kda_decay_map
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
-          4: "KDA_ERR_DEVICE_TIMEOUT"}
+          4: "KDA_ERR_DEVICE_TIMEOUT", 5: "KDA_ERR_NONFINITE"}
 _DT = {torch.float32: 0, torch.bfloat16: 1}
 SIZE_MAX = (1 << 64) - 1
 

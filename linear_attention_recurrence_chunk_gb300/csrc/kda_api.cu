@@ -88,6 +88,7 @@ const char* kda_status_string(kda_status s) {
     case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
     case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT";
+    case KDA_ERR_NONFINITE: return "KDA_ERR_NONFINITE";
   }
   return "KDA_ERR_UNKNOWN";
 }
@@ -356,6 +357,7 @@ kda_status kda_device_error(cudaStream_t stream, int32_t* code) {
   *code = h;
   if (h == 0) return KDA_OK;
   if (h == kda::kDevErrBadSeqlens) return KDA_ERR_INVALID_ARG;
+  if (h == kda::kDevErrNonFinite) return KDA_ERR_NONFINITE;
   return KDA_ERR_DEVICE_TIMEOUT;
 }
 

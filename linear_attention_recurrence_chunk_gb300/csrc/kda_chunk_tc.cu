@@ -1065,8 +1065,8 @@ struct ChainTcSmem {
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
   static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
   static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
-  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready
-  static constexpr uint32_t oTmem = oBar + 9 * 8;
+  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2]
+  static constexpr uint32_t oTmem = oBar + 11 * 8;
   static constexpr uint32_t kBytes = oTmem + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
@@ -1088,6 +1088,15 @@ __device__ __forceinline__ void store_bf16x16(bf16* dst, const float (&x)[16]) {
   for (int j = 0; j < 2; ++j)
     d[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
                       pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+}
+
+// Whole warp: records kDevErrNonFinite in the device error word (unless a code is
+// already there) when any lane's accumulated x * 0 checks are not 0, i.e. some
+// o or state value it wrote was inf or NaN (an fp16 operand of the chain out of
+// range, or non-finite inputs).
+__device__ __forceinline__ void report_nonfinite(float acc, int32_t* dev_err) {
+  if (__any_sync(0xffffffffu, !(acc == 0.f)) && (threadIdx.x & 31) == 0)
+    atomicCAS(dev_err, 0, (int32_t)kDevErrNonFinite);
 }
 
 // Inter-chunk pass of one (sequence, head, 32-column value block): the state
@@ -1115,6 +1124,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* drain = full + 6;
   uint64_t* vn_ready = full + 7;   // the 4 V_new warps have stored their rows
   uint64_t* s_ready = full + 8;    // the 8 consumer warps have stored the state and read TMEM
+  uint64_t* cons = full + 9;       // [2] the 8 consumer warps are done reading a stage (gam, u)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
@@ -1132,6 +1142,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     for (int i = 0; i < 7; ++i) tc::mbar_init(full + i, 1);
     tc::mbar_init(vn_ready, 4);                      // one arrival per V_new warp
     tc::mbar_init(s_ready, kChainConsumerWarps);     // one arrival per consumer warp
+    tc::mbar_init(cons, kChainConsumerWarps);        // one arrival per consumer warp and chunk
+    tc::mbar_init(cons + 1, kChainConsumerWarps);
     tc::fence_mbar_init();
   }
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
@@ -1160,7 +1172,11 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       int issued = 0;
       for (int i = 0; i < nch; ++i) {
         const int st = i & 1;
-        if (i >= 2 && !tc::mbar_wait(empty + st, ((i >> 1) - 1) & 1, kWaitLimit)) {
+        // a stage is refilled once the MMAs and every consumer warp are done with
+        // its previous chunk: a consumer can then never see this barrier two phases
+        // ahead of the chunk it waits for
+        if (i >= 2 && !(tc::mbar_wait(empty + st, ((i >> 1) - 1) & 1, kWaitLimit) &&
+                        tc::mbar_wait(cons + st, ((i >> 1) - 1) & 1, kWaitLimit))) {
           atomicExch(dev_err, (int32_t)kDevErrTimeout);
           break;
         }
@@ -1241,6 +1257,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(s_ready);
+    float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -1255,6 +1272,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
       if (q >= 2) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(cons + st);   // this warp reads nothing more of the stage
         // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer,
         // read while the state product is issued: its o product completed
         // before this chunk's group 1 (mma1)
@@ -1269,7 +1288,11 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
           const int r = c - 64;
           float ov[16];
           tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
-          if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+          if (r < prev_len) {
+            store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+          }
         }
       }
       if (q < 2) {   // V_new rows (tokens) 0-63: u - w S
@@ -1292,7 +1315,10 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(vn_ready);
+        if (lane == 0) {
+          tc::mbar_arrive(vn_ready);
+          tc::mbar_arrive(cons + st);   // u and gam of the stage have been read
+        }
       }
       bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
       if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
@@ -1327,11 +1353,20 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       const int r = c - 64;
       float ov[16];
       tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
-      if (r < prev_len) store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+      if (r < prev_len) {
+        store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+      }
     }
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
-    } else if (s_final) {
+    } else {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) nonfinite = fmaf(S[n], 0.f, nonfinite);
+      report_nonfinite(nonfinite, dev_err);
+    }
+    if (i == nch && !bad && s_final) {
       float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + n0 + 16 * hf;
 #pragma unroll
       for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
@@ -1366,8 +1401,8 @@ struct ChainWideSmem {
   static constexpr uint32_t kSAtom = DK * 64, kVAtom = C * 64;   // MN atom strides
   static constexpr uint32_t oS = 2 * kStage;                      // state block, DV/32 atoms
   static constexpr uint32_t oVN = oS + (DV / 32) * kSAtom;        // V_new, DV/32 atoms
-  static constexpr uint32_t oBar = oVN + (DV / 32) * kVAtom;      // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, rs[2]
-  static constexpr uint32_t oTmem = oBar + 11 * 8;
+  static constexpr uint32_t oBar = oVN + (DV / 32) * kVAtom;      // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, rs[2], cons[2]
+  static constexpr uint32_t oTmem = oBar + 13 * 8;
   static constexpr uint32_t oRss = oTmem + 16;                    // output epilogue: fp32 [2][DV/32][64] row sums of squares
   static constexpr uint32_t kBytes = oRss + 2 * (DV / 32) * 64 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -1404,6 +1439,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   uint64_t* vn_ready = full + 7;
   uint64_t* s_ready = full + 8;
   uint64_t* rs_full = full + 9;   // [2] output epilogue: row sums of squares of a chunk published
+  uint64_t* cons = full + 11;     // [2] every consumer warp is done reading a stage (gam, u)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
   float* rss = reinterpret_cast<float*>(sm + L::oRss);
   uint8_t* sS = sm + L::oS;
@@ -1424,6 +1460,8 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     tc::mbar_init(s_ready, L::kConsumerWarps);        // one arrival per consumer warp
     tc::mbar_init(rs_full, L::kConsumerWarps / 2);    // one arrival per o warp
     tc::mbar_init(rs_full + 1, L::kConsumerWarps / 2);
+    tc::mbar_init(cons, L::kConsumerWarps);
+    tc::mbar_init(cons + 1, L::kConsumerWarps);
     tc::fence_mbar_init();
   }
   for (int i = tid; i < 2 * 512; i += L::kThreads) {   // rows 0-63 of both [0; P] tiles stay zero
@@ -1450,7 +1488,11 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
       int issued = 0;
       for (int i = 0; i < nch; ++i) {
         const int st = i & 1;
-        if (i >= 2 && !tc::mbar_wait(empty + st, ((i >> 1) - 1) & 1, kWaitLimit)) {
+        // a stage is refilled once the MMAs and every consumer warp are done with
+        // its previous chunk: a consumer can then never see this barrier two phases
+        // ahead of the chunk it waits for
+        if (i >= 2 && !(tc::mbar_wait(empty + st, ((i >> 1) - 1) & 1, kWaitLimit) &&
+                        tc::mbar_wait(cons + st, ((i >> 1) - 1) & 1, kWaitLimit))) {
           atomicExch(dev_err, (int32_t)kDevErrTimeout);
           break;
         }
@@ -1517,6 +1559,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     // groups gives the RMS, then the weight and the Sigmoid gate scale the row
     // (loaded where used: at this kernel's register limit, holding them longer
     // spilled and measured slower).
+    float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
     auto emit_o = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
       const int r = c - 64;
       float sc = 1.f;
@@ -1562,6 +1605,8 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
             }
           }
           store_bf16x16(o + ((t0 + r) * H + h) * DV + col0, ov);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
         }
       }
       return true;
@@ -1593,14 +1638,9 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         break;
       }
       const float gam = reinterpret_cast<const float*>(stg + L::oGam)[c];
-      if constexpr (kGated) {   // the previous chunk's o rows, before this chunk's products are seen
-        if (i > 0 && q >= 2) {
-          bad |= !emit_o((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
-          if (__any_sync(0xffffffffu, bad)) {
-            bad = true;
-            break;
-          }
-        }
+      if (q >= 2) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(cons + st);   // this warp reads nothing more of the stage
       }
       bad |= !tc::mbar_wait(mma1, i & 1, kWaitLimit);
       if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
@@ -1627,7 +1667,10 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(vn_ready);
+        if (lane == 0) {
+          tc::mbar_arrive(vn_ready);
+          tc::mbar_arrive(cons + st);   // u and gam of the stage have been read
+        }
       }
       bad |= !tc::mbar_wait(mma2, i & 1, kWaitLimit);
       if (__any_sync(0xffffffffu, bad)) {   // warp-uniform, so that no lane is left at a __syncwarp
@@ -1654,12 +1697,13 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
 #pragma unroll
         for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
       }
-      // Without the epilogue the previous chunk's o rows are emitted after the
-      // state hand-off (off the chain's critical path): their buffer, (i - 1) % 3,
-      // is next written by the first group of chunk i + 2, issued only after this
-      // warp's next hand-off.  (With the epilogue, whose row exchange among the
-      // o warps timed out there for d_v = 128, they are emitted at the step start.)
-      if (!kGated && i > 0 && q >= 2) {
+      // The previous chunk's o rows are emitted after the state hand-off (off the
+      // chain's critical path): their buffer, (i - 1) % 3, is next written by the
+      // first group of chunk i + 2, issued only after this warp's next hand-off.
+      // Meanwhile the MMAs and the TMA producer may run a chunk ahead; the stage
+      // release barrier (cons) keeps the producer from refilling the stage this
+      // warp reads next before the warp has waited for it.
+      if (i > 0 && q >= 2) {
         bad |= !emit_o((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
         if (__any_sync(0xffffffffu, bad)) {
           bad = true;
@@ -1674,7 +1718,12 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     }
     if (i < nch || bad) {
       atomicExch(dev_err, (int32_t)kDevErrTimeout);
-    } else if (s_final) {
+    } else {
+#pragma unroll
+      for (int n = 0; n < 32; ++n) nonfinite = fmaf(S[n], 0.f, nonfinite);
+      report_nonfinite(nonfinite, dev_err);
+    }
+    if (i == nch && !bad && s_final) {
       float* dst = s_final + (((int64_t)s * H + h) * DK + c) * DV + n0 + 32 * cg;
 #pragma unroll
       for (int n = 0; n < 32; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);

@@ -16,6 +16,7 @@ enum DeviceError : int32_t {
   kDevErrNone = 0,
   kDevErrBadSeqlens = 1,   // cu_seqlens not starting at 0, decreasing, or not ending at T
   kDevErrTimeout = 2,      // a bounded wait on an mbarrier ran out
+  kDevErrNonFinite = 3,    // an output or final-state value came out inf or NaN (fp16 chain range exceeded)
 };
 
 // Chunk length of the prefill (tokens per chunk) and the sub-tile length whose

@@ -12,7 +12,11 @@
 // this library holds KDA_NOALLOC_SCRATCH_BYTES of it until the process exits.
 // In host code its name is only a stand-in for the symbol, not a device
 // address, so the address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and then cached.
+// cudaGetSymbolAddress (with that device current) and then cached.  The cache
+// assumes the device's primary context for the life of the process: after a
+// cudaDeviceReset the module is loaded again and the cached address would be
+// stale, so a caller that resets a device must not use this entry point on it
+// afterwards.
 //
 // Nothing in the array has to start at zero: every byte that a call reads was
 // written earlier in that same call (chunk map, then per-chunk records), so
@@ -60,10 +64,9 @@ kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  int64_t T, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dt, void* o,
                                  float* final_state, cudaStream_t stream) {
   const size_t need = kda_chunk_fwd_workspace_size(B, T, H, d_k, d_v, num_seqs, dt);
-  if (need == SIZE_MAX) {
-    const bool dims_ok = (d_k == 64 || d_k == 128) && (d_v == 64 || d_v == 128);
-    return dims_ok ? KDA_ERR_INVALID_ARG : KDA_ERR_UNSUPPORTED;
-  }
+  if (need == SIZE_MAX)   // invalid or unsupported shape: kda_chunk_fwd's own status, in its own order
+    return kda_chunk_fwd(q, k, v, g, beta, initial_state, cu_seqlens, num_seqs, B, T, H, d_k, d_v, dt, o,
+                         final_state, nullptr, 0, stream);
   if (need > kScratchBytes) return KDA_ERR_INVALID_ARG;   // problem too large for the fixed scratch array
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;

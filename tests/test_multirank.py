@@ -2,7 +2,9 @@
 would start them, rendezvous on 127.0.0.1) go through the same process-group
 setup, barrier, max/min-over-ranks timing and weak-scaling aggregation that
 bench.py uses with NCCL on GPUs, and the reference arm does no work on ranks
-other than 0."""
+other than 0.  The job is sharded by sequence: every (sequence, head) unit of
+the whole job is computed by exactly one rank, on exactly the values the
+whole job's generator gives it."""
 import json
 import os
 import socket
@@ -22,7 +24,8 @@ assert dist.is_initialized() and dist.get_backend() == "gloo"
 bench.barrier(ws)
 elapsed = [12.5, 20.0][rank]           # each rank's own timed region, ms
 tput = [4.0e6, 3.0e6][rank]            # each rank's own end-to-end throughput
-res = {"rank": rank, "ws": ws,
+wr = bench.rank_workload(bench.get_workload(bench.WORKLOAD), rank, ws)
+res = {"rank": rank, "ws": ws, "seq_base": wr.seq_base, "num_seqs": wr.num_seqs, "tok_base": wr.tok_base,
        "max_ms": bench.max_over_ranks(elapsed, ws),
        "min_tput": bench.min_over_ranks(tput, ws),
        "value": bench.job_throughput(1000.0, 3, bench.max_over_ranks(elapsed, ws), ws)}
@@ -61,8 +64,43 @@ def test_two_gloo_ranks_time_and_aggregate_like_the_benchmark():
         lines = [ln for ln in out.splitlines() if ln.startswith("RESULT ")]
         assert len(lines) == 1 and out.strip() == lines[0], out   # nothing else printed (no reference line)
         outs.append(json.loads(lines[0][len("RESULT "):]))
+    assert sorted((r["seq_base"], r["num_seqs"]) for r in outs) == [(0, 1), (1, 1)]   # one sequence each
+    assert sorted(r["tok_base"] for r in outs) == [0, 65536]
     for r in outs:
         assert r["ws"] == 2
         assert r["max_ms"] == 20.0                      # the job takes as long as its slowest rank
         assert r["min_tput"] == 3.0e6                   # end-to-end: the slowest rank, times the ranks
         assert abs(r["value"] - 2 * 1000.0 * 3 / 0.020) < 1e-6
+
+
+def test_shards_cover_every_sequence_and_head_once():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import kda_synth as ks
+
+    for name in ("prefill_b1_h32_t65536_d128", "prefill_b8_h96_t8192_d128", "varlen_12seq_1m_h32_d128"):
+        w = ks.workloads()[name]
+        for ws in (1, 2, 3, 4, 8):
+            wg = bench.global_workload(w, ws)
+            assert wg.num_seqs == w.num_seqs * ws and wg.tokens == w.tokens * ws
+            seen = {}
+            for rank in range(ws):
+                wr = bench.rank_workload(w, rank, ws)
+                assert wr.num_seqs == w.num_seqs and wr.tokens == w.tokens   # weak scaling: same work per rank
+                for s in range(wr.num_seqs):
+                    for h in range(wr.H):
+                        key = (wr.seq_base + s, h)
+                        assert key not in seen, (name, ws, key)
+                        seen[key] = rank
+            assert set(seen) == {(s, h) for s in range(wg.num_seqs) for h in range(wg.H)}
+            # a rank's values are the whole job's values of its sequences
+            wr = bench.rank_workload(w, ws - 1, ws)
+            s_loc = wr.num_seqs - 1
+            a = wr.chain_inputs(s_loc, wr.H - 1, ntok=64)
+            b = wg.chain_inputs(wr.seq_base + s_loc, wr.H - 1, ntok=64)
+            for k in ("q", "k", "v", "g", "beta"):
+                assert np.array_equal(a[k], b[k]), (name, ws, k)
+            if w.s0_std is not None:
+                assert np.array_equal(a["s0"], b["s0"])

@@ -26,13 +26,13 @@ def _run_prefill(w, t, **kw):
     return o, sf
 
 
-def _check_all_chains(w, o, sf, pairs=None, ntok=None):
+def _check_all_chains(w, o, sf, pairs=None, ntok=None, record=None):
     pairs = pairs or [(s, h) for s in range(w.num_seqs) for h in range(w.H)]
     o_ref, s_ref = oracle_chains(w, pairs, ntok)
-    assert_o_close(gpu_chain_outputs(w, o, pairs, ntok), o_ref, w.dtype)
+    assert_o_close(gpu_chain_outputs(w, o, pairs, ntok), o_ref, w.dtype, record=record)
     if ntok is None and sf is not None:
         s_gpu = np.stack([sf[s, h].cpu().numpy() for s, h in pairs])
-        assert_state_close(s_gpu, s_ref)
+        assert_state_close(s_gpu, s_ref, record=record)
 
 
 # --------------------------------------------------------------------- prefill
@@ -84,7 +84,7 @@ def test_fp32_b1_h2_t256_d64_workload():
     w = ks.workloads()["fp32_b1_h2_t256_d64"]
     t = prefill_device_inputs(w, DEV)
     o, sf = _run_prefill(w, t)
-    _check_all_chains(w, o, sf)
+    _check_all_chains(w, o, sf, record="fp32_b1_h2_t256_d64 (all chains)")
 
 
 @pytest.mark.parametrize("lens", [[0, 1, 63, 64, 65, 200, 0, 17], [128], [5, 0, 0, 300]])
@@ -106,29 +106,37 @@ def test_prefill_h32_t65536_full_size_sampled():
     w = ks.workloads()["prefill_b1_h32_t65536_d128"]
     t = prefill_device_inputs(w, DEV)
     o, sf = _run_prefill(w, t)
-    _check_all_chains(w, o, sf, pairs=[(0, 0), (0, 7), (0, 19), (0, 31)])
+    _check_all_chains(w, o, sf, pairs=[(0, 0), (0, 7), (0, 19), (0, 31)],
+                      record="prefill_b1_h32_t65536_d128 (4 heads)")
 
 
 def test_prefill_b8_h96_t8192_full_size_sampled():
-    """Full-size B=8, H=96, T=8192 bf16, no initial state: sampled chains."""
+    """Full-size B=8, H=96, T=8192 bf16, no initial state: 32 chains, four on
+    each of the eight sequences, every output and final state."""
     w = ks.workloads()["prefill_b8_h96_t8192_d128"]
     t = prefill_device_inputs(w, DEV)
     o, sf = _run_prefill(w, t)
-    _check_all_chains(w, o, sf, pairs=[(0, 0), (3, 50), (7, 95), (5, 1), (2, 77), (6, 33), (1, 12), (4, 64)])
+    rng = np.random.default_rng(2)
+    pairs = [(s, int(h)) for s in range(w.num_seqs) for h in rng.choice(w.H, 4, replace=False)]
+    _check_all_chains(w, o, sf, pairs=pairs, record="prefill_b8_h96_t8192_d128 (32 chains)")
 
 
 def test_varlen_1m_full_size_sampled():
     """Full-size packed varlen (12 sequences, 1,048,576 tokens, H=32): the
-    three shortest sequences in full on every head, and the first 4096 tokens
-    of the longest sequence on two heads."""
+    three shortest sequences in full on every fourth head, and the longest
+    sequence (the deepest chain, thousands of chunks) in full on two heads,
+    every output row and its final state."""
     w = ks.workloads()["varlen_12seq_1m_h32_d128"]
     t = prefill_device_inputs(w, DEV)
     o, sf = _run_prefill(w, t)
     order = np.argsort(w.seq_lens)
     short = [int(s) for s in order[:3]]
-    _check_all_chains(w, o, sf, pairs=[(s, h) for s in short for h in range(0, w.H, 4)])
+    _check_all_chains(w, o, sf, pairs=[(s, h) for s in short for h in range(0, w.H, 4)],
+                      record="varlen_12seq_1m_h32_d128 (3 shortest seqs)")
     longest = int(order[-1])
-    _check_all_chains(w, o, None, pairs=[(longest, 3), (longest, 30)], ntok=4096)
+    assert w.seq_lens[longest] > 200_000
+    _check_all_chains(w, o, sf, pairs=[(longest, 3), (longest, 30)],
+                      record="varlen_12seq_1m_h32_d128 (longest seq, 2 heads)")
 
 
 # ---------------------------------------------------------- prefill invariants
@@ -277,9 +285,10 @@ def test_decode_n256_h96_100_steps_sampled():
         outs, ref, _ = oracle.chains(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], oracle.BF16, 128, 128, 1,
                                      list(range(len(sample))), [1] * len(sample), ref)
         got = o.reshape(heads, 128)[torch.from_numpy(sample).to(DEV)].float().cpu().numpy()
-        assert_o_close([got], [np.concatenate(outs)], "bf16", what=f"o at step {step}")
+        assert_o_close([got], [np.concatenate(outs)], "bf16", what=f"o at step {step}",
+                       record="decode_n256_h96_d128_x100 (384 heads)")
     s_gpu = state.reshape(heads, 128, 128)[torch.from_numpy(sample).to(DEV)].cpu().numpy()
-    assert_state_close(s_gpu, ref)
+    assert_state_close(s_gpu, ref, record="decode_n256_h96_d128_x100 (384 heads)")
 
 
 def test_decode_steps_equal_prefill():
