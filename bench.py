@@ -61,6 +61,8 @@ def parse_args():
                     help="skip the decay-map ablation (diagonal tiles by position pairs, bounded and -Softplus maps)")
     ap.add_argument("--snapshot-interval", type=int, default=512)
     ap.add_argument("--decode-steps", type=int, default=100)
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run only the decode legs (a short command for profiler captures of the decode kernels)")
     ap.add_argument("--workload", choices=[WORKLOAD, PROFILE_WORKLOAD, "prefill_b8_h96_t8192_d128",
                                            "varlen_12seq_1m_h32_d128"], default=WORKLOAD,
                     help="the headline workload (default), a T=8192 cut of it for profiler captures, "
@@ -462,7 +464,7 @@ def bench_gated(args, r, steps):
     del gate, nw
     return {"value": w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
             "spread": spread, "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
-            "note": "fused into the chain where its CTAs hold all d_v columns of a head, else a pass of its own over o"}
+            "note": "fused into the chain: the 32-column CTAs of a head exchange row sums within their cluster"}
 
 
 def bench_decay_ablation(args, r, steps):
@@ -743,6 +745,12 @@ def main():
 
     ws_size, rank, local = dist_setup(args)
     peak, peak_kind = peaks()
+    if args.decode_only:
+        dec = bench_decode(args, peak)
+        if rank == 0:
+            print(json.dumps({"metric": "KDA decode GB/s (256 sequences x 96 heads, d=128)", "value": dec["GB/s"],
+                              "unit": "GB/s", "n_gpus": ws_size, "decode": dec}), flush=True)
+        return
     r = bench_prefill(args, ws_size, local)
     w = r["w"]
     steps = args.steps

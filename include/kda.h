@@ -172,8 +172,11 @@ KDA_API kda_status kda_chunk_fwd_snapshots(const void* q, const void* k, const v
  *  eps_rms      >= 0.
  * Supported on the bf16 path with d_k = 128 (d_v = 64 or 128); other head sizes
  * or fp32 inputs return KDA_ERR_UNSUPPORTED.  The RMS needs a token's whole
- * row: where the inter-chunk pass holds all d_v columns of a head per CTA (many
- * heads) the epilogue is applied there, else by a pass of its own over o.
+ * row, and the epilogue is always applied inside the inter-chunk pass before
+ * o is written: where that pass holds all d_v columns of a head per CTA (many
+ * heads) directly, else (few heads: 32 columns per CTA) the CTAs of a head run
+ * as one thread-block cluster and exchange each row's partial sums of squares
+ * through distributed shared memory.
  */
 KDA_API kda_status kda_chunk_fwd_gated(const void* q, const void* k, const void* v, const void* g,
                                        const float* beta, const float* initial_state, const int32_t* cu_seqlens,

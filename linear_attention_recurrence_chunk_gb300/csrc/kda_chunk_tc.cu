@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   // accumulator (columns 0-255, rows 0-63 in lanes 0-63)
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdescWU = tc::idesc_f16_f32(128, L::kWuN) | (1u << 16);   // B (KV) MN-major
-  constexpr int kWuIssuer = 64;
+  constexpr int kWuIssuer = 2;   // warp that issues [w | u]
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sRow = smem + L::oRow;   // row operand of the A / P products
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     //      D2 = [q e^G high ; low]   (M = 128) x (own sub-tile, high part)^T (N = 64)
     //    A_ri = beta_r D1[r][..] (rows 0-63); P_ri = D1[64 + r][..], plus, on the
     //    diagonal blocks, the low-part products D1[64 + r][64 + i] + D2[64 + r][i].
-    if (tid == 0) {
+    if (tid == 0) {   // one thread issues (a whole-warp issue measured 3 % slower here)
       const uint64_t dR = tc::desc_kmajor_sw128(tc::smem_u32(sRow));
       // the pair path multiplies by the later sub-tiles' rows only (128-223: N = 96)
       const uint64_t dC = tc::desc_kmajor_sw128(tc::smem_u32(sCol + (kPairs ? 2 * C * 128 : 0)));
@@ -604,19 +604,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
       for (int kk = 0; kk < DK / 16; ++kk) {
         const uint64_t oR = (((kk >> 2) * L::kRowAtom) + (kk & 3) * 32) >> 4;
         const uint64_t oC = (((kk >> 2) * L::kColAtom) + (kk & 3) * 32) >> 4;
-        if (kk == 0)
-          tc::mma_16bit_first(tmem, dR + oR, dC + oC, kId1);
-        else
-          tc::mma_16bit_acc(tmem, dR + oR, dC + oC, kId1);
+        tc::mma_16bit(tmem, dR + oR, dC + oC, kId1, kk > 0);
       }
 #pragma unroll
       for (int kk = 0; kk < (kPairs ? 0 : DK / 16); ++kk) {
         const uint64_t oR = (((kk >> 2) * L::kRowAtom) + C * 128 + (kk & 3) * 32) >> 4;
         const uint64_t oC = (((kk >> 2) * L::kColAtom) + (kk & 3) * 32) >> 4;
-        if (kk == 0)
-          tc::mma_16bit_first(tmem + L::kColRows, dR + oR, dC + oC, kId2);
-        else
-          tc::mma_16bit_acc(tmem + L::kColRows, dR + oR, dC + oC, kId2);
+        tc::mma_16bit(tmem + L::kColRows, dR + oR, dC + oC, kId2, kk > 0);
       }
       tc::mma_commit(bar + 2);
     }
@@ -1015,21 +1009,19 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (tid == kWuIssuer) {   // lane 0 of warp 2, which has no part in the next drain: it catches up there
+    if (tid == 32 * kWuIssuer) {   // lane 0 of warp 2, which has no part in the next drain: it catches up there
       const uint64_t dX = tc::desc_kmajor_sw128(tc::smem_u32(sX));
       const uint64_t dKV = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sKV), 8192);
-      tc::mma_16bit_first(tmem, dX, dKV, kIdescWU);
 #pragma unroll
-      for (int kk = 1; kk < C / 16; ++kk)
-        tc::mma_16bit_acc(tmem, dX + ((kk * 32) >> 4), dKV + ((kk * 2048) >> 4), kIdescWU);
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit(tmem, dX + ((kk * 32) >> 4), dKV + ((kk * 2048) >> 4), kIdescWU, kk > 0);
       tc::mma_commit(bar + 1);
     }
     wu_pending = true;
     wu_rec = rec;
     // No barrier here: until the next task's first one the threads write only
     // sBeta, whose last readers (the A / P epilogue, the operand of [w | u])
-    // finished before the barrier above; the issuing thread, held while the
-    // tensor pipe takes the [w | u] products, joins there (a barrier here cost 7 %).
+    // finished before the barrier above (a barrier here cost 7 %).
   }
   wu_drain(false);   // the last task's [w | u]
   if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
@@ -1051,8 +1043,7 @@ constexpr int kChainTcThreads = 32 * (kChainConsumerWarps + 2);
 // M = 128, N = 32.
 constexpr uint32_t kIdescMN = tc::idesc_f16_f32(128, BV) | (1u << 16);
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kTmemD12 = 0;    // two buffers of 32 columns (chunk parity)
-constexpr uint32_t kTmemD3 = 64;
+constexpr uint32_t kTmemD12 = 0;    // D12 buffers of 32 columns: two (chunk parity), three with the output epilogue
 
 struct ChainTcSmem {
   // one pipeline stage (all tiles 1024-byte aligned, 128-byte swizzle unless noted)
@@ -1065,9 +1056,12 @@ struct ChainTcSmem {
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
   static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
   static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
-  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2]
-  static constexpr uint32_t oTmem = oBar + 11 * 8;
-  static constexpr uint32_t kBytes = oTmem + 16;
+  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2], rs[2]
+  static constexpr uint32_t oTmem = oBar + 13 * 8;
+  // output epilogue: per chunk parity, the row sums of squares of o of every
+  // (cluster rank, 16-column half) of the head, fp32 [2][8][64]
+  static constexpr uint32_t oRss = oTmem + 16;
+  static constexpr uint32_t kBytes = oRss + 2 * 8 * 64 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
 
@@ -1106,15 +1100,28 @@ __device__ __forceinline__ void report_nonfinite(float acc, int32_t* dev_err) {
 //   V_new  = u - (w S)                                 (consumers, to SMEM)
 //   group 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
 //   S      = e^{G_last} S + D3                          (consumers)
-template <int DV>
+// With kGated, the output epilogue (Sigmoid gate times the per-head RMSNorm of
+// o) is applied before o is written.  A token's d_v outputs are spread over the
+// DV/32 CTAs of its head, which the launch groups into one thread-block cluster:
+// every o thread sends its row's partial sum of squares to each CTA of the
+// cluster (distributed shared memory, an mbarrier per chunk parity with
+// cluster-scope release / acquire), then scales its row by the total.  The o
+// rows of a chunk are then emitted after the next state hand-off, off the
+// chain's critical path, so D12 has three buffers (chunk i in buffer i % 3,
+// next written by group 1 of chunk i + 3).
+template <int DV, bool kGated>
 __global__ void __launch_bounds__(kChainTcThreads, 1)
     chunk_chain_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
                    const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu, int32_t num_seqs,
                    int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0, float* __restrict__ s_final,
-                   bf16* __restrict__ o, int32_t* dev_err) {
+                   bf16* __restrict__ o, OutEpilogue ep, int32_t* dev_err) {
   using L = ChainTcSmem;
-  if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
+  constexpr int kRanks = DV / BV;                    // CTAs (column blocks) per head: the cluster with kGated
+  constexpr uint32_t kNBuf = kGated ? 3 : 2;         // D12 buffers
+  constexpr uint32_t kTmemD3 = kTmemD12 + kNBuf * BV;
+  static_assert(kTmemD3 + BV <= kTmemCols, "TMEM columns");
+  if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing (every CTA of a cluster alike)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::oBar);
@@ -1125,7 +1132,9 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* vn_ready = full + 7;   // the 4 V_new warps have stored their rows
   uint64_t* s_ready = full + 8;    // the 8 consumer warps have stored the state and read TMEM
   uint64_t* cons = full + 9;       // [2] the 8 consumer warps are done reading a stage (gam, u)
+  uint64_t* rs_full = full + 11;   // [2] output epilogue: every o warp of the cluster has sent its row sums
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
+  float* rss = reinterpret_cast<float*>(sm + L::oRss);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
@@ -1144,6 +1153,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     tc::mbar_init(s_ready, kChainConsumerWarps);     // one arrival per consumer warp
     tc::mbar_init(cons, kChainConsumerWarps);        // one arrival per consumer warp and chunk
     tc::mbar_init(cons + 1, kChainConsumerWarps);
+    tc::mbar_init(rs_full, 4 * kRanks);              // one arrival per o warp of the cluster
+    tc::mbar_init(rs_full + 1, 4 * kRanks);
     tc::fence_mbar_init();
   }
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
@@ -1159,6 +1170,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // the cluster's barriers are initialised before any CTA of it sends row sums
+  if constexpr (kGated) tc::cluster_sync_all();
   const uint32_t tmem = *tslot;
 
   if (warp == kChainTmaWarp) {
@@ -1195,48 +1208,49 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) tc::mbar_wait(full + (i & 1), (i >> 1) & 1, kWaitLimit);
     }
   } else if (warp == kChainMmaWarp) {
-    // ---------------- MMA issue (one thread).  Descriptors: the B tiles never
-    // move; A tiles differ per stage only by the stage offset, K slices by
-    // constant offsets added to the start-address field.
-    if (lane == 0) {
-      const uint64_t dS0 = tc::desc_mnmajor_sw64(tc::smem_u32(sS));
-      const uint64_t dV0 = tc::desc_mnmajor_sw64(tc::smem_u32(sVN));
-      const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));   // stage 0 base
-      bool ok = true, issued = false;
-      for (int i = 0; i < nch && ok; ++i) {
-        const int st = i & 1;
-        ok = tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit) && tc::mbar_wait(s_ready, i & 1, kWaitLimit);
-        if (!ok) break;
-        tc::tc_fence_after();
-        const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
-        const uint32_t d12 = tmem + kTmemD12 + (uint32_t)st * 32;
-        tc::mma_16bit_first(d12, dA, dS0, kIdescMN);   // group 1
+    // ---------------- MMA issue: the whole warp runs this loop with warp-uniform
+    // operands and one elected lane issues (fast back-to-back issue).
+    // Descriptors: the B tiles never move; A tiles differ per stage only by the
+    // stage offset, K slices by constant offsets added to the start-address field.
+    const uint64_t dS0 = tc::desc_mnmajor_sw64(tc::smem_u32(sS));
+    const uint64_t dV0 = tc::desc_mnmajor_sw64(tc::smem_u32(sVN));
+    const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));   // stage 0 base
+    auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, tc::mbar_wait(b, parity, kWaitLimit));
+    };
+    bool ok = true, issued = false;
+    for (int i = 0; i < nch && ok; ++i) {
+      const int st = i & 1;
+      ok = wait_all(full + st, (i >> 1) & 1) && wait_all(s_ready, i & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
+      const uint32_t d12 = tmem + kTmemD12 + (uint32_t)(i % (int)kNBuf) * BV;
 #pragma unroll
-        for (int kk = 1; kk < DK / 16; ++kk)
-          tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN);
-        tc::mma_commit(mma1);
-        issued = true;
-        ok = tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
-        if (!ok) break;
-        tc::tc_fence_after();
-        // group 2: the state product first, committed on its own, then the o rows;
-        // the o rows are read once group 1 of the next chunk (issued after
-        // them) has completed, or after the final drain
-        tc::mma_16bit_first(tmem + kTmemD3, dA + (L::oKT >> 4), dV0, kIdescMN);
+      for (int kk = 0; kk < DK / 16; ++kk)   // group 1
+        tc::mma_16bit_w(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdescMN,
+                        kk > 0);
+      tc::mma_commit_w(mma1);
+      issued = true;
+      ok = wait_all(vn_ready, i & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      // group 2: the state product first, committed on its own, then the o rows;
+      // the o rows are read once group 1 of the next chunk (issued after
+      // them) has completed, or after the final drain
 #pragma unroll
-        for (int kk = 1; kk < C / 16; ++kk)
-          tc::mma_16bit_acc(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
-        tc::mma_commit(mma2);
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit_w(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, kk > 0);
+      tc::mma_commit_w(mma2);
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)
-          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN);
-        tc::mma_commit(empty + st);
-      }
-      if (!ok) atomicExch(dev_err, (int32_t)kDevErrTimeout);
-      if (issued) {   // no MMA may still be writing TMEM when it is freed
-        tc::mma_commit(drain);
-        tc::mbar_wait(drain, 0, kWaitLimit);
-      }
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit_w(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, 1u);
+      tc::mma_commit_w(empty + st);
+    }
+    if (!ok && lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    if (issued) {   // no MMA may still be writing TMEM when it is freed
+      tc::mma_commit_w(drain);
+      wait_all(drain, 0);
     }
   } else {
     // ---------------- consumers: TMEM lane quarter q, value columns 16 hf .. 16 hf + 15
@@ -1258,6 +1272,56 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(s_ready);
     float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
+    // Output epilogue (kGated, o warps q >= 2, row r = token of the chunk):
+    // this thread's 16 norm weights, and the gate logits of the chunk it emits
+    // next, loaded a chunk ahead.
+    const int r = c - 64;
+    float wgt[16];
+    uint4 gcur[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if constexpr (kGated) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) wgt[e] = (q >= 2 && ep.weight) ? ep.weight[(int64_t)h * DV + n0 + 16 * hf + e] : 1.f;
+    }
+    const uint32_t crank = kGated ? tc::cluster_ctarank() : 0u;
+    auto load_gate = [&](int64_t t0, int64_t len) {
+      if (r < len) {
+        const uint4* gp = reinterpret_cast<const uint4*>(ep.gate + ((t0 + r) * H + h) * DV + n0 + 16 * hf);
+        gcur[0] = gp[0];
+        gcur[1] = gp[1];
+      }
+    };
+    // o rows of chunk j from D12 buffer `buf`: row sums of squares to every CTA
+    // of the cluster, the total from all of them, then the scaled row.
+    auto emit_gated = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
+      float ov[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + buf * BV + 16 * hf), ov);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ss = fmaf(ov[e], ov[e], ss);
+      const int par = j & 1;
+      float* slot = rss + (par * 8 + (int)crank * 2 + hf) * 64 + r;
+#pragma unroll
+      for (uint32_t d = 0; d < (uint32_t)kRanks; ++d) tc::st_shared_cluster_f32(tc::mapa_shared(slot, d), ss);
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (uint32_t d = 0; d < (uint32_t)kRanks; ++d) tc::mbar_arrive_cluster(tc::mapa_shared(rs_full + par, d));
+      }
+      if (!tc::mbar_wait_cluster(rs_full + par, (uint32_t)(j >> 1) & 1u, kWaitLimit)) return false;
+      float tot = 0.f;
+#pragma unroll
+      for (int k2 = 0; k2 < 2 * kRanks; ++k2) tot += rss[(par * 8 + k2) * 64 + r];
+      const float sc = rsqrtf(tot * (1.f / DV) + ep.eps);
+      if (r < len) {
+        const bf16* gv = reinterpret_cast<const bf16*>(gcur);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ov[e] *= sc * wgt[e] / (1.f + __expf(-__bfloat162float(gv[e])));
+        store_bf16x16(o + ((t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+      }
+      return true;
+    };
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -1274,6 +1338,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       if (q >= 2) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(cons + st);   // this warp reads nothing more of the stage
+      }
+      if (!kGated && q >= 2) {
         // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer,
         // read while the state product is issued: its o product completed
         // before this chunk's group 1 (mma1)
@@ -1303,7 +1369,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         }
         tc::tc_fence_after();
         float d[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)st * 32 + 16 * hf), d);
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(i % (int)kNBuf) * BV + 16 * hf), d);
 #pragma unroll
         for (int q4 = 0; q4 < 2; ++q4) {
           const uint4 raw = *reinterpret_cast<const uint4*>(stg + L::oU + tc::sw64_chunk_offset(c, 2 * hf + q4));
@@ -1342,6 +1408,22 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 #pragma unroll
         for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
       }
+      if constexpr (kGated) {
+        // the previous chunk's o rows, after this warp's state hand-off (their
+        // product completed before this chunk's group 1, whose completion this
+        // warp has seen through mma2); then the gate logits of this chunk
+        if (q >= 2) {
+          if (i > 0) {
+            bad |= !emit_gated((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
+            if (__any_sync(0xffffffffu, bad)) {
+              bad = true;
+              break;
+            }
+          }
+          const int64_t t0 = seq_start + (int64_t)i * C;
+          load_gate(t0, min((int64_t)C, seq_end - t0));
+        }
+      }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
@@ -1349,8 +1431,9 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       bad = __any_sync(0xffffffffu, !tc::mbar_wait(drain, 0, kWaitLimit));
       tc::tc_fence_after();
     }
-    if (i == nch && !bad && nch > 0 && q >= 2) {
-      const int r = c - 64;
+    if (kGated && i == nch && !bad && nch > 0 && q >= 2)
+      bad = __any_sync(0xffffffffu, !emit_gated((uint32_t)((nch - 1) % 3), prev_t0, prev_len, nch - 1));
+    if (!kGated && i == nch && !bad && nch > 0 && q >= 2) {
       float ov[16];
       tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
       if (r < prev_len) {
@@ -1375,6 +1458,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  // no CTA of the cluster leaves while another may still send it row sums
+  if constexpr (kGated) tc::cluster_sync_all();
 }
 
 // ------------------------------------------------------- wide chain kernel
@@ -1512,42 +1597,43 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
       for (int i = (issued > 2 ? issued - 2 : 0); i < issued; ++i) tc::mbar_wait(full + (i & 1), (i >> 1) & 1, kWaitLimit);
     }
   } else if (warp == L::kMmaWarp) {
-    if (lane == 0) {
-      const uint64_t dS0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sS), L::kSAtom);
-      const uint64_t dV0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sVN), L::kVAtom);
-      const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));
-      bool ok = true, issued = false;
-      for (int i = 0; i < nch && ok; ++i) {
-        const int st = i & 1;
-        ok = tc::mbar_wait(full + st, (i >> 1) & 1, kWaitLimit) && tc::mbar_wait(s_ready, i & 1, kWaitLimit);
-        if (!ok) break;
-        tc::tc_fence_after();
-        const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
-        const uint32_t d12 = tmem + (uint32_t)(i % 3) * NC;
-        tc::mma_16bit_first(d12, dA, dS0, kIdesc);   // group 1
+    // the whole warp runs the issue loop (warp-uniform operands, one elected lane issues)
+    const uint64_t dS0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sS), L::kSAtom);
+    const uint64_t dV0 = tc::desc_mnmajor_sw64_atoms(tc::smem_u32(sVN), L::kVAtom);
+    const uint64_t dA0 = tc::desc_kmajor_sw128(tc::smem_u32(sm));
+    auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, tc::mbar_wait(b, parity, kWaitLimit));
+    };
+    bool ok = true, issued = false;
+    for (int i = 0; i < nch && ok; ++i) {
+      const int st = i & 1;
+      ok = wait_all(full + st, (i >> 1) & 1) && wait_all(s_ready, i & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
+      const uint32_t d12 = tmem + (uint32_t)(i % 3) * NC;
 #pragma unroll
-        for (int kk = 1; kk < DK / 16; ++kk)
-          tc::mma_16bit_acc(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdesc);
-        tc::mma_commit(mma1);
-        issued = true;
-        ok = tc::mbar_wait(vn_ready, i & 1, kWaitLimit);
-        if (!ok) break;
-        tc::tc_fence_after();
+      for (int kk = 0; kk < DK / 16; ++kk)   // group 1
+        tc::mma_16bit_w(d12, dA + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), dS0 + ((kk * 1024) >> 4), kIdesc,
+                        kk > 0);
+      tc::mma_commit_w(mma1);
+      issued = true;
+      ok = wait_all(vn_ready, i & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < C / 16; ++kk)   // group 2
-          tc::mma_16bit_acc(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc);
-        tc::mma_16bit_first(tmem + kD3, dA + (L::oKT >> 4), dV0, kIdesc);
+      for (int kk = 0; kk < C / 16; ++kk)   // group 2
+        tc::mma_16bit_w(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc, 1u);
 #pragma unroll
-        for (int kk = 1; kk < C / 16; ++kk)
-          tc::mma_16bit_acc(tmem + kD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc);
-        tc::mma_commit(mma2);
-        tc::mma_commit(empty + st);
-      }
-      if (!ok) atomicExch(dev_err, (int32_t)kDevErrTimeout);
-      if (issued) {
-        tc::mma_commit(drain);
-        tc::mbar_wait(drain, 0, kWaitLimit);
-      }
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit_w(tmem + kD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdesc, kk > 0);
+      tc::mma_commit_w(mma2);
+      tc::mma_commit_w(empty + st);
+    }
+    if (!ok && lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    if (issued) {
+      tc::mma_commit_w(drain);
+      wait_all(drain, 0);
     }
   } else {
     const int q = warp & 3, cg = warp >> 2;   // TMEM lane quarter, 32-column group
@@ -1734,58 +1820,6 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// ------------------------------------------------- output epilogue, own pass
-// The output epilogue as a pass of its own over o, for chains whose CTAs hold
-// only part of a token's d_v outputs: each warp takes kRows (token, head) rows,
-// issues all their loads (o, gate logits: 8 bytes per lane and row) before using
-// any, then writes each row back as Sigmoid(gate) * row / RMS(row) * weight.
-constexpr int kEpiRows = 4;   // rows per warp
-
-template <int DV>
-__global__ void __launch_bounds__(256) out_epilogue_kernel(bf16* __restrict__ o, const bf16* __restrict__ gate,
-                                                           const float* __restrict__ weight, float eps,
-                                                           int64_t rows, int32_t H) {
-  constexpr int V = DV / 32;   // values per lane: 4 or 2
-  using Vec = typename std::conditional<V == 4, uint2, uint32_t>::type;
-  const int lane = threadIdx.x & 31;
-  const int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * kEpiRows;
-  Vec xo[kEpiRows], xg[kEpiRows];
-#pragma unroll
-  for (int k = 0; k < kEpiRows; ++k) {
-    const int64_t row = row0 + k;
-    if (row < rows) {
-      xo[k] = *reinterpret_cast<const Vec*>(o + row * DV + lane * V);
-      xg[k] = *reinterpret_cast<const Vec*>(gate + row * DV + lane * V);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kEpiRows; ++k) {
-    const int64_t row = row0 + k;
-    if (row >= rows) break;   // rows are contiguous: the rest of this warp's rows are past the end too
-    const int h = (int)(row % H);
-    const bf16* xv = reinterpret_cast<const bf16*>(&xo[k]);
-    const bf16* gv = reinterpret_cast<const bf16*>(&xg[k]);
-    float x[V];
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      x[e] = __bfloat162float(xv[e]);
-      ss += x[e] * x[e];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float sc = rsqrtf(ss * (1.f / DV) + eps);
-    Vec out;
-    bf16* ov = reinterpret_cast<bf16*>(&out);
-#pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const float w = weight ? weight[(int64_t)h * DV + lane * V + e] : 1.f;
-      ov[e] = __float2bfloat16_rn(x[e] * sc * w / (1.f + __expf(-__bfloat162float(gv[e]))));
-    }
-    *reinterpret_cast<Vec*>(o + row * DV + lane * V) = out;
-  }
-}
-
 // --------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1913,8 +1947,10 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int cols = std::atoi(env);
     if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
-  // The output epilogue needs a token's d_v outputs: fused into the chain when
-  // its CTAs hold all of them, else applied by a pass of its own afterwards.
+  // The output epilogue needs a token's d_v outputs: fused into the chain, the
+  // 32-column CTAs of a head exchanging row sums within their cluster, or one CTA
+  // holding all d_v columns (the 64-column wide form is not used with it).
+  if (p.out_gate && ncol != BV) ncol = DV;
   const bool fuse = p.out_gate && ncol == DV;
   const bool wide = ncol != BV;
   CUtensorMap mWQ, mP, mKT, mU, mGam;
@@ -1926,25 +1962,41 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
                 wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (wide) {
-    e = launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
-  } else {
-    e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
+  if (wide) return launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
+  const unsigned n_ctas = (unsigned)p.num_seqs * p.H * (DV / BV);
+  if (!p.out_gate) {
+    e = cudaFuncSetAttribute(chunk_chain_tc<DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ChainTcSmem::kAlloc);
     if (e != cudaSuccess) return e;
     prof_begin(stream, "chunk_chain_tc");
-    chunk_chain_tc<DV><<<(unsigned)p.num_seqs * p.H * (DV / BV), kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
+    chunk_chain_tc<DV, false><<<n_ctas, kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
         mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-        p.dev_err);
+        OutEpilogue{nullptr, nullptr, 0.f}, p.dev_err);
     prof_end(stream);
-    e = cudaGetLastError();
+    return cudaGetLastError();
   }
-  if (e != cudaSuccess || !p.out_gate || fuse) return e;
-  const int64_t rows = p.total_tokens * p.H;
-  if (rows == 0) return cudaSuccess;
-  prof_begin(stream, "out_epilogue");
-  out_epilogue_kernel<DV><<<(unsigned)((rows + 8 * kEpiRows - 1) / (8 * kEpiRows)), 256, 0, stream>>>(
-      static_cast<bf16*>(p.o), static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms, rows, p.H);
+  // with the output epilogue: the DV / 32 CTAs of a head (consecutive blocks) form one cluster
+  e = cudaFuncSetAttribute(chunk_chain_tc<DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)ChainTcSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas, 1, 1);
+  cfg.blockDim = dim3(kChainTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = ChainTcSmem::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = DV / BV;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const OutEpilogue ep{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms};
+  prof_begin(stream, "chunk_chain_tc_gated");
+  e = cudaLaunchKernelEx(&cfg, chunk_chain_tc<DV, true>, mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map,
+                         p.s0, p.s_final, static_cast<bf16*>(p.o), ep, p.dev_err);
   prof_end(stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -68,6 +68,63 @@ __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t nthreads, bool
   return r != 0;
 }
 
+// ------------------------------------------------------------------ clusters
+// Rank of this CTA in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address, in the cluster's shared window, of the same shared-memory location
+// of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Store to a (possibly remote) cluster shared-memory address from mapa_shared.
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of a (possibly remote) CTA of the cluster, with
+// release semantics at cluster scope (orders this thread's earlier writes,
+// and those it has observed, before the arrival).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// Bounded wait for a phase of a local mbarrier that CTAs of the cluster arrive
+// on, with acquire semantics at cluster scope.  Returns false after
+// `limit_cycles`.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit_cycles) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// Every thread of every CTA of the cluster arrives, then waits for all of
+// them (a hardware barrier like __syncthreads, at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -295,6 +352,34 @@ __device__ __forceinline__ void mma_16bit_ta(uint32_t d_tmem, uint32_t a_tmem, u
 // Ordered with the MMAs issued later by the same thread.
 __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t src_desc) {
   asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// Warp-level forms: executed by all 32 lanes of a warp with warp-uniform
+// operands; elect.sync picks one lane (always the same one, lane 0, when the
+// whole warp is active) to issue.  Keeping the operands uniform across the
+// warp lets them live in uniform registers, so back-to-back MMAs issue in a
+// few cycles each instead of waiting on per-instruction register moves
+// (measured: 8 MMAs issued in ~17 cycles this way, ~600-800 from one lane
+// inside a lane-0 branch).
+__device__ __forceinline__ void mma_16bit_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, pe;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by the warp's elected lane has completed
+// (whole warp).
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred pe;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
