@@ -57,6 +57,8 @@
 
 #include <cstdlib>
 #include "tc_ptx.cuh"
+#include "chain_common.cuh"
+#include "kda_chain_transition.cuh"
 
 namespace kda {
 namespace {
@@ -66,7 +68,12 @@ using f16 = __half;
 constexpr int C = kChunk;         // 64 tokens per chunk
 constexpr int DK = 128;           // key dim of this path
 constexpr int BV = 32;            // value columns per chain CTA
-constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clocks per bounded wait
+using tcu::kWaitLimit;
+using tcu::pack_bf16x2;
+using tcu::pack_f16x2;
+using tcu::report_nonfinite;
+using tcu::store_bf16x16;
+using tcu::store_mn_half;
 
 // ------------------------------------------------------------ mma.sync helpers
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -91,10 +98,6 @@ __device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
 
@@ -142,11 +145,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // Global loads issued where they stand (the compiler may not sink them to the
 // first use), for values needed a task later.
@@ -1043,7 +1041,7 @@ constexpr int kChainTcThreads = 32 * (kChainConsumerWarps + 2);
 // M = 128, N = 32.
 constexpr uint32_t kIdescMN = tc::idesc_f16_f32(128, BV) | (1u << 16);
 constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kTmemD12 = 0;    // D12 buffers of 32 columns: two (chunk parity), three with the output epilogue
+constexpr uint32_t kTmemD12 = 0;    // D12 buffers of 32 columns, one per chunk parity
 
 struct ChainTcSmem {
   // one pipeline stage (all tiles 1024-byte aligned, 128-byte swizzle unless noted)
@@ -1056,42 +1054,11 @@ struct ChainTcSmem {
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
   static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
   static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
-  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2], rs[2]
-  static constexpr uint32_t oTmem = oBar + 13 * 8;
-  // output epilogue: per chunk parity, the row sums of squares of o of every
-  // (cluster rank, 16-column half) of the head, fp32 [2][8][64]
-  static constexpr uint32_t oRss = oTmem + 16;
-  static constexpr uint32_t kBytes = oRss + 2 * 8 * 64 * 4;
+  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2]
+  static constexpr uint32_t oTmem = oBar + 11 * 8;
+  static constexpr uint32_t kBytes = oTmem + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
-
-// 16 fp32 values (value columns 16 hf .. 16 hf + 15) of K row `k` of an MN-major
-// SW64 operand, as fp16, in two 16-byte stores.
-__device__ __forceinline__ void store_mn_half(uint8_t* tile, int k, int hf, const float (&x)[16]) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j)
-    *reinterpret_cast<uint4*>(tile + tc::sw64_chunk_offset(k, 2 * hf + j)) =
-        make_uint4(pack_f16x2(x[8 * j + 0], x[8 * j + 1]), pack_f16x2(x[8 * j + 2], x[8 * j + 3]),
-                   pack_f16x2(x[8 * j + 4], x[8 * j + 5]), pack_f16x2(x[8 * j + 6], x[8 * j + 7]));
-}
-
-// 16 fp32 values as bf16 to global memory (two 16-byte stores).
-__device__ __forceinline__ void store_bf16x16(bf16* dst, const float (&x)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int j = 0; j < 2; ++j)
-    d[j] = make_uint4(pack_bf16x2(x[8 * j + 0], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
-                      pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
-}
-
-// Whole warp: records kDevErrNonFinite in the device error word (unless a code is
-// already there) when any lane's accumulated x * 0 checks are not 0, i.e. some
-// o or state value it wrote was inf or NaN (an fp16 operand of the chain out of
-// range, or non-finite inputs).
-__device__ __forceinline__ void report_nonfinite(float acc, int32_t* dev_err) {
-  if (__any_sync(0xffffffffu, !(acc == 0.f)) && (threadIdx.x & 31) == 0)
-    atomicCAS(dev_err, 0, (int32_t)kDevErrNonFinite);
-}
 
 // Inter-chunk pass of one (sequence, head, 32-column value block): the state
 // lives in fp32 registers of the consumer threads (key channel = TMEM lane),
@@ -1100,28 +1067,20 @@ __device__ __forceinline__ void report_nonfinite(float acc, int32_t* dev_err) {
 //   V_new  = u - (w S)                                 (consumers, to SMEM)
 //   group 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
 //   S      = e^{G_last} S + D3                          (consumers)
-// With kGated, the output epilogue (Sigmoid gate times the per-head RMSNorm of
-// o) is applied before o is written.  A token's d_v outputs are spread over the
-// DV/32 CTAs of its head, which the launch groups into one thread-block cluster:
-// every o thread sends its row's partial sum of squares to each CTA of the
-// cluster (distributed shared memory, an mbarrier per chunk parity with
-// cluster-scope release / acquire), then scales its row by the total.  The o
-// rows of a chunk are then emitted after the next state hand-off, off the
-// chain's critical path, so D12 has three buffers (chunk i in buffer i % 3,
-// next written by group 1 of chunk i + 3).
-template <int DV, bool kGated>
+// (With the output epilogue the 32-column chain is the transition-form kernel of
+// kda_chain_transition.cu.)
+template <int DV>
 __global__ void __launch_bounds__(kChainTcThreads, 1)
     chunk_chain_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
                    const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu, int32_t num_seqs,
                    int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0, float* __restrict__ s_final,
-                   bf16* __restrict__ o, OutEpilogue ep, int32_t* dev_err) {
+                   bf16* __restrict__ o, int32_t* dev_err) {
   using L = ChainTcSmem;
-  constexpr int kRanks = DV / BV;                    // CTAs (column blocks) per head: the cluster with kGated
-  constexpr uint32_t kNBuf = kGated ? 3 : 2;         // D12 buffers
+  constexpr uint32_t kNBuf = 2;                      // D12 buffers
   constexpr uint32_t kTmemD3 = kTmemD12 + kNBuf * BV;
   static_assert(kTmemD3 + BV <= kTmemCols, "TMEM columns");
-  if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing (every CTA of a cluster alike)
+  if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::oBar);
@@ -1132,9 +1091,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* vn_ready = full + 7;   // the 4 V_new warps have stored their rows
   uint64_t* s_ready = full + 8;    // the 8 consumer warps have stored the state and read TMEM
   uint64_t* cons = full + 9;       // [2] the 8 consumer warps are done reading a stage (gam, u)
-  uint64_t* rs_full = full + 11;   // [2] output epilogue: every o warp of the cluster has sent its row sums
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
-  float* rss = reinterpret_cast<float*>(sm + L::oRss);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
 
@@ -1153,8 +1110,6 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     tc::mbar_init(s_ready, kChainConsumerWarps);     // one arrival per consumer warp
     tc::mbar_init(cons, kChainConsumerWarps);        // one arrival per consumer warp and chunk
     tc::mbar_init(cons + 1, kChainConsumerWarps);
-    tc::mbar_init(rs_full, 4 * kRanks);              // one arrival per o warp of the cluster
-    tc::mbar_init(rs_full + 1, 4 * kRanks);
     tc::fence_mbar_init();
   }
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
@@ -1170,8 +1125,6 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  // the cluster's barriers are initialised before any CTA of it sends row sums
-  if constexpr (kGated) tc::cluster_sync_all();
   const uint32_t tmem = *tslot;
 
   if (warp == kChainTmaWarp) {
@@ -1272,56 +1225,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(s_ready);
     float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
-    // Output epilogue (kGated, o warps q >= 2, row r = token of the chunk):
-    // this thread's 16 norm weights, and the gate logits of the chunk it emits
-    // next, loaded a chunk ahead.
-    const int r = c - 64;
-    float wgt[16];
-    uint4 gcur[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-    if constexpr (kGated) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) wgt[e] = (q >= 2 && ep.weight) ? ep.weight[(int64_t)h * DV + n0 + 16 * hf + e] : 1.f;
-    }
-    const uint32_t crank = kGated ? tc::cluster_ctarank() : 0u;
-    auto load_gate = [&](int64_t t0, int64_t len) {
-      if (r < len) {
-        const uint4* gp = reinterpret_cast<const uint4*>(ep.gate + ((t0 + r) * H + h) * DV + n0 + 16 * hf);
-        gcur[0] = gp[0];
-        gcur[1] = gp[1];
-      }
-    };
-    // o rows of chunk j from D12 buffer `buf`: row sums of squares to every CTA
-    // of the cluster, the total from all of them, then the scaled row.
-    auto emit_gated = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
-      float ov[16];
-      tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + buf * BV + 16 * hf), ov);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) ss = fmaf(ov[e], ov[e], ss);
-      const int par = j & 1;
-      float* slot = rss + (par * 8 + (int)crank * 2 + hf) * 64 + r;
-#pragma unroll
-      for (uint32_t d = 0; d < (uint32_t)kRanks; ++d) tc::st_shared_cluster_f32(tc::mapa_shared(slot, d), ss);
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (uint32_t d = 0; d < (uint32_t)kRanks; ++d) tc::mbar_arrive_cluster(tc::mapa_shared(rs_full + par, d));
-      }
-      if (!tc::mbar_wait_cluster(rs_full + par, (uint32_t)(j >> 1) & 1u, kWaitLimit)) return false;
-      float tot = 0.f;
-#pragma unroll
-      for (int k2 = 0; k2 < 2 * kRanks; ++k2) tot += rss[(par * 8 + k2) * 64 + r];
-      const float sc = rsqrtf(tot * (1.f / DV) + ep.eps);
-      if (r < len) {
-        const bf16* gv = reinterpret_cast<const bf16*>(gcur);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ov[e] *= sc * wgt[e] / (1.f + __expf(-__bfloat162float(gv[e])));
-        store_bf16x16(o + ((t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
-      }
-      return true;
-    };
+    const int r = c - 64;   // o warps (q >= 2): token row of the chunk
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -1339,7 +1243,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(cons + st);   // this warp reads nothing more of the stage
       }
-      if (!kGated && q >= 2) {
+      if (q >= 2) {
         // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer,
         // read while the state product is issued: its o product completed
         // before this chunk's group 1 (mma1)
@@ -1351,7 +1255,6 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         }
         tc::tc_fence_after();
         if (i > 0) {
-          const int r = c - 64;
           float ov[16];
           tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
           if (r < prev_len) {
@@ -1408,22 +1311,6 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 #pragma unroll
         for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
       }
-      if constexpr (kGated) {
-        // the previous chunk's o rows, after this warp's state hand-off (their
-        // product completed before this chunk's group 1, whose completion this
-        // warp has seen through mma2); then the gate logits of this chunk
-        if (q >= 2) {
-          if (i > 0) {
-            bad |= !emit_gated((uint32_t)((i - 1) % 3), prev_t0, prev_len, i - 1);
-            if (__any_sync(0xffffffffu, bad)) {
-              bad = true;
-              break;
-            }
-          }
-          const int64_t t0 = seq_start + (int64_t)i * C;
-          load_gate(t0, min((int64_t)C, seq_end - t0));
-        }
-      }
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
@@ -1431,9 +1318,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       bad = __any_sync(0xffffffffu, !tc::mbar_wait(drain, 0, kWaitLimit));
       tc::tc_fence_after();
     }
-    if (kGated && i == nch && !bad && nch > 0 && q >= 2)
-      bad = __any_sync(0xffffffffu, !emit_gated((uint32_t)((nch - 1) % 3), prev_t0, prev_len, nch - 1));
-    if (!kGated && i == nch && !bad && nch > 0 && q >= 2) {
+    if (i == nch && !bad && nch > 0 && q >= 2) {
       float ov[16];
       tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
       if (r < prev_len) {
@@ -1458,8 +1343,6 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
-  // no CTA of the cluster leaves while another may still send it row sums
-  if constexpr (kGated) tc::cluster_sync_all();
 }
 
 // ------------------------------------------------------- wide chain kernel
@@ -1679,7 +1562,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
 #pragma unroll
             for (int v8 = 0; v8 < 2; ++v8) {
               const uint4 raw = gp[v8];
-              const bf16* gv = reinterpret_cast<const bf16*>(&raw);
+              const uint32_t gw[4] = {raw.x, raw.y, raw.z, raw.w};   // bf16 pairs, unpacked by shifts
               float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
               if (ep.weight) {
                 w0 = *reinterpret_cast<const float4*>(ep.weight + (int64_t)h * DV + col0 + 8 * v8);
@@ -1687,7 +1570,10 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
               }
               const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-              for (int e = 0; e < 8; ++e) ov[8 * v8 + e] *= sc * wv[e] / (1.f + __expf(-__bfloat162float(gv[e])));
+              for (int e = 0; e < 8; ++e) {
+                const float x = (e & 1) ? __uint_as_float(gw[e >> 1] & 0xffff0000u) : __uint_as_float(gw[e >> 1] << 16);
+                ov[8 * v8 + e] *= __fdividef(sc * wv[e], 1.f + __expf(-x));
+              }
             }
           }
           store_bf16x16(o + ((t0 + r) * H + h) * DV + col0, ov);
@@ -1947,9 +1833,10 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     const int cols = std::atoi(env);
     if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
-  // The output epilogue needs a token's d_v outputs: fused into the chain, the
-  // 32-column CTAs of a head exchanging row sums within their cluster, or one CTA
-  // holding all d_v columns (the 64-column wide form is not used with it).
+  // The output epilogue needs a token's d_v outputs: fused into the chain, either
+  // the transition-form 32-column chain (the CTAs of a head exchange row sums
+  // within their cluster) or one CTA holding all d_v columns (the 64-column wide
+  // form is not used with it).
   if (p.out_gate && ncol != BV) ncol = DV;
   const bool fuse = p.out_gate && ncol == DV;
   const bool wide = ncol != BV;
@@ -1963,40 +1850,14 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (wide) return launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
+  if (p.out_gate) return launch_chain_transition_gated(mWQ, mP, mKT, mU, mGam, p, map, stream);
   const unsigned n_ctas = (unsigned)p.num_seqs * p.H * (DV / BV);
-  if (!p.out_gate) {
-    e = cudaFuncSetAttribute(chunk_chain_tc<DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)ChainTcSmem::kAlloc);
-    if (e != cudaSuccess) return e;
-    prof_begin(stream, "chunk_chain_tc");
-    chunk_chain_tc<DV, false><<<n_ctas, kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
-        mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o),
-        OutEpilogue{nullptr, nullptr, 0.f}, p.dev_err);
-    prof_end(stream);
-    return cudaGetLastError();
-  }
-  // with the output epilogue: the DV / 32 CTAs of a head (consecutive blocks) form one cluster
-  e = cudaFuncSetAttribute(chunk_chain_tc<DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)ChainTcSmem::kAlloc);
+  e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_ctas, 1, 1);
-  cfg.blockDim = dim3(kChainTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = ChainTcSmem::kAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = DV / BV;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const OutEpilogue ep{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms};
-  prof_begin(stream, "chunk_chain_tc_gated");
-  e = cudaLaunchKernelEx(&cfg, chunk_chain_tc<DV, true>, mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map,
-                         p.s0, p.s_final, static_cast<bf16*>(p.o), ep, p.dev_err);
+  prof_begin(stream, "chunk_chain_tc");
+  chunk_chain_tc<DV><<<n_ctas, kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
+      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o), p.dev_err);
   prof_end(stream);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -89,6 +89,16 @@ __device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Asynchronous 4-byte store to a (possibly remote) cluster shared-memory address
+// that, once written, counts its bytes on an mbarrier of the same CTA (both
+// addresses from mapa_shared): the receiver's wait on that barrier sees the
+// data, with no fence on the sender's side.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr), "f"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
 // Arrive on an mbarrier of a (possibly remote) CTA of the cluster, with
 // release semantics at cluster scope (orders this thread's earlier writes,
 // and those it has observed, before the arrival).
@@ -133,6 +143,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // 2D tiled load of the box at (x = inner coordinate, y) into shared memory;
 // completion is counted in bytes on `bar`.  x * element size must be a
 // multiple of 16 bytes.
+// Prefetch of a 2D tile into L2 (no shared-memory destination, no completion
+// to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -158,6 +176,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, 
                "r"(x), "r"(y), "r"(smem_u32(src))
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to a
+// (possibly remote) cluster shared-memory address, counted on an mbarrier of
+// the destination CTA (dst and bar from mapa_shared).  Part of the thread's
+// bulk-copy groups (bulk_commit, bulk_wait_read0 / bulk_wait0).
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// Waits until at most one bulk-copy group of this thread is still reading its source.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -218,6 +247,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 16 consecutive 32-bit columns of this thread's lane written from registers
+// (warp w writes lanes 32*(w%4) .. +31); tmem_st_wait() waits for the warp's
+// stores to complete.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor of a K-major bf16 operand laid out in the
@@ -369,6 +411,19 @@ __device__ __forceinline__ void mma_16bit_w(uint32_t d_tmem, uint64_t a_desc, ui
       "elect.sync _|pe, 0xffffffff;\n\t"
       "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Whole-warp form with the A operand in TMEM (16-bit K elements packed two per
+// column, lower K index in the low half; a K = 16 slice spans 8 columns).
+__device__ __forceinline__ void mma_16bit_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, pe;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|pe, 0xffffffff;\n\t"
+      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
