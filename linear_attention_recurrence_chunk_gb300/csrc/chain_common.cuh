@@ -25,6 +25,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// V_new = u - w S for eight value columns: u as four fp16 pairs (one 16-byte
+// load), w S as fp32 from TMEM.  w S is rounded to fp16 and the difference taken
+// in packed fp16 arithmetic (round-to-nearest), two instructions per pair; the
+// extra rounding of w S leaves the path's error unchanged (checked against the
+// oracle by the CPU emulation of the rounding scheme).
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint4 vnew_f16x8(uint4 u, const float* ws) {
+  return make_uint4(sub_f16x2(u.x, pack_f16x2(ws[0], ws[1])), sub_f16x2(u.y, pack_f16x2(ws[2], ws[3])),
+                    sub_f16x2(u.z, pack_f16x2(ws[4], ws[5])), sub_f16x2(u.w, pack_f16x2(ws[6], ws[7])));
+}
+
 // 16 fp32 values (value columns 16 hf .. 16 hf + 15) of K row `k` of an MN-major
 // SW64 operand, as fp16, in two 16-byte stores.
 __device__ __forceinline__ void store_mn_half(uint8_t* tile, int k, int hf, const float (&x)[16]) {

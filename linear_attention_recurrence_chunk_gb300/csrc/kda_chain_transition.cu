@@ -107,14 +107,9 @@ struct TransitionSmem {
   static_assert(kAlloc <= 232448, "fits the shared-memory limit");
 };
 
-// The two bf16 (fp16) values of a packed word as floats, without going through memory.
+// The two bf16 values of a packed word as floats, without going through memory.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
-  __half2 h;
-  memcpy(&h, &w, 4);
-  return __half22float2(h);
-}
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 v;
@@ -503,16 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld32(tc::tmem_addr(tmem, tl, kColD12 + (uint32_t)(i % kNB) * NC), d);
       uint8_t* vb = sm + L::oVN;   // one buffer: the o product of chunk i - 1 preceded [w; q e^G] S of chunk i
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t uw[4] = {uraw[k].x, uraw[k].y, uraw[k].z, uraw[k].w};
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 uf = f16x2_to_float2(uw[e]);
-          pk[e] = pack_f16x2(uf.x - d[8 * k + 2 * e], uf.y - d[8 * k + 2 * e + 1]);
-        }
-        *reinterpret_cast<uint4*>(vb + tc::sw64_chunk_offset(r, k)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint4*>(vb + tc::sw64_chunk_offset(r, k)) = tcu::vnew_f16x8(uraw[k], d + 8 * k);
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();

@@ -1276,11 +1276,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 2; ++q4) {
           const uint4 raw = *reinterpret_cast<const uint4*>(stg + L::oU + tc::sw64_chunk_offset(c, 2 * hf + q4));
-          const f16* uv = reinterpret_cast<const f16*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
+          *reinterpret_cast<uint4*>(sVN + tc::sw64_chunk_offset(c, 2 * hf + q4)) = tcu::vnew_f16x8(raw, d + 8 * q4);
         }
-        store_mn_half(sVN, c, hf, d);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncwarp();
@@ -1630,11 +1627,9 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
           for (int q4 = 0; q4 < 2; ++q4) {
             const uint4 raw =
                 *reinterpret_cast<const uint4*>(uat + tc::sw128_offset(c, 32 * (cg & 1) + 16 * hf + 8 * q4));
-            const f16* uv = reinterpret_cast<const f16*>(&raw);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) d[q4 * 8 + e] = __half2float(uv[e]) - d[q4 * 8 + e];
+            *reinterpret_cast<uint4*>(sVN + cg * L::kVAtom + tc::sw64_chunk_offset(c, 2 * hf + q4)) =
+                tcu::vnew_f16x8(raw, d + 8 * q4);
           }
-          store_mn_half(sVN + cg * L::kVAtom, c, hf, d);
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();

@@ -14,7 +14,8 @@ test_chunk_algebra.py) with the kernels' operands and records:
     in fp16 (P V_new and w S are the error-sensitive products: V_new is
     O(|v|) while o is an order of magnitude smaller);
   - the chain: fp32 master state, its fp16 copy and V_new in fp16 as MMA
-    operands, o rounded to bf16.
+    operands (V_new = u - w S with w S rounded to fp16 first, as the kernels'
+    packed fp16 subtraction does), o rounded to bf16.
 X is formed exactly from the rounded A and then rounded; the kernel's fp16
 products for X's blocks below the diagonal also round their intermediate
 16x16 blocks, which this does not model.
@@ -92,7 +93,7 @@ def emulate(q, k, v, g, beta, s0, scheme):
         kt = rec(kk * np.exp(G[-1] - G))
         gam = np.exp(G[-1])
         Sop = rec(S)
-        vn = rec(u - w @ Sop)
+        vn = rec(u - rec(w @ Sop))   # w S rounded to fp16, the difference in fp16 (packed arithmetic)
         o = _bf16(qh @ Sop + P @ vn)
         S = _f32(gam[:, None] * S + kt.T @ vn)
         outs.append(o[:L])
