@@ -460,11 +460,24 @@ def bench_gated(args, r, steps):
     st, code = kda.kda_device_error()
     if st != 0:
         raise RuntimeError(f"device error {code} in the gated leg")
+    lib = kda.load_library()
+    _prof(lib, True)
     ms, spread = timed_steps(step, steps, stream)
+    _prof(lib, False)
+    _, recs = _collect(lib)
+    per = {}
+    for nm, v in recs:
+        per.setdefault(nm, []).append(v)
+    kernels = {nm: round(statistics.mean(v), 4) for nm, v in per.items()}
+    if "chunk_chain_transition_tc" in kernels:
+        note = ("fused into the 32-column chain in transition form: the CTAs of a head form a cluster and "
+                "exchange row sums of squares")
+    else:
+        note = "fused into the all-columns chain: the o warps of the CTA exchange row sums of squares"
     del gate, nw
     return {"value": w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "spread": spread, "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps),
-            "note": "fused into the chain: the 32-column CTAs of a head exchange row sums within their cluster"}
+            "spread": spread, "slowdown_vs_plain": ms / (r["elapsed_ms"] / args.steps), "kernels_ms": kernels,
+            "note": note}
 
 
 def bench_decay_ablation(args, r, steps):
