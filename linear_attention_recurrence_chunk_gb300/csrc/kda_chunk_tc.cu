@@ -58,7 +58,6 @@
 #include <cstdlib>
 #include "tc_ptx.cuh"
 #include "chain_common.cuh"
-#include "kda_chain_transition.cuh"
 
 namespace kda {
 namespace {
@@ -1032,16 +1031,24 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 
 // -------------------------------------------------------------- chain kernel
 // Warp roles: 8 consumer warps (warp w reads TMEM lanes 32(w%4)..+31 and the
-// value columns 16(w/4)..+15 of the CTA's block), one TMA producer warp and
-// one MMA-issuing warp.
+// value columns 16(w/4)..+15 of the CTA's block), one TMA producer warp and one
+// MMA-issuing warp.  Without the output epilogue the consumer warps of lanes
+// 64-127 also write the o rows.  With it, four o warps do: TMEM lanes 64-127
+// are readable by warps 2 and 3 mod 4 only, so warps 10 and 11 take value
+// columns 0-15 of the o rows and warps 14 and 15 columns 16-31 (12 and 13 have
+// no role).  (Dedicated o warps without the epilogue measured 9 % slower.)
 constexpr int kChainConsumerWarps = 8;
 constexpr int kChainTmaWarp = 8, kChainMmaWarp = 9;
-constexpr int kChainTcThreads = 32 * (kChainConsumerWarps + 2);
+constexpr int kChainOWarp0 = 10, kChainOWarp1 = 14, kChainOWarps = 4;
+constexpr int chain_threads(bool gated) { return 32 * (gated ? 16 : kChainConsumerWarps + 2); }
+// D12 buffers: one per chunk parity, four with the o warps (which may read a
+// chunk's rows while later chunks are formed)
+constexpr int chain_buffers(bool gated) { return gated ? 4 : 2; }
+constexpr int kMaxRanks = 4;    // CTAs of a head at most (d_v / 32)
 // K-major A (TMA-staged tiles), MN-major B (the state block / V_new written by the threads), fp16,
 // M = 128, N = 32.
 constexpr uint32_t kIdescMN = tc::idesc_f16_f32(128, BV) | (1u << 16);
-constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kTmemD12 = 0;    // D12 buffers of 32 columns, one per chunk parity
+constexpr uint32_t kTmemD12 = 0;    // D12 buffers of 32 columns, then D3
 
 struct ChainTcSmem {
   // one pipeline stage (all tiles 1024-byte aligned, 128-byte swizzle unless noted)
@@ -1054,8 +1061,16 @@ struct ChainTcSmem {
   static constexpr uint32_t kTxBytes = 32768 + 8192 + 16384 + 64 * BV * 2 + DK * 4;
   static constexpr uint32_t oS = 2 * kStage;   // state block as MN-major B operand: [128 keys][32 value cols]
   static constexpr uint32_t oVN = oS + 8192;   // V_new as MN-major B operand: [64 tokens][32 value cols]
-  static constexpr uint32_t oBar = oVN + 4096; // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2]
-  static constexpr uint32_t oTmem = oBar + 11 * 8;
+  // output epilogue: the CTA's 32 norm weights, the row sums of squares to send
+  // (fp32 [2 parities][4 o warps][32]) and those received (fp32 [2 parities]
+  // [kMaxRanks][2 column halves][64 rows])
+  static constexpr uint32_t oWgt = oVN + 4096;
+  static constexpr uint32_t oStg = oWgt + BV * 4;
+  static constexpr uint32_t oRss = oStg + 2 * kChainOWarps * 32 * 4;
+  // full[2], empty[2], mma1, mma2, drain, vn_ready, s_ready, cons[2]; with the output
+  // epilogue ofull[4], dfree[4], rs[2]
+  static constexpr uint32_t oBar = oRss + 2 * kMaxRanks * 2 * 64 * 4;
+  static constexpr uint32_t oTmem = oBar + 21 * 8;
   static constexpr uint32_t kBytes = oTmem + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;   // slack to align the base to 1024
 };
@@ -1067,18 +1082,27 @@ struct ChainTcSmem {
 //   V_new  = u - (w S)                                 (consumers, to SMEM)
 //   group 2: D12 += [0; P] V_new (o rows), D3 = K~^T V_new
 //   S      = e^{G_last} S + D3                          (consumers)
-// (With the output epilogue the 32-column chain is the transition-form kernel of
-// kda_chain_transition.cu.)
-template <int DV>
-__global__ void __launch_bounds__(kChainTcThreads, 1)
+// With kGated the o rows of a chunk are read by the four o warps once its o
+// product has completed, and they apply the output epilogue (Sigmoid gate times
+// the per-head RMSNorm of o and its weight) first: a token's d_v outputs are
+// spread over the DV/32 CTAs of its head, which the launch groups into one
+// thread-block cluster, and each o warp sends its 32 rows' partial sums of
+// squares to every CTA of it as one bulk shared-memory copy counted on the
+// receiver's mbarrier.
+template <int DV, bool kGated>
+__global__ void __launch_bounds__(chain_threads(kGated), 1)
     chunk_chain_tc(const __grid_constant__ CUtensorMap tmWQ, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmKT, const __grid_constant__ CUtensorMap tmU,
                    const __grid_constant__ CUtensorMap tmGam, const int32_t* __restrict__ cu, int32_t num_seqs,
                    int64_t T_seq, int32_t H, ChunkMap map, const float* __restrict__ s0, float* __restrict__ s_final,
-                   bf16* __restrict__ o, int32_t* dev_err) {
+                   bf16* __restrict__ o, OutEpilogue ep, int32_t* dev_err) {
   using L = ChainTcSmem;
-  constexpr uint32_t kNBuf = 2;                      // D12 buffers
+  constexpr int kRanks = DV / BV;                    // CTAs per head (the cluster with kGated)
+  static_assert(kRanks <= kMaxRanks, "row-sum slots");
+  constexpr uint32_t kNBuf = chain_buffers(kGated);  // D12 buffers
   constexpr uint32_t kTmemD3 = kTmemD12 + kNBuf * BV;
+  constexpr uint32_t kTmemCols = kGated ? 256 : 128;
+  constexpr int kThreads = chain_threads(kGated);
   static_assert(kTmemD3 + BV <= kTmemCols, "TMEM columns");
   if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
   extern __shared__ uint8_t smem_raw[];
@@ -1091,9 +1115,15 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   uint64_t* vn_ready = full + 7;   // the 4 V_new warps have stored their rows
   uint64_t* s_ready = full + 8;    // the 8 consumer warps have stored the state and read TMEM
   uint64_t* cons = full + 9;       // [2] the 8 consumer warps are done reading a stage (gam, u)
+  uint64_t* ofull = full + 11;     // [4] a chunk's o rows are complete in its D12 buffer
+  uint64_t* dfree = full + 15;     // [4] the o warps have read a D12 buffer
+  uint64_t* rs = full + 19;        // [2] output epilogue: the row sums of every o warp of the cluster have landed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
   uint8_t* sS = sm + L::oS;
   uint8_t* sVN = sm + L::oVN;
+  float* sWgt = reinterpret_cast<float*>(sm + L::oWgt);
+  float* sStg = reinterpret_cast<float*>(sm + L::oStg);
+  float* rss = reinterpret_cast<float*>(sm + L::oRss);
 
   // one-dimensional grid, sequence-rank major: all blocks of the longest chain first
   const int blk = (int)(blockIdx.x % (unsigned)(H * (DV / BV)));
@@ -1110,10 +1140,17 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     tc::mbar_init(s_ready, kChainConsumerWarps);     // one arrival per consumer warp
     tc::mbar_init(cons, kChainConsumerWarps);        // one arrival per consumer warp and chunk
     tc::mbar_init(cons + 1, kChainConsumerWarps);
+    for (int b = 0; b < (int)kNBuf; ++b) {
+      tc::mbar_init(ofull + b, 1);
+      tc::mbar_init(dfree + b, kChainOWarps);
+    }
+    tc::mbar_init(rs, 1);   // one local arrival (with the expected bytes) per phase
+    tc::mbar_init(rs + 1, 1);
     tc::fence_mbar_init();
   }
+  if (kGated && tid < BV) sWgt[tid] = ep.weight ? ep.weight[(int64_t)h * DV + n0 + tid] : 1.f;
   // rows 0-63 of both [0; P] tiles are zero for the whole kernel
-  for (int i = tid; i < 2 * 512; i += kChainTcThreads) {
+  for (int i = tid; i < 2 * 512; i += kThreads) {
     const int st = i >> 9, off = (i & 511) * 16;
     *reinterpret_cast<uint4*>(sm + st * L::kStage + L::oPZ + off) = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -1125,6 +1162,8 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // the cluster's barriers are initialised before any CTA of it sends row sums
+  if constexpr (kGated) tc::cluster_sync_all();
   const uint32_t tmem = *tslot;
 
   if (warp == kChainTmaWarp) {
@@ -1177,6 +1216,11 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       ok = wait_all(full + st, (i >> 1) & 1) && wait_all(s_ready, i & 1);
       if (!ok) break;
       tc::tc_fence_after();
+      if (kGated && i >= (int)kNBuf) {   // the o warps have read what this buffer held kNBuf chunks ago
+        ok = wait_all(dfree + i % (int)kNBuf, (uint32_t)((i / (int)kNBuf) - 1) & 1u);
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
       const uint64_t dA = dA0 + ((uint64_t)(st * L::kStage) >> 4);
       const uint32_t d12 = tmem + kTmemD12 + (uint32_t)(i % (int)kNBuf) * BV;
 #pragma unroll
@@ -1188,9 +1232,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       ok = wait_all(vn_ready, i & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      // group 2: the state product first, committed on its own, then the o rows;
-      // the o rows are read once group 1 of the next chunk (issued after
-      // them) has completed, or after the final drain
+      // group 2: the state product first, committed on its own, then the o rows
 #pragma unroll
       for (int kk = 0; kk < C / 16; ++kk)
         tc::mma_16bit_w(tmem + kTmemD3, dA + ((L::oKT + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, kk > 0);
@@ -1199,13 +1241,14 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       for (int kk = 0; kk < C / 16; ++kk)
         tc::mma_16bit_w(d12, dA + ((L::oPZ + kk * 32) >> 4), dV0 + ((kk * 1024) >> 4), kIdescMN, 1u);
       tc::mma_commit_w(empty + st);
+      if constexpr (kGated) tc::mma_commit_w(ofull + i % (int)kNBuf);
     }
     if (!ok && lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
     if (issued) {   // no MMA may still be writing TMEM when it is freed
       tc::mma_commit_w(drain);
       wait_all(drain, 0);
     }
-  } else {
+  } else if (warp < kChainConsumerWarps) {
     // ---------------- consumers: TMEM lane quarter q, value columns 16 hf .. 16 hf + 15
     const int q = warp & 3, hf = warp >> 2;
     const int c = 32 * q + lane;   // key channel of this thread's state row; token row for V_new / o
@@ -1225,7 +1268,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(s_ready);
     float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
-    const int r = c - 64;   // o warps (q >= 2): token row of the chunk
+    const int r = c - 64;    // without the epilogue, consumer warps q >= 2 write the o rows: token row
     bool bad = false;
     int i = 0;
     int64_t prev_t0 = 0;
@@ -1243,7 +1286,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(cons + st);   // this warp reads nothing more of the stage
       }
-      if (q >= 2) {
+      if (!kGated && q >= 2) {
         // previous chunk's o rows (tokens 32(q-2)+lane) from the other buffer,
         // read while the state product is issued: its o product completed
         // before this chunk's group 1 (mma1)
@@ -1256,7 +1299,7 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
         tc::tc_fence_after();
         if (i > 0) {
           float ov[16];
-          tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * 32 + 16 * hf), ov);
+          tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)(st ^ 1) * BV + 16 * hf), ov);
           if (r < prev_len) {
             store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
 #pragma unroll
@@ -1311,17 +1354,17 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
       prev_t0 = seq_start + (int64_t)i * C;
       prev_len = min((int64_t)C, seq_end - prev_t0);
     }
-    if (i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o, once the final drain has completed
+    if (!kGated && i == nch && !bad && nch > 0 && q >= 2) {   // the last chunk's o, once the final drain has completed
       bad = __any_sync(0xffffffffu, !tc::mbar_wait(drain, 0, kWaitLimit));
       tc::tc_fence_after();
-    }
-    if (i == nch && !bad && nch > 0 && q >= 2) {
-      float ov[16];
-      tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * 32 + 16 * hf), ov);
-      if (r < prev_len) {
-        store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+      if (!bad) {
+        float ov[16];
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)((nch - 1) & 1) * BV + 16 * hf), ov);
+        if (r < prev_len) {
+          store_bf16x16(o + ((prev_t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+          for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+        }
       }
     }
     if (i < nch || bad) {
@@ -1336,10 +1379,121 @@ __global__ void __launch_bounds__(kChainTcThreads, 1)
 #pragma unroll
       for (int n = 0; n < 16; n += 4) *reinterpret_cast<float4*>(dst + n) = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
     }
+  } else if (kGated && (warp & 3) >= 2) {
+    // ---------------- o rows (TMEM lanes 64-127, token r of the chunk), value columns 16 hf .. 16 hf + 15
+    const int q = warp & 3, r = 32 * (q - 2) + lane, hf = warp >= kChainOWarp1 ? 1 : 0;
+    const int wi = 2 * hf + (q - 2);   // this warp's slot in the row-sum exchange
+    const uint32_t tl = (uint32_t)(32 * q);
+    const uint32_t crank = kGated ? tc::cluster_ctarank() : 0u;
+    float nonfinite = 0.f;   // stays 0 unless an o value is inf or NaN (x * 0 is then NaN)
+    // gate logits of the row: prefetched into L2 a few chunks ahead, into registers a chunk ahead
+    constexpr int kGatePf = 4;
+    uint4 gnext[2] = {};
+    auto gate_row = [&](int i) -> const bf16* {   // null past the sequence
+      const int64_t t0 = seq_start + (int64_t)i * C;
+      return (i < nch && r < seq_end - t0) ? ep.gate + ((t0 + r) * H + h) * DV + n0 + 16 * hf : nullptr;
+    };
+    auto load_gate = [&](int i) {   // issued where it stands
+      if (const bf16* gp = gate_row(i)) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int4 v = ld_early_v4(reinterpret_cast<const int4*>(gp) + k);
+          gnext[k] = make_uint4((uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w);
+        }
+      }
+    };
+    for (int k = 0; k < kGatePf; ++k)
+      if (const bf16* gp = gate_row(k)) asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
+    load_gate(0);
+    bool bad = false;
+    int i = 0;
+    for (; i < nch; ++i) {
+      const int b = i % (int)kNBuf;
+      const int64_t t0 = seq_start + (int64_t)i * C;
+      const int64_t len = min((int64_t)C, seq_end - t0);
+      bad |= !tc::mbar_wait(ofull + b, (uint32_t)(i / (int)kNBuf) & 1u, kWaitLimit);
+      if (__any_sync(0xffffffffu, bad)) {
+        bad = true;
+        break;
+      }
+      tc::tc_fence_after();
+      float ov[16];
+      tc::tmem_ld16(tc::tmem_addr(tmem, tl, kTmemD12 + (uint32_t)b * BV + 16 * hf), ov);
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(dfree + b);
+      {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss = fmaf(ov[e], ov[e], ss);
+        const int par = i & 1;
+        // The warp's 32 row sums go to every CTA of the cluster as one 128-byte
+        // bulk copy per destination, counted on the destination's barrier; the
+        // staging row of this parity is rewritten once the copies of chunk i - 2
+        // (the group before the latest) have read it.
+        float* stg = sStg + (par * kChainOWarps + wi) * 32;
+        if (lane == 0 && i >= 2) tc::bulk_wait_read1();
+        __syncwarp();
+        stg[lane] = ss;
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          // this CTA expects 128 bytes from each (rank, o warp) of the cluster in this phase
+          if (warp == kChainOWarp0) tc::mbar_arrive_expect_tx(rs + par, (uint32_t)kRanks * kChainOWarps * 128u);
+          float* slot = rss + ((par * kMaxRanks + (int)crank) * 2 + hf) * 64 + 32 * (q - 2);
+#pragma unroll
+          for (uint32_t d = 0; d < (uint32_t)kRanks; ++d)
+            tc::bulk_copy_s2c(tc::mapa_shared(slot, d), stg, 128u, tc::mapa_shared(rs + par, d));
+          tc::bulk_commit();
+        }
+        uint4 gcur[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) gcur[k] = gnext[k];
+        load_gate(i + 1);
+        if (const bf16* gp = gate_row(i + kGatePf)) asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
+        // the gate and the weight while the other CTAs' row sums arrive (bf16
+        // pairs unpacked with shifts, the sigmoid with the fast exponential and divide)
+        const float* wt = sWgt + 16 * hf;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t gw[4] = {gcur[k].x, gcur[k].y, gcur[k].z, gcur[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c0 = 8 * k + 2 * e;
+            ov[c0] *= __fdividef(wt[c0], 1.f + __expf(-__uint_as_float(gw[e] << 16)));
+            ov[c0 + 1] *= __fdividef(wt[c0 + 1], 1.f + __expf(-__uint_as_float(gw[e] & 0xffff0000u)));
+          }
+        }
+        bad |= !tc::mbar_wait(rs + par, (uint32_t)(i >> 1) & 1u, kWaitLimit);
+        if (__any_sync(0xffffffffu, bad)) {
+          bad = true;
+          break;
+        }
+        float tot = 0.f;
+#pragma unroll
+        for (int d = 0; d < 2 * kRanks; ++d) tot += rss[(par * kMaxRanks * 2 + d) * 64 + r];
+        const float sc = rsqrtf(tot * (1.f / DV) + ep.eps);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ov[e] *= sc;
+      }
+      if (r < len) {
+        store_bf16x16(o + ((t0 + r) * H + h) * DV + n0 + 16 * hf, ov);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) nonfinite = fmaf(ov[e], 0.f, nonfinite);
+      }
+    }
+    if (lane == 0) tc::bulk_wait0();   // every row-sum copy of this warp has completed
+    if (i < nch || bad) {
+      if (lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    } else {
+      report_nonfinite(nonfinite, dev_err);
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  // no CTA of the cluster leaves while another may still send it row sums
+  if constexpr (kGated) tc::cluster_sync_all();
 }
 
 // ------------------------------------------------------- wide chain kernel
@@ -1523,12 +1677,33 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
     // `buf`, with the optional output epilogue: each o warp publishes its 32
     // columns' sum of squares per row, the row's total over the NC/32 column
     // groups gives the RMS, then the weight and the Sigmoid gate scale the row
-    // (loaded where used: at this kernel's register limit, holding them longer
-    // spilled and measured slower).
+    // (the gate logits are loaded where used, at this kernel's register limit
+    // holding them longer spilled and measured slower; they are prefetched into
+    // L2 kGatePf chunks ahead and into L1 a chunk ahead).
+    constexpr int kGatePf = 3;
     float nonfinite = 0.f;   // stays 0 unless an o or state value is inf or NaN (x * 0 is then NaN)
+    auto prefetch_gate = [&](int j, bool l1) {
+      const int64_t t0 = seq_start + (int64_t)j * C;
+      const int r = c - 64;
+      if (j < nch && r < seq_end - t0) {
+        const bf16* gp = ep.gate + ((t0 + r) * H + h) * DV + n0 + 32 * cg;
+        if (l1) asm volatile("prefetch.global.L1 [%0];" ::"l"(gp));
+        else asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
+      }
+    };
+    if constexpr (kGated) {
+      if (q >= 2) {
+        for (int j = 0; j < kGatePf; ++j) prefetch_gate(j, false);
+        prefetch_gate(0, true);
+      }
+    }
     auto emit_o = [&](uint32_t buf, int64_t t0, int64_t len, int j) -> bool {
       const int r = c - 64;
       float sc = 1.f;
+      if constexpr (kGated) {   // the next chunk's gate rows into L1, a later one's into L2
+        prefetch_gate(j + 1, true);
+        prefetch_gate(j + kGatePf, false);
+      }
       if constexpr (kGated) {   // first pass over TMEM: this warp's share of the row's sum of squares
         float ss = 0.f;
 #pragma unroll
@@ -1742,6 +1917,39 @@ bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The 32-column chain: with the output epilogue (kGated) the DV/32 CTAs of a head
+// (consecutive blocks) form one thread-block cluster.
+template <int DV, bool kGated>
+cudaError_t launch_chain_narrow(const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
+                                const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
+                                const ChunkMap& map, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(chunk_chain_tc<DV, kGated>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ChainTcSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.num_seqs * p.H * (DV / BV), 1, 1);
+  cfg.blockDim = dim3(chain_threads(kGated), 1, 1);
+  cfg.dynamicSmemBytes = ChainTcSmem::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (kGated) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = DV / BV;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const OutEpilogue ep = kGated ? OutEpilogue{static_cast<const bf16*>(p.out_gate), p.norm_weight, p.eps_rms}
+                                : OutEpilogue{nullptr, nullptr, 0.f};
+  prof_begin(stream, kGated ? "chunk_chain_tc_gated" : "chunk_chain_tc");
+  e = cudaLaunchKernelEx(&cfg, chunk_chain_tc<DV, kGated>, mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H,
+                         map, p.s0, p.s_final, static_cast<bf16*>(p.o), ep, p.dev_err);
+  prof_end(stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int DV, int NC, bool kGated>
 cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, const CUtensorMap& mKT,
                                  const CUtensorMap& mU, const CUtensorMap& mGam, const ChunkProblem& p,
@@ -1845,15 +2053,8 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (wide) return launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
-  if (p.out_gate) return launch_chain_transition_gated(mWQ, mP, mKT, mU, mGam, p, map, stream);
-  const unsigned n_ctas = (unsigned)p.num_seqs * p.H * (DV / BV);
-  e = cudaFuncSetAttribute(chunk_chain_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainTcSmem::kAlloc);
-  if (e != cudaSuccess) return e;
-  prof_begin(stream, "chunk_chain_tc");
-  chunk_chain_tc<DV><<<n_ctas, kChainTcThreads, ChainTcSmem::kAlloc, stream>>>(
-      mWQ, mP, mKT, mU, mGam, p.cu, p.num_seqs, p.T_seq, p.H, map, p.s0, p.s_final, static_cast<bf16*>(p.o), p.dev_err);
-  prof_end(stream);
-  return cudaGetLastError();
+  return p.out_gate ? launch_chain_narrow<DV, true>(mWQ, mP, mKT, mU, mGam, p, map, stream)
+                    : launch_chain_narrow<DV, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
 }
 
 }  // namespace

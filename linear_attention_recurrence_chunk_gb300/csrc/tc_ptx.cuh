@@ -84,51 +84,6 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Store to a (possibly remote) cluster shared-memory address from mapa_shared.
-__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// Asynchronous 4-byte store to a (possibly remote) cluster shared-memory address
-// that, once written, counts its bytes on an mbarrier of the same CTA (both
-// addresses from mapa_shared): the receiver's wait on that barrier sees the
-// data, with no fence on the sender's side.
-__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(remote_addr), "f"(v),
-               "r"(remote_bar)
-               : "memory");
-}
-
-// Arrive on an mbarrier of a (possibly remote) CTA of the cluster, with
-// release semantics at cluster scope (orders this thread's earlier writes,
-// and those it has observed, before the arrival).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-
-// Bounded wait for a phase of a local mbarrier that CTAs of the cluster arrive
-// on, with acquire semantics at cluster scope.  Returns false after
-// `limit_cycles`.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit_cycles) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait_cluster(bar, parity)) {
-    if (clock64() - t0 > limit_cycles) return false;
-  }
-  return true;
-}
-
 // Every thread of every CTA of the cluster arrives, then waits for all of
 // them (a hardware barrier like __syncthreads, at cluster scope).
 __device__ __forceinline__ void cluster_sync_all() {
@@ -138,17 +93,6 @@ __device__ __forceinline__ void cluster_sync_all() {
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-// 2D tiled load of the box at (x = inner coordinate, y) into shared memory;
-// completion is counted in bytes on `bar`.  x * element size must be a
-// multiple of 16 bytes.
-// Prefetch of a 2D tile into L2 (no shared-memory destination, no completion
-// to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
@@ -247,19 +191,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-// 16 consecutive 32-bit columns of this thread's lane written from registers
-// (warp w writes lanes 32*(w%4) .. +31); tmem_st_wait() waits for the warp's
-// stores to complete.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor of a K-major bf16 operand laid out in the
@@ -377,25 +308,6 @@ __device__ __forceinline__ void mma_16bit_acc(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-// Same with the A operand already in TMEM (lane = row, 16-bit K elements packed
-// two per column, a K = 16 slice spanning 8 columns).
-__device__ __forceinline__ void mma_16bit_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Asynchronous copy of a 128-row x 32-byte (one K = 16 slice of 16-bit values)
-// operand slice, described by a shared-memory matrix descriptor, into TMEM.
-// Ordered with the MMAs issued later by the same thread.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t src_desc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
-}
-
 // Warp-level forms: executed by all 32 lanes of a warp with warp-uniform
 // operands; elect.sync picks one lane (always the same one, lane 0, when the
 // whole warp is active) to issue.  Keeping the operands uniform across the
@@ -411,19 +323,6 @@ __device__ __forceinline__ void mma_16bit_w(uint32_t d_tmem, uint64_t a_desc, ui
       "elect.sync _|pe, 0xffffffff;\n\t"
       "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Whole-warp form with the A operand in TMEM (16-bit K elements packed two per
-// column, lower K index in the low half; a K = 16 slice spans 8 columns).
-__device__ __forceinline__ void mma_16bit_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, pe;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|pe, 0xffffffff;\n\t"
-      "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
