@@ -58,6 +58,7 @@
 #include <cstdlib>
 #include "tc_ptx.cuh"
 #include "chain_common.cuh"
+#include "chain_vm.cuh"
 
 namespace kda {
 namespace {
@@ -1500,7 +1501,8 @@ __global__ void __launch_bounds__(chain_threads(kGated), 1)
 // The same inter-chunk pass with NC = 64 or 128 value columns per CTA: the
 // per-chunk A tiles are read and the MMAs issued once per NC columns instead
 // of once per 32.  Used when the 32-column grid would exceed one wave of the
-// GPU.  Consumer warp w reads TMEM lanes 32(w%4)..+31 and value columns
+// GPU and the value-major chain does not apply (d_v = 64, or the output
+// epilogue fused), and for a forced 64-column width.  Consumer warp w reads TMEM lanes 32(w%4)..+31 and value columns
 // 32(w/4)..+31 of the block; the state block and V_new are MN-major B operands
 // of NC/32 atoms of 32 columns.
 template <int NC>
@@ -1903,17 +1905,19 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, void* base, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3D tensor map over a token-major [tokens][H][inner] bf16 input, one box =
-// 64 tokens of one head.
-bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H, uint64_t tokens) {
+// 3D tensor map over a token-major [tokens][H][inner] bf16 array, one box =
+// 64 tokens of one head and box_inner of its inner elements: the inputs (whole
+// rows, no swizzle) and the output o (64-value boxes, 128-byte swizzle).
+bool make_input_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t H, uint64_t tokens,
+                    uint32_t box_inner = 0, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {inner, H, tokens};
   const cuuint64_t strides[2] = {inner * 2, H * inner * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)C};
+  const cuuint32_t box[3] = {box_inner ? box_inner : (cuuint32_t)inner, 1, (cuuint32_t)C};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1969,12 +1973,12 @@ cudaError_t launch_chain_wide_nc(const CUtensorMap& mWQ, const CUtensorMap& mP, 
 }
 
 template <int DV>
-cudaError_t launch_chain_wide(int ncol, bool fuse_epilogue, const CUtensorMap& mWQ, const CUtensorMap& mP,
+cudaError_t launch_chain_wide(bool fuse_epilogue, const CUtensorMap& mWQ, const CUtensorMap& mP,
                               const CUtensorMap& mKT, const CUtensorMap& mU, const CUtensorMap& mGam,
                               const ChunkProblem& p, const ChunkMap& map, cudaStream_t stream) {
+  // (all 128 value columns without the epilogue run in the value-major chain)
   constexpr int kFull = DV == 128 ? 128 : 64;
   if (fuse_epilogue) return launch_chain_wide_nc<DV, kFull, true>(mWQ, mP, mKT, mU, mGam, p, map, stream);
-  if (DV == 128 && ncol == 128) return launch_chain_wide_nc<DV, kFull, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
   return launch_chain_wide_nc<DV, 64, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
 }
 
@@ -2027,7 +2031,9 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   // Chain variant: 32 value columns per CTA (the most CTAs, for few long
   // chains) unless that grid exceeds one wave of the GPU; then one CTA per
   // (sequence, head) with all DV columns, which reads the per-chunk tiles and
-  // issues the MMAs once per head.  KDA_CHAIN_COLUMNS=32, 64 or DV forces a width.
+  // issues the MMAs once per head: the value-major chain for d_v = 128 without
+  // the output epilogue, the wide chain otherwise.  KDA_CHAIN_COLUMNS=32, 64 or
+  // DV forces a width.
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -2037,9 +2043,9 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
     if (cols == BV || cols == 64 || cols == DV) ncol = cols;
   }
   // The output epilogue needs a token's d_v outputs: fused into the chain, either
-  // the transition-form 32-column chain (the CTAs of a head exchange row sums
-  // within their cluster) or one CTA holding all d_v columns (the 64-column wide
-  // form is not used with it).
+  // the 32-column chain (the CTAs of a head exchange row sums within their
+  // cluster) or the wide chain holding all d_v columns (the 64-column width is
+  // not used with it).
   if (p.out_gate && ncol != BV) ncol = DV;
   const bool fuse = p.out_gate && ncol == DV;
   const bool wide = ncol != BV;
@@ -2052,7 +2058,14 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
                 wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (wide) return launch_chain_wide<DV>(ncol, fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
+  if (DV == 128 && ncol == DV && !p.out_gate) {
+    CUtensorMap mO = {};   // o rows by TMA store: 64 tokens x 64 values per box (unused without tokens)
+    if (p.total_tokens > 0 &&
+        !make_input_map(&mO, p.o, DV, p.H, (uint64_t)p.total_tokens, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    return launch_chain_vm(mWQ, mP, mKT, mU, mGam, mO, p, map, stream);
+  }
+  if (wide) return launch_chain_wide<DV>(fuse, mWQ, mP, mKT, mU, mGam, p, map, stream);
   return p.out_gate ? launch_chain_narrow<DV, true>(mWQ, mP, mKT, mU, mGam, p, map, stream)
                     : launch_chain_narrow<DV, false>(mWQ, mP, mKT, mU, mGam, p, map, stream);
 }
