@@ -6,21 +6,22 @@
 // §3.3, chunked prefill with the state carried across chunk boundaries) are
 // taken transposed, value column = TMEM lane:
 //
-//   group 1:  D1[:, 0:64]   = u^T I - S^T w^T    (M = 128 values, N = 64 tokens, K = 64, then d_k)
-//             D1[:, 64:128] = S^T (q e^G)^T       (N = 64 rows, K = d_k)
-//             V_new^T = D1[:, 0:64], to fp16       (threads)
+//   group 1:  VN   = -S^T w^T + u^T I          (M = 128 values, N = 64 tokens, K = d_k, then 64)
+//             V_new^T = VN, to fp16               (threads)
 //   group 2:  D3   = V_new^T K~                  (M = 128, N = d_k, K = 64 tokens)
-//             D1[:, 64:128] += V_new^T P^T        (the o rows)
+//             O    = -S^T (q e^G)^T - V_new^T P^T (the o rows, negated; N = 64)
 //             S^T  = S^T Diag(e^{G_last}) + D3   (threads, fp32 in registers)
 //
 // so that both operands the threads produce, S^T and V_new^T, are the A
 // operands of the next products and go straight back into TMEM (tcgen05.st)
 // instead of through shared memory: each hand-off is a TMEM read, a rounding
 // to fp16 (and for the state the decay and sum), a TMEM write and an mbarrier
-// arrive.  u enters the accumulator through a product with the identity (u as
-// an MN-major A operand, as stored), and w S is subtracted by the same
-// accumulation with the instruction's negate-B flag, so V_new = u - w S is
-// formed in fp32 and rounded to fp16 once.  The records are read as the other
+// arrive.  The products that need a minus sign take the instruction's negate-B
+// flag, u enters the accumulator through a product with the identity (u as an
+// MN-major A operand, as stored), so V_new = u - w S is formed in fp32 and
+// rounded to fp16 once, and the o rows come out negated.  The o product, off
+// the chain's path, runs after the state product, from its own copy of S^T
+// (two TMEM buffers, by chunk parity).  The records are read as the other
 // chains read them: [w; q e^G] (rows x keys), P (rows x tokens) and K~^T
 // (keys x tokens) are K-major B operands as stored.
 //
@@ -64,9 +65,10 @@ constexpr int kSlotsA = 3, kSlotsB = 2;
 constexpr int kGamSlots = 4;   // e^{G_last} ring: a chunk's factors stay until its state update has used them
 
 // TMEM columns (512 allocated)
-constexpr uint32_t kD1 = 0;      // two buffers of 128 (chunk parity): V_new^T in 0-63, o^T in 64-127
-constexpr uint32_t kD3 = 256;    // (K~^T V_new)^T, 128 columns
-constexpr uint32_t kSA = 384;    // S^T as the fp16 A operand: 64 columns (pairs of keys)
+constexpr uint32_t kVN = 0;      // V_new^T, 64 columns (fp32)
+constexpr uint32_t kO = 64;      // two buffers of 64 (chunk parity): -o^T
+constexpr uint32_t kD3 = 192;    // (K~^T V_new)^T, 128 columns
+constexpr uint32_t kSA = 320;    // two buffers of 64 (chunk parity): S^T as the fp16 A operand (pairs of keys)
 constexpr uint32_t kVA = 448;    // V_new^T as the fp16 A operand: 32 columns (pairs of tokens)
 constexpr uint32_t kTmemCols = 512;
 
@@ -100,22 +102,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                       int32_t* dev_err) {
   using L = VmSmem;
   constexpr uint32_t kIdN64 = tc::idesc_f16_f32(128, 64), kIdN128 = tc::idesc_f16_f32(128, 128);
-  constexpr uint32_t kIdU = kIdN64 | (1u << 15);     // u^T I: A (u) MN-major
-  constexpr uint32_t kIdNegW = kIdN64 | (1u << 14);  // - S^T w^T: B negated
+  constexpr uint32_t kIdU = kIdN64 | (1u << 15);       // u^T I: A (u) MN-major
+  constexpr uint32_t kIdNeg64 = kIdN64 | (1u << 14);    // B negated
   if (map.seq_chunk0[num_seqs] < 0) return;   // malformed cu_seqlens: write nothing
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + L::oBar);   // [3] a ring-A slot has landed
-  uint64_t* emptyA = fullA + 3;    // [3] group 1 is done with a ring-A slot
+  uint64_t* emptyA = fullA + 3;    // [3] the products are done with a ring-A slot
   uint64_t* fullB = fullA + 6;     // [2] a ring-B slot (and its e^{G_last}) has landed
   uint64_t* emptyB = fullA + 8;    // [2] group 2 is done with a ring-B slot
-  uint64_t* mma1 = fullA + 10;     // V_new^T complete in its D1 buffer
+  uint64_t* mma1 = fullA + 10;     // group 1 complete: V_new^T in VN
   uint64_t* mma2 = fullA + 11;     // the state product complete
   uint64_t* drain = fullA + 12;    // every MMA complete (kernel end)
   uint64_t* vn_ready = fullA + 13; // the consumer warps have written V_new^T
   uint64_t* s_ready = fullA + 14;  // the consumer warps have written S^T (and read D3)
-  uint64_t* ofull = fullA + 15;    // [2] a chunk's o^T is complete in its D1 buffer
-  uint64_t* ofree = fullA + 17;    // [2] the o warps have read a D1 buffer
+  uint64_t* ofull = fullA + 15;    // [2] a chunk's -o^T is complete in its O buffer
+  uint64_t* ofree = fullA + 17;    // [2] the o warps have read an O buffer
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::oTmem);
 
   // one-dimensional grid, sequence-rank major: all heads of the longest sequence first
@@ -216,40 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(b, parity, kWaitLimit));
     };
-    // u^T I of chunk j into its D1 buffer (columns 0-63), once its ring-A slot has landed
-    auto issue_u = [&](int j) -> bool {
-      const int sl = j % kSlotsA;
-      if (!wait_all(fullA + sl, (j / kSlotsA) & 1)) return false;
-      tc::tc_fence_after();
-      const uint64_t dU = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sm + sl * L::kSlotA + L::kAU), 8192);
-#pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)
-        tc::mma_16bit_w(tmem + kD1 + (uint32_t)(j & 1) * 128, dU + ((kk * 2048) >> 4), dI + ((kk * 32) >> 4), kIdU,
-                        kk > 0);
-      return true;
-    };
-    bool ok = nch == 0 || issue_u(0), issued = nch > 0 && ok;
+    bool ok = true, issued = false;
     for (int i = 0; i < nch && ok; ++i) {
       const int sa = i % kSlotsA, sb = i & 1;
       const uint32_t b = (uint32_t)(i & 1);
-      const uint32_t d1 = tmem + kD1 + b * 128;
+      const uint32_t sA = tmem + kSA + b * 64;   // this chunk's S^T
       const uint64_t dWQ = dSm + ((uint64_t)(sa * L::kSlotA) >> 4);
-      ok = wait_all(s_ready, i & 1);
+      ok = wait_all(s_ready, i & 1) && wait_all(fullA + sa, (i / kSlotsA) & 1);
       if (!ok) break;
       tc::tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < DK / 16; ++kk)   // group 1: V_new^T = u^T - S^T w^T
-        tc::mma_16bit_tw(d1, tmem + kSA + 8 * kk, dWQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdNegW, 1u);
+      for (int kk = 0; kk < DK / 16; ++kk)   // group 1: -S^T w^T
+        tc::mma_16bit_tw(tmem + kVN, sA + 8 * kk, dWQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdNeg64, kk > 0);
+      const uint64_t dU = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sm + sa * L::kSlotA + L::kAU), 8192);
+#pragma unroll
+      for (int kk = 0; kk < C / 16; ++kk)    // + u^T I
+        tc::mma_16bit_w(tmem + kVN, dU + ((kk * 2048) >> 4), dI + ((kk * 32) >> 4), kIdU, 1u);
       tc::mma_commit_w(mma1);
-      // the o rows S^T (q e^G)^T, once the o warps have read this buffer's previous chunk
-      ok = i < 2 || wait_all(ofree + b, ((i >> 1) - 1) & 1);
-      if (!ok) break;
-      tc::tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < DK / 16; ++kk)
-        tc::mma_16bit_tw(d1 + 64, tmem + kSA + 8 * kk, dWQ + ((8192 + (kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                         kIdN64, kk > 0);
-      tc::mma_commit_w(emptyA + sa);
+      issued = true;
       ok = wait_all(vn_ready, i & 1) && wait_all(fullB + sb, (i >> 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
@@ -258,14 +244,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < C / 16; ++kk)   // group 2: the state product first, it is on the chain's path
         tc::mma_16bit_tw(tmem + kD3, tmem + kVA + 8 * kk, dKT + ((kk * 32) >> 4), kIdN128, kk > 0);
       tc::mma_commit_w(mma2);
+      // the o rows, once the o warps have read this buffer's previous chunk:
+      // -S^T (q e^G)^T from this chunk's copy of S^T (the state update writes the
+      // other one), then -V_new^T P^T
+      ok = i < 2 || wait_all(ofree + b, ((i >> 1) - 1) & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint32_t dO = tmem + kO + b * 64;
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)   // then the o rows: += V_new^T P^T
-        tc::mma_16bit_tw(d1 + 64, tmem + kVA + 8 * kk, dKT + ((L::kBP + kk * 32) >> 4), kIdN64, 1u);
+      for (int kk = 0; kk < DK / 16; ++kk)
+        tc::mma_16bit_tw(dO, sA + 8 * kk, dWQ + ((8192 + (kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdNeg64, kk > 0);
+      tc::mma_commit_w(emptyA + sa);
+#pragma unroll
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit_tw(dO, tmem + kVA + 8 * kk, dKT + ((L::kBP + kk * 32) >> 4), kIdNeg64, 1u);
       tc::mma_commit_w(ofull + b);
       tc::mma_commit_w(emptyB + sb);
-      // the next chunk's u^T I (its buffer's V_new^T of chunk i - 1 was read before
-      // this chunk's V_new hand-off) runs while the state is updated
-      if (i + 1 < nch) ok = issue_u(i + 1);
     }
     if (!ok && lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
     if (issued) {
@@ -281,14 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t sbase = ((int64_t)s * H + h) * DK * DV + (int64_t)(32 * part) * DV + c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) S[j] = s0 ? s0[sbase + (int64_t)j * DV] : 0.f;
-    // S^T into TMEM as the fp16 A operand (key pairs per column)
-    auto write_sa = [&]() {
+    // S^T into TMEM buffer `buf` as the fp16 A operand (key pairs per column)
+    auto write_sa = [&](uint32_t buf) {
       uint32_t w[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m) w[m] = pack_f16x2(S[2 * m], S[2 * m + 1]);
-      tc::tmem_st16(tc::tmem_addr(tmem, tl, kSA + 16 * part), w);
+      tc::tmem_st16(tc::tmem_addr(tmem, tl, kSA + 64 * buf + 16 * part), w);
     };
-    write_sa();
+    write_sa(0);
     tc::tmem_st_wait();
     tc::tc_fence_before();
     __syncwarp();
@@ -314,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // V_new^T (fp32, tokens 16 part .. +15) to fp16 pairs, as the A operand of group 2
       {
         float d[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kD1 + b * 128 + 16 * part), d);
+        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kVN + 16 * part), d);
         uint32_t vw[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) vw[m] = pack_f16x2(d[2 * m], d[2 * m + 1]);
@@ -330,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::tc_fence_after();
-      // S^T = S^T Diag(e^{G_last}) + D3 for the warp's 32 keys, then its fp16 copy into TMEM
+      // S^T = S^T Diag(e^{G_last}) + D3 for the warp's 32 keys, then its fp16 copy
+      // into the next chunk's buffer
       const float* gam = reinterpret_cast<const float*>(sm + L::oGam + (i % kGamSlots) * DK * 4) + 32 * part;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
@@ -345,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           S[16 * g + 4 * e4 + 3] = fmaf(gv.w, S[16 * g + 4 * e4 + 3], d[4 * e4 + 3]);
         }
       }
-      write_sa();
+      write_sa(b ^ 1u);
       tc::tmem_st_wait();
       tc::tc_fence_before();
       __syncwarp();
@@ -375,14 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kOWarp0 + kOWarps) {
     // ---------------- o warps
-    // Each chunk: o^T out of TMEM (this warp's 32 value lanes, 64 tokens) as bf16
-    // into the two staging boxes (the layout of a TMA store), the D1 buffer
-    // released; then, after a barrier of the four o warps, a full chunk leaves
+    // Each chunk: o^T out of TMEM (this warp's 32 value lanes, 64 tokens, in 16 x 8
+    // blocks) as bf16 into the two staging boxes (the layout of a TMA store, by
+    // transposing 8 x 8 matrix stores), the O buffer released; then, after a
+    // barrier of the four o warps, a full chunk leaves
     // by two TMA stores, and a sequence's last, partial chunk row by row (thread
     // ot writes the 8 values 8 (ot % 16) .. +7 of rows 8 j + ot / 16: 16 lanes
     // per 256-byte row).
-    const int q = warp & 3, c = 32 * q + lane;
-    const uint32_t tl = (uint32_t)(32 * q);
+    const int q = warp & 3;
     const int ot = tid - 32 * kOWarp0, g8 = ot & 15, r0 = ot >> 4;
     uint8_t* stile = sm + L::oO;
     // byte offset of (token t, value v) in the staging boxes: box v / 64, 16-byte chunk (v % 64) / 8 ^ t % 8
@@ -410,14 +405,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tc_fence_after();
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
-        float v[16];
-        tc::tmem_ld16(tc::tmem_addr(tmem, tl, kD1 + b * 128 + 64 + 16 * part), v);
+      for (int hl = 0; hl < 2; ++hl) {   // value lanes 32 q + 16 hl .. +15
+        float v[32];
+        tc::tmem_ld_16x256b_x8(tc::tmem_addr(tmem, (uint32_t)(32 * q + 16 * hl), kO + b * 64), v);
+        // o (the accumulator holds -o) as bf16 pairs of consecutive tokens: the 8 x 8
+        // blocks [8 values][8 tokens] of token block tb, value half vh in pk[2 tb + vh]
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          nonfinite = fmaf(v[e], 0.f, nonfinite);
-          *reinterpret_cast<bf16*>(stile + soff(16 * part + e, c)) = __float2bfloat16_rn(v[e]);
+        for (int tb = 0; tb < 8; ++tb) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) nonfinite = fmaf(v[4 * tb + e], 0.f, nonfinite);
+          pk[2 * tb] = pack_bf16x2(-v[4 * tb], -v[4 * tb + 1]);
+          pk[2 * tb + 1] = pack_bf16x2(-v[4 * tb + 2], -v[4 * tb + 3]);
         }
+        // stored transposed (token rows of 8 values): call sc takes token blocks
+        // 2 sc, 2 sc + 1; lane L gives the address of row L % 8 of block L / 8
+        const int mL = lane >> 3, rL = lane & 7;
+#pragma unroll
+        for (int sc = 0; sc < 4; ++sc)
+          tc::stmatrix_x4_trans(tc::smem_u32(stile + soff(8 * (2 * sc + (mL >> 1)) + rL, 32 * q + 16 * hl + 8 * (mL & 1))),
+                                pk[4 * sc], pk[4 * sc + 1], pk[4 * sc + 2], pk[4 * sc + 3]);
       }
       tc::tc_fence_before();
       __syncwarp();
