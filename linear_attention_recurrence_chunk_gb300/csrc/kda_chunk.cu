@@ -458,7 +458,8 @@ Workspace chunk_workspace_layout(int64_t total_tokens, int32_t num_seqs, int32_t
     w.off_kt = w.off_p + align256(R * kChunk * kChunk * 2);
     w.off_u = w.off_kt + align256(R * d_k * kChunk * 2);
     w.off_gam = w.off_u + align256(R * kChunk * d_v * 2);
-    w.bytes = w.off_gam + align256(R * d_k * 4);
+    w.off_flags = w.off_gam + align256(R * d_k * 4);
+    w.bytes = w.off_flags + align256(R * 4);
   } else {
     w.bytes = w.off_inter + align256(w.inter_bytes_per_chunk_head * R);
   }

@@ -59,6 +59,7 @@
 #include "tc_ptx.cuh"
 #include "chain_common.cuh"
 #include "chain_vm.cuh"
+#include "chain_vm_body.cuh"
 
 namespace kda {
 namespace {
@@ -258,14 +259,25 @@ __device__ __forceinline__ uint32_t opnd_off(int rows, int row, int ch) {
 }
 
 
+// Record publication for the fused kernel: a release store of 1 into the
+// record's flag once every store of the record has completed (the TMA stores
+// by the bulk-group wait, the threads' stores by the CTA barriers since).
+__device__ __forceinline__ void publish_record(int32_t* flag) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+
+// One CTA's share of the prep tasks, cta + i * ncta (chunk-major), run by the
+// whole CTA.  With `ready`, each record is published (publish_record) two tasks
+// of this CTA later, when its [w | u] stores, issued a task later, are complete.
 template <int DV, int kVariant>
-__global__ void __launch_bounds__(kPrepTcThreads, 1)
-    chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
-                  const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
-                  const __grid_constant__ CUtensorMap tmPs,
-                  const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
-                  int64_t n_tasks, int32_t* __restrict__ dev_err) {
+__device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensorMap& tmK, const CUtensorMap& tmQ,
+                                          const CUtensorMap& tmV, const CUtensorMap& tmWs, const CUtensorMap& tmUs,
+                                          const CUtensorMap& tmPs, const float* __restrict__ beta, int32_t num_seqs,
+                                          int32_t H, const ChunkMap& map, const TcRecords& out, int64_t n_tasks,
+                                          int32_t* __restrict__ dev_err, int cta, int ncta,
+                                          int32_t* __restrict__ ready) {
   using L = PrepTcSmem<DV, kVariant>;
   constexpr int LDX = L::LDX, LDA = L::LDA;
   constexpr bool kPairs = L::kPairs, kSoftplus = kVariant == kPrepSoftplusPairs;
@@ -325,6 +337,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   // stores to the record with TMA; the tiles are released (bulk read wait)
   // before that area is rewritten.
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
+  int64_t pub_rec = -1;                             // thread 0: the next record to publish (with `ready`)
   uint32_t wu_parity = 0, ap_parity = 0;
   int64_t wu_rec = 0;
   // Returns the OR over the CTA of `raw_bad` (taken at the drain's CTA
@@ -356,6 +369,13 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     tc::fence_proxy_async_smem();   // the tiles, written by the threads, read by the TMA unit
     tc::tc_fence_before();
     const bool any_raw_bad = __syncthreads_or(raw_bad);
+    if (ready && tid == 0) {   // the record two tasks back is complete once all but the last group are
+      if (pub_rec >= 0) {
+        tc::bulk_wait1();
+        publish_record(ready + pub_rec);
+      }
+      pub_rec = wu_rec;   // complete once its [w | u] stores, issued below, are
+    }
     if (tid == 0 && okw) {
 #pragma unroll
       for (int t = 0; t < L::kWuN / 64; ++t) {
@@ -371,11 +391,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     return any_raw_bad;
   };
 
-  // This CTA's tasks are blockIdx.x + i * gridDim.x; (chunk, head) of the
+  // This CTA's tasks are cta + i * ncta; (chunk, head) of the
   // next two are tracked incrementally, without 64-bit divisions.
   const int32_t n_chunks = map.seq_chunk0[num_seqs];   // negative after malformed cu_seqlens
-  const int32_t dj = (int32_t)(gridDim.x / (unsigned)H), dh = (int32_t)(gridDim.x % (unsigned)H);
-  int32_t j_next = (int32_t)(blockIdx.x / (unsigned)H), h_next = (int32_t)(blockIdx.x % (unsigned)H);
+  const int32_t dj = (int32_t)((unsigned)ncta / (unsigned)H), dh = (int32_t)((unsigned)ncta % (unsigned)H);
+  int32_t j_next = (int32_t)((unsigned)cta / (unsigned)H), h_next = (int32_t)((unsigned)cta % (unsigned)H);
   auto advance = [&](int32_t& jt, int32_t& ht) {
     jt += dj;
     ht += dh;
@@ -409,11 +429,11 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   auto load_beta = [&](int32_t ht, int4 ci) -> float {
     return (tid < ci.y) ? ld_early_f32(beta + ((int64_t)(uint32_t)ci.z + tid) * H + ht) : 0.f;   // ci.y <= 64
   };
-  int4 ci_next = fetch(blockIdx.x, j_next);
+  int4 ci_next = fetch(cta, j_next);
   float beta_next = tid < C ? load_beta(h_next, ci_next) : 0.f;
   int32_t j_next2 = j_next, h_next2 = h_next;
   advance(j_next2, h_next2);
-  int4 ci_next2 = fetch((int64_t)blockIdx.x + gridDim.x, j_next2);
+  int4 ci_next2 = fetch((int64_t)cta + ncta, j_next2);
   arm(ci_next);
   __syncthreads();
   issue(h_next, ci_next);
@@ -421,7 +441,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
 
   bool failed = false;
   // Persistent: tasks (chunk j, head h) in chunk-major order, strided over the grid.
-  for (int64_t task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+  for (int64_t task = cta; task < n_tasks; task += ncta) {
     const int4 ci = ci_next;
     const float beta_cur = beta_next;
     ci_next = ci_next2;   // the next task (record fetched a task ago)
@@ -429,7 +449,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
     h_next = h_next2;
     if (tid < C) beta_next = load_beta(h_next, ci_next);
     advance(j_next2, h_next2);
-    ci_next2 = fetch(task + 2 * (int64_t)gridDim.x, j_next2);
+    ci_next2 = fetch(task + 2 * (int64_t)ncta, j_next2);
     if (ci.y <= 0) {
       arm(ci_next);
       __syncthreads();
@@ -1024,10 +1044,23 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   wu_drain(false);   // the last task's [w | u]
   if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
   if (bulk_pending) tc::bulk_wait0();   // thread 0: every record store has completed
+  if (ready && tid == 0 && pub_rec >= 0) publish_record(ready + pub_rec);
   (void)failed;
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int DV, int kVariant>
+__global__ void __launch_bounds__(kPrepTcThreads, 1)
+    chunk_prep_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
+                  const __grid_constant__ CUtensorMap tmPs,
+                  const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
+                  int64_t n_tasks, int32_t* __restrict__ dev_err) {
+  prep_body<DV, kVariant>(tmG, tmK, tmQ, tmV, tmWs, tmUs, tmPs, beta, num_seqs, H, map, out, n_tasks, dev_err,
+                          (int)blockIdx.x, (int)gridDim.x, nullptr);
 }
 
 // -------------------------------------------------------------- chain kernel
@@ -1878,6 +1911,37 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, L::kTmemCols);
 }
 
+// ------------------------------------------------------------- fused kernel
+// Prep and the value-major chain in one persistent launch (cooperative, one
+// CTA per SM, so that every CTA is resident at once): CTAs 0 .. n_chain-1 run
+// the chains of the (sequence, head) pairs, each loading a chunk's record only
+// once it has been published; the other CTAs run the prep tasks in chunk-major
+// order and publish each record when its stores have completed.  The chains
+// then trail prep by a few chunks (their records still in L2) instead of
+// waiting for the whole prep pass, and prep never waits for a chain, so every
+// wait ends.
+__global__ void __launch_bounds__(kPrepTcThreads, 1)
+    chunk_fused_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
+                   const __grid_constant__ CUtensorMap tmPs, const __grid_constant__ CUtensorMap tmWQ,
+                   const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmKT,
+                   const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmGam,
+                   const __grid_constant__ CUtensorMap tmO, const float* __restrict__ beta,
+                   const int32_t* __restrict__ cu, int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map,
+                   TcRecords out, int64_t n_tasks, const float* __restrict__ s0, float* __restrict__ s_final,
+                   bf16* __restrict__ o, int32_t* __restrict__ dev_err, int32_t* __restrict__ ready, int32_t n_chain) {
+  static_assert(vm::VmWarps<8>::kThreads <= kPrepTcThreads, "the chain role fits the prep CTA");
+  if ((int)blockIdx.x < n_chain)
+    vm::chain_body<8>(tmWQ, tmP, tmKT, tmU, tmGam, tmO, cu, num_seqs, T_seq, H, map, s0, s_final, o, dev_err,
+                      (int)blockIdx.x, ready);
+  else
+    prep_body<128, kPrepBounded>(tmG, tmK, tmQ, tmV, tmWs, tmUs, tmPs, beta, num_seqs, H, map, out, n_tasks, dev_err,
+                                 (int)blockIdx.x - n_chain, (int)gridDim.x - n_chain, ready);
+}
+constexpr size_t kFusedSmem =
+    PrepTcSmem<128, kPrepBounded>::kAlloc > vm::VmSmem::kAlloc ? PrepTcSmem<128, kPrepBounded>::kAlloc : vm::VmSmem::kAlloc;
+
 // --------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1992,7 +2056,29 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   rec.u = reinterpret_cast<f16*>(base + ws.off_u);
   rec.gam = reinterpret_cast<float*>(base + ws.off_gam);
   const uint64_t R = (uint64_t)ws.max_chunks * (uint64_t)p.H;
+  const uint64_t Rr = R > 0 ? R : 1;
   cudaError_t e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // The records as the chains read them: [w; q e^G] boxes of 64 x 128, P of 64 x 64,
+  // (k e^{G_last - G})^T of 64 x 128, u of u_cols x 64, e^{G_last} of 128 x 1.
+  CUtensorMap mWQ, mP, mKT, mU, mGam;
+  auto chain_maps = [&](uint32_t u_cols) -> bool {
+    return make_map(&mWQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, Rr * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&mP, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, Rr * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&mKT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.kt, C, Rr * DK, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, u_cols, 64,
+                    u_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+           make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  };
+  // Prep and the value-major chain fused (chunk_fused_tc) when the (sequence, head)
+  // chains are few enough to leave most SMs to prep: d_v = 128, the plain call,
+  // the bounded map.  KDA_FUSED=0, or a forced chain width, runs the two passes.
+  const int64_t n_chain = (int64_t)p.num_seqs * p.H;
+  bool fused = DV == 128 && !p.out_gate && p.decay_map == KDA_DECAY_BOUNDED && !p.diag_pairs && ws.max_chunks > 0 &&
+               p.total_tokens > 0 && n_chain <= sms / 4 && !std::getenv("KDA_CHAIN_COLUMNS");
+  if (const char* env = std::getenv("KDA_FUSED")) fused = fused && std::atoi(env) != 0;
   if (ws.max_chunks > 0 && p.total_tokens > 0) {
     CUtensorMap mG, mK, mQ, mV;
     const uint64_t tok = (uint64_t)p.total_tokens;
@@ -2004,10 +2090,36 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
         !make_map(&mUs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&mPs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, R * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t n_tasks = (int64_t)ws.max_chunks * p.H;
+    if constexpr (DV == 128) {
+      if (fused) {
+        CUtensorMap mO;   // o rows by TMA store: 64 tokens x 64 values per box
+        if (!chain_maps(64) || !make_input_map(&mO, p.o, DV, p.H, tok, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+          return cudaErrorInvalidValue;
+        int32_t* flags = reinterpret_cast<int32_t*>(base + ws.off_flags);
+        if ((e = cudaMemsetAsync(flags, 0, R * sizeof(int32_t), stream)) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(chunk_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmem)) !=
+            cudaSuccess)
+          return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)sms, 1, 1);   // one CTA per SM, all resident (cooperative)
+        cfg.blockDim = dim3(kPrepTcThreads, 1, 1);
+        cfg.dynamicSmemBytes = kFusedSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        prof_begin(stream, "chunk_fused_tc");
+        e = cudaLaunchKernelEx(&cfg, chunk_fused_tc, mG, mK, mQ, mV, mWs, mUs, mPs, mWQ, mP, mKT, mU, mGam, mO, p.beta,
+                               p.cu, p.num_seqs, p.T_seq, p.H, map, rec, n_tasks, p.s0, p.s_final,
+                               static_cast<bf16*>(p.o), p.dev_err, flags, (int32_t)n_chain);
+        prof_end(stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+      }
+    }
     const int grid = (int)std::min<int64_t>(n_tasks, sms);
     auto prep = [&](auto variant_tag, const char* name) -> cudaError_t {
       constexpr int kV = decltype(variant_tag)::value;
@@ -2034,9 +2146,6 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   // issues the MMAs once per head: the value-major chain for d_v = 128 without
   // the output epilogue, the wide chain otherwise.  KDA_CHAIN_COLUMNS=32, 64 or
   // DV forces a width.
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   int ncol = (int64_t)p.num_seqs * p.H * (DV / BV) > sms ? DV : BV;
   if (const char* env = std::getenv("KDA_CHAIN_COLUMNS")) {
     const int cols = std::atoi(env);
@@ -2049,15 +2158,7 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   if (p.out_gate && ncol != BV) ncol = DV;
   const bool fuse = p.out_gate && ncol == DV;
   const bool wide = ncol != BV;
-  CUtensorMap mWQ, mP, mKT, mU, mGam;
-  const uint64_t Rr = R > 0 ? R : 1;
-  if (!make_map(&mWQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, Rr * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mP, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.p, C, Rr * C, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mKT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.kt, C, Rr * DK, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.u, DV, Rr * C, wide ? 64 : BV, 64,
-                wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&mGam, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rec.gam, DK, Rr, DK, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  if (!chain_maps(wide ? 64 : BV)) return cudaErrorInvalidValue;
   if (DV == 128 && ncol == DV && !p.out_gate) {
     CUtensorMap mO = {};   // o rows by TMA store: 64 tokens x 64 values per box (unused without tokens)
     if (p.total_tokens > 0 &&

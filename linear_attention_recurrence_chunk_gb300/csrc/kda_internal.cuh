@@ -129,6 +129,7 @@ struct Workspace {
   size_t inter_bytes_per_chunk_head;
   bool tc;
   size_t off_wq, off_p, off_kt, off_u, off_gam;   // tensor-core path arrays
+  size_t off_flags;                                // tensor-core path: int32 [R] record publication flags
 };
 
 // fp16 records of the tensor-core path, R = max_chunks * H records each.
