@@ -259,18 +259,24 @@ __device__ __forceinline__ uint32_t opnd_off(int rows, int row, int ch) {
 }
 
 
-// Record publication for the fused kernel: a release store of 1 into the
-// record's flag once every store of the record has completed (the TMA stores
-// by the bulk-group wait, the threads' stores by the CTA barriers since).
-__device__ __forceinline__ void publish_record(int32_t* flag) {
+// Record publication for the fused kernel: once every store of the records
+// first, first + step, .., last has completed (the TMA stores by the bulk-group
+// wait, the threads' stores by the CTA barriers since), one release fence and a
+// store of 1 into each record's flag.  The fences cost far more than the flag
+// stores, so records are published a few at a time.
+constexpr int kPublishBatch = 4;
+__device__ __forceinline__ void publish_records(int32_t* ready, int64_t first, int64_t last, int64_t step) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  __threadfence();
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  for (int64_t r = first; r <= last; r += step)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ready + r), "r"(1u) : "memory");
 }
 
 // One CTA's share of the prep tasks, cta + i * ncta (chunk-major), run by the
-// whole CTA.  With `ready`, each record is published (publish_record) two tasks
-// of this CTA later, when its [w | u] stores, issued a task later, are complete.
+// whole CTA.  With `ready`, the records are published (publish_records) in
+// groups of kPublishBatch, each at the earliest two tasks of this CTA later, when
+// its [w | u] stores, issued a task later, are complete (the CTA's records are
+// consecutive tasks, ncta apart).
 template <int DV, int kVariant>
 __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensorMap& tmK, const CUtensorMap& tmQ,
                                           const CUtensorMap& tmV, const CUtensorMap& tmWs, const CUtensorMap& tmUs,
@@ -337,7 +343,10 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
   // stores to the record with TMA; the tiles are released (bulk read wait)
   // before that area is rewritten.
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
-  int64_t pub_rec = -1;                             // thread 0: the next record to publish (with `ready`)
+  // thread 0, with `ready`: the record that is complete after the next drain, the
+  // oldest complete one not yet published and how many are waiting
+  int64_t pub_rec = -1, unpub = -1;
+  int n_unpub = 0;
   uint32_t wu_parity = 0, ap_parity = 0;
   int64_t wu_rec = 0;
   // Returns the OR over the CTA of `raw_bad` (taken at the drain's CTA
@@ -371,8 +380,13 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
     const bool any_raw_bad = __syncthreads_or(raw_bad);
     if (ready && tid == 0) {   // the record two tasks back is complete once all but the last group are
       if (pub_rec >= 0) {
-        tc::bulk_wait1();
-        publish_record(ready + pub_rec);
+        if (unpub < 0) unpub = pub_rec;
+        if (++n_unpub == kPublishBatch) {
+          tc::bulk_wait1();
+          publish_records(ready, unpub, pub_rec, ncta);
+          unpub = -1;
+          n_unpub = 0;
+        }
       }
       pub_rec = wu_rec;   // complete once its [w | u] stores, issued below, are
     }
@@ -1044,7 +1058,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
   wu_drain(false);   // the last task's [w | u]
   if (!drain_ok && tid == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
   if (bulk_pending) tc::bulk_wait0();   // thread 0: every record store has completed
-  if (ready && tid == 0 && pub_rec >= 0) publish_record(ready + pub_rec);
+  if (ready && tid == 0 && pub_rec >= 0) publish_records(ready, unpub >= 0 ? unpub : pub_rec, pub_rec, ncta);
   (void)failed;
   tc::tc_fence_before();
   __syncthreads();
