@@ -123,14 +123,16 @@ __device__ __forceinline__ bool wait_record(const int32_t* flag) {
 // The chain of (sequence, head) `chain_idx` (sequence-rank major order), run by
 // the whole CTA.  `ready` (or null) holds the publication flags of the records,
 // [max_chunks * H], when the records are written concurrently by the fused
-// kernel's prep role.
+// kernel's prep role; the records are then loaded with evict-first priority and,
+// given `recs`, their L2 lines dropped once consumed (nothing reads them again).
 template <int kCons>
 __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtensorMap& tmP, const CUtensorMap& tmKT,
                                            const CUtensorMap& tmU, const CUtensorMap& tmGam, const CUtensorMap& tmO,
                                            const int32_t* __restrict__ cu, int32_t num_seqs, int64_t T_seq, int32_t H,
                                            const ChunkMap& map, const float* __restrict__ s0,
                                            float* __restrict__ s_final, bf16* __restrict__ o, int32_t* dev_err,
-                                           int chain_idx, const int32_t* __restrict__ ready) {
+                                           int chain_idx, const int32_t* __restrict__ ready,
+                                           const TcRecords* recs = nullptr) {
   using W = VmWarps<kCons>;
   constexpr int kConsumerWarps = W::kConsumerWarps, kOWarp0 = W::kOWarp0, kTmaWarp = W::kTmaWarp,
                 kMmaWarp = W::kMmaWarp;
@@ -199,6 +201,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
   if (warp == kTmaWarp) {
     // ---------------- TMA producer: lane 0 ring A, lane 16 ring B (each slot refilled
     // once the products that read it have completed)
+    const uint64_t pol = ready ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
     if (lane == 0) {
       tc::tma_prefetch_desc(&tmWQ);
       tc::tma_prefetch_desc(&tmU);
@@ -216,10 +219,10 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
         }
         uint8_t* slot = sm + sl * L::kSlotA;
         tc::mbar_arrive_expect_tx(fullA + sl, L::kTxA);
-        tc::tma_load_2d(slot, &tmWQ, 0, (int32_t)(rec * 128), fullA + sl);
-        tc::tma_load_2d(slot + 16384, &tmWQ, 64, (int32_t)(rec * 128), fullA + sl);
-        tc::tma_load_2d(slot + L::kAU, &tmU, 0, (int32_t)(rec * C), fullA + sl);
-        tc::tma_load_2d(slot + L::kAU + 8192, &tmU, 64, (int32_t)(rec * C), fullA + sl);
+        tc::tma_load_2d_hint(slot, &tmWQ, 0, (int32_t)(rec * 128), fullA + sl, pol);
+        tc::tma_load_2d_hint(slot + 16384, &tmWQ, 64, (int32_t)(rec * 128), fullA + sl, pol);
+        tc::tma_load_2d_hint(slot + L::kAU, &tmU, 0, (int32_t)(rec * C), fullA + sl, pol);
+        tc::tma_load_2d_hint(slot + L::kAU + 8192, &tmU, 64, (int32_t)(rec * C), fullA + sl, pol);
         ++issued;
       }
       // never leave loads in flight: wait (bounded) until the last ones landed
@@ -245,9 +248,9 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
         }
         uint8_t* slot = sm + L::oB + sl * L::kSlotB;
         tc::mbar_arrive_expect_tx(fullB + sl, L::kTxB);
-        tc::tma_load_2d(slot, &tmKT, 0, (int32_t)(rec * DK), fullB + sl);
-        tc::tma_load_2d(slot + L::kBP, &tmP, 0, (int32_t)(rec * C), fullB + sl);
-        tc::tma_load_2d(sm + L::oGam + (i % kGamSlots) * DK * 4, &tmGam, 0, (int32_t)rec, fullB + sl);
+        tc::tma_load_2d_hint(slot, &tmKT, 0, (int32_t)(rec * DK), fullB + sl, pol);
+        tc::tma_load_2d_hint(slot + L::kBP, &tmP, 0, (int32_t)(rec * C), fullB + sl, pol);
+        tc::tma_load_2d_hint(sm + L::oGam + (i % kGamSlots) * DK * 4, &tmGam, 0, (int32_t)rec, fullB + sl, pol);
         ++issued;
       }
       for (int i = (issued > kSlotsB ? issued - kSlotsB : 0); i < issued; ++i)
@@ -451,6 +454,16 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
         break;
       }
       tc::tc_fence_after();
+      if (recs) {   // every product of this chunk has completed: its record's L2 lines are dead
+        const int64_t rec = (int64_t)(j0 + i) * H + h;
+        for (int l = ot; l < 256 + 128 + 128 + 64; l += 32 * kOWarps) {
+          const __half* line = l < 256 ? recs->wq + rec * 128 * DK + l * 64
+                               : l < 384 ? recs->u + rec * C * DV + (l - 256) * 64
+                               : l < 512 ? recs->kt + rec * DK * C + (l - 384) * 64
+                                         : recs->p + rec * C * C + (l - 512) * 64;
+          tc::discard_l2_line(line);
+        }
+      }
 #pragma unroll
       for (int hl = 0; hl < 2; ++hl) {   // value lanes 32 q + 16 hl .. +15
         float v[32];

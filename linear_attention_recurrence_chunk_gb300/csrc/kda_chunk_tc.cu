@@ -342,6 +342,11 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
   // the product's own B operand, free once the product is done, which thread 0
   // stores to the record with TMA; the tiles are released (bulk read wait)
   // before that area is rewritten.
+  // In the fused kernel (with `ready`) the records are read back within a few chunks
+  // from L2: they are stored with evict-last priority and the inputs, read once,
+  // loaded with evict-first; alone, prep keeps the default priority.
+  const uint64_t pol_in = ready ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
+  const uint64_t pol_rec = ready ? tc::l2_policy_evict_last() : tc::l2_policy_evict_normal();
   bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
   // thread 0, with `ready`: the record that is complete after the next drain, the
   // oldest complete one not yet published and how many are waiting
@@ -394,9 +399,9 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
 #pragma unroll
       for (int t = 0; t < L::kWuN / 64; ++t) {
         if (t < DK / 64)
-          tc::tma_store_2d(&tmWs, 64 * t, (int32_t)(wu_rec * 128), stg + t * 8192);
+          tc::tma_store_2d_hint(&tmWs, 64 * t, (int32_t)(wu_rec * 128), stg + t * 8192, pol_rec);
         else
-          tc::tma_store_2d(&tmUs, 64 * (t - DK / 64), (int32_t)(wu_rec * C), stg + t * 8192);
+          tc::tma_store_2d_hint(&tmUs, 64 * (t - DK / 64), (int32_t)(wu_rec * C), stg + t * 8192, pol_rec);
       }
       tc::bulk_commit();
       bulk_pending = true;
@@ -438,7 +443,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
     const int which = warp - 12;
     if (!((which_mask >> which) & 1u)) return;
     const CUtensorMap* m = which == 0 ? &tmG : (which == 1 ? &tmK : (which == 2 ? &tmQ : &tmV));
-    tc::tma_load_3d(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, ht, ci.z, bar);
+    tc::tma_load_3d_hint(smem + L::oRawG + (size_t)which * C * DK * 2, m, 0, ht, ci.z, bar, pol_in);
   };
   auto load_beta = [&](int32_t ht, int4 ci) -> float {
     return (tid < ci.y) ? ld_early_f32(beta + ((int64_t)(uint32_t)ci.z + tid) * H + ht) : 0.f;   // ci.y <= 64
@@ -574,7 +579,10 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
     for (int a2 = 0; a2 < 4; ++a2)
       om[a2] = (!kPairs && a2 > a) ? make_float2(ex2_approx(gsA[a2].x - gs.x), ex2_approx(gsA[a2].y - gs.y))
                                    : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
-    if (rg == 0) *reinterpret_cast<float2*>(o_gam + c) = make_float2(ex2_approx(gl.x), ex2_approx(gl.y));
+    if (rg == 0) {
+      tc::st_global_hint(o_gam + c, __float_as_uint(ex2_approx(gl.x)), pol_rec);
+      tc::st_global_hint(o_gam + c + 1, __float_as_uint(ex2_approx(gl.y)), pol_rec);
+    }
 
     // 3. The operands of the A / P products (every 16-bit operand is stored as
     //    a 32-bit pair).
@@ -665,7 +673,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
         const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
         const float br = bw[rr];
         *reinterpret_cast<uint32_t*>(sKV + kv_off(r, c)) = pack_f16x2(br * k0 * eg0, br * k1 * eg1);
-        *reinterpret_cast<uint32_t*>(o_wq + (C + r) * DK + c) = pack_f16x2(q0 * eg0, q1 * eg1);
+        tc::st_global_hint(o_wq + (C + r) * DK + c, pack_f16x2(q0 * eg0, q1 * eg1), pol_rec);
         const __half2 kt = __floats2half2_rn(k0 * el0, k1 * el1);
         const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x), hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
         if (rr & 1) {
@@ -676,8 +684,8 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
           kt1[rr >> 1] = hi16;
         }
       }
-      *reinterpret_cast<uint4*>(o_kt + c * C + r0) = make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]);
-      *reinterpret_cast<uint4*>(o_kt + (c + 1) * C + r0) = make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]);
+      tc::st_global_hint(o_kt + c * C + r0, make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]), pol_rec);
+      tc::st_global_hint(o_kt + (c + 1) * C + r0, make_uint4(kt1[0], kt1[1], kt1[2], kt1[3]), pol_rec);
 #pragma unroll
       for (int e2 = 0; e2 < kPerV; ++e2) {   // beta V (beta is 0 on rows past the sequence end)
         const int idx = tid + e2 * NTH;
@@ -881,7 +889,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tmG, const CUtensor
     tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     __syncthreads();
     if (tid == 0) {   // P to the record (the tile is released before the next task's product barrier)
-      tc::tma_store_2d(&tmPs, 0, (int32_t)(rec * C), sPst);
+      tc::tma_store_2d_hint(&tmPs, 0, (int32_t)(rec * C), sPst, pol_rec);
       tc::bulk_commit();
       bulk_pending = true;
     }
@@ -1948,7 +1956,7 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
   static_assert(vm::VmWarps<8>::kThreads <= kPrepTcThreads, "the chain role fits the prep CTA");
   if ((int)blockIdx.x < n_chain)
     vm::chain_body<8>(tmWQ, tmP, tmKT, tmU, tmGam, tmO, cu, num_seqs, T_seq, H, map, s0, s_final, o, dev_err,
-                      (int)blockIdx.x, ready);
+                      (int)blockIdx.x, ready, &out);
   else
     prep_body<128, kPrepBounded>(tmG, tmK, tmQ, tmV, tmWs, tmUs, tmPs, beta, num_seqs, H, map, out, n_tasks, dev_err,
                                  (int)blockIdx.x - n_chain, (int)gridDim.x - n_chain, ready);
