@@ -1,6 +1,9 @@
 // Tensor-core chunked prefill for bf16 inputs with d_k = 128 (d_v = 64 or 128).
 //
-// Two kernels per call, after the sequence -> chunk map:
+// After the sequence -> chunk map, prep then a chain kernel, or, for few
+// (sequence, head) chains with d_v = 128, both in one launch (chunk_fused_tc at
+// the end of this file: the chains, in the value-major form of
+// chain_vm_body.cuh, trail the prep CTAs chunk by chunk):
 //
 //  chunk_prep_tc   persistent, one 512-thread CTA per SM over (64-token chunk,
 //                  head) tasks in chunk-major order; the next task's raw rows
@@ -20,7 +23,8 @@
 //                  e^{G_last}.
 //
 //  chunk_chain_tc  one CTA per (sequence, head, 32 value columns); the wide
-//  (_wide_tc)      form takes 64 or all value columns per CTA.  Walks the
+//  (_wide_tc)      form takes 64 or all value columns per CTA (the value-major
+//                  chain, kda_chain_vm.cu, all 128 without the epilogue).  Walks the
 //                  sequence's chunks in order with the fp32 state block in
 //                  registers, feeding tcgen05 MMAs (fp32 accumulators in TMEM,
 //                  issued by one warp) from TMA-staged fp16 tiles
