@@ -6,7 +6,7 @@
 // §3.3, chunked prefill with the state carried across chunk boundaries) are
 // taken transposed, value column = TMEM lane:
 //
-//   group 1:  VN   = -S^T w^T + u^T I          (M = 128 values, N = 64 tokens, K = d_k, then 64)
+//   group 1:  VN   = u^T I - S^T w^T          (M = 128 values, N = 64 tokens, K = 64, then d_k)
 //             V_new^T = VN, to fp16               (threads)
 //   group 2:  D3   = V_new^T K~                  (M = 128, N = d_k, K = 64 tokens)
 //             O    = -S^T (q e^G)^T - V_new^T P^T (the o rows, negated; N = 64)
@@ -263,24 +263,32 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, tc::mbar_wait(b, parity, kWaitLimit));
     };
-    bool ok = true, issued = false;
+    // u^T I of chunk j into VN (its V_new^T of chunk j - 1 was read before that
+    // chunk's V_new hand-off), once chunk j's ring-A slot has landed: issued
+    // after the previous chunk's o product, it runs while the state is updated
+    auto issue_u = [&](int j) -> bool {
+      const int sa = j % kSlotsA;
+      if (!wait_all(fullA + sa, (j / kSlotsA) & 1)) return false;
+      tc::tc_fence_after();
+      const uint64_t dU = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sm + sa * L::kSlotA + L::kAU), 8192);
+#pragma unroll
+      for (int kk = 0; kk < C / 16; ++kk)
+        tc::mma_16bit_w(tmem + kVN, dU + ((kk * 2048) >> 4), dI + ((kk * 32) >> 4), kIdU, kk > 0);
+      return true;
+    };
+    bool ok = nch == 0 || issue_u(0), issued = nch > 0 && ok;
     for (int i = 0; i < nch && ok; ++i) {
       const int sa = i % kSlotsA, sb = i & 1;
       const uint32_t b = (uint32_t)(i & 1);
       const uint32_t sA = tmem + kSA + b * 64;   // this chunk's S^T
       const uint64_t dWQ = dSm + ((uint64_t)(sa * L::kSlotA) >> 4);
-      ok = wait_all(s_ready, i & 1) && wait_all(fullA + sa, (i / kSlotsA) & 1);
+      ok = wait_all(s_ready, i & 1);
       if (!ok) break;
       tc::tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < DK / 16; ++kk)   // group 1: -S^T w^T
-        tc::mma_16bit_tw(tmem + kVN, sA + 8 * kk, dWQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdNeg64, kk > 0);
-      const uint64_t dU = tc::desc_mnmajor_sw128_atoms(tc::smem_u32(sm + sa * L::kSlotA + L::kAU), 8192);
-#pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk)    // + u^T I
-        tc::mma_16bit_w(tmem + kVN, dU + ((kk * 2048) >> 4), dI + ((kk * 32) >> 4), kIdU, 1u);
+      for (int kk = 0; kk < DK / 16; ++kk)   // group 1: VN += -S^T w^T
+        tc::mma_16bit_tw(tmem + kVN, sA + 8 * kk, dWQ + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4), kIdNeg64, 1u);
       tc::mma_commit_w(mma1);
-      issued = true;
       ok = wait_all(vn_ready, i & 1) && wait_all(fullB + sb, (i >> 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
@@ -305,6 +313,7 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
         tc::mma_16bit_tw(dO, tmem + kVA + 8 * kk, dKT + ((L::kBP + kk * 32) >> 4), kIdNeg64, 1u);
       tc::mma_commit_w(ofull + b);
       tc::mma_commit_w(emptyB + sb);
+      if (i + 1 < nch) ok = issue_u(i + 1);
     }
     if (!ok && lane == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
     if (issued) {
