@@ -14,8 +14,10 @@ test_chunk_algebra.py) with the kernels' operands and records:
     in fp16 (P V_new and w S are the error-sensitive products: V_new is
     O(|v|) while o is an order of magnitude smaller);
   - the chain: fp32 master state, its fp16 copy and V_new in fp16 as MMA
-    operands (V_new = u - w S with w S rounded to fp16 first, as the kernels'
-    packed fp16 subtraction does), o rounded to bf16.
+    operands (V_new = u - w S with w S rounded to fp16 first, as the 32-column
+    and wide chains' packed fp16 subtraction does; the value-major chain
+    accumulates u - w S in fp32 and rounds once, scheme 'value_major'), o
+    rounded to bf16.
 X is formed exactly from the rounded A and then rounded; the kernel's fp16
 products for X's blocks below the diagonal also round their intermediate
 16x16 blocks, which this does not model.
@@ -51,8 +53,9 @@ def _split(x):
 
 def emulate(q, k, v, g, beta, s0, scheme):
     """o [T, d_v] (bf16 values) and S [d_k, d_v] under the given scheme:
-    'kernel', 'no_split' (P's diagonal sub-tiles single bf16) or 'bf16' (every
-    intermediate bf16, no split)."""
+    'kernel', 'value_major' (the same with V_new rounded once), 'no_split'
+    (P's diagonal sub-tiles single bf16) or 'bf16' (every intermediate bf16, no
+    split)."""
     T, d_k = q.shape
     rec = _bf16 if scheme == "bf16" else _f16
     S = np.array(s0, dtype=np.float64)
@@ -72,7 +75,7 @@ def emulate(q, k, v, g, beta, s0, scheme):
             rk = _bf16(kk[rows] * np.exp(G[rows] - Gs[a]))            # row operands, factors <= 1
             rq_hi, rq_lo = _split(qq[rows] * np.exp(G[rows] - Gs[a]))
             cd_hi, cd_lo = _split(kk[rows] * np.exp(Gs[a] - G[rows]))   # own sub-tile, factors >= 1
-            if scheme != "kernel":
+            if scheme not in ("kernel", "value_major"):
                 rq_hi, rq_lo = _bf16(qq[rows] * np.exp(G[rows] - Gs[a])), 0.0 * rq_lo
                 cd_lo = 0.0 * cd_lo
             A[rows, rows] = _f32(rk @ cd_hi.T)
@@ -93,7 +96,10 @@ def emulate(q, k, v, g, beta, s0, scheme):
         kt = rec(kk * np.exp(G[-1] - G))
         gam = np.exp(G[-1])
         Sop = rec(S)
-        vn = rec(u - rec(w @ Sop))   # w S rounded to fp16, the difference in fp16 (packed arithmetic)
+        if scheme == "value_major":
+            vn = rec(u - _f32(w @ Sop))   # u - w S accumulated in fp32 (one MMA accumulator), rounded once
+        else:
+            vn = rec(u - rec(w @ Sop))   # w S rounded to fp16, the difference in fp16 (packed arithmetic)
         o = _bf16(qh @ Sop + P @ vn)
         S = _f32(gam[:, None] * S + kt.T @ vn)
         outs.append(o[:L])
@@ -118,6 +124,14 @@ def _worst(scheme, cases=((5, 0.05, 300), (7, 0.01, 640))):
 
 def test_kernel_scheme_meets_the_bf16_bound_with_margin():
     o_err, s_err = _worst("kernel")
+    assert o_err <= 0.5 * 2e-2, o_err
+    assert s_err <= 1e-2, s_err
+
+
+def test_value_major_scheme_meets_the_bf16_bound_with_margin():
+    """The value-major chain's V_new (u - w S in the fp32 accumulator, one
+    rounding to fp16) under the same bound and margin."""
+    o_err, s_err = _worst("value_major")
     assert o_err <= 0.5 * 2e-2, o_err
     assert s_err <= 1e-2, s_err
 
