@@ -166,7 +166,7 @@ def _kernel_src_sha(kernel: str = "", csrc: str = "") -> str:
     h = hashlib.sha256()
     d = csrc or os.path.join(ROOT, "linear_attention_recurrence_chunk_gb300", "csrc")
     if kernel in _TC_SECTIONS:
-        for fn in ("kda_internal.cuh", "tc_ptx.cuh"):
+        for fn in ("kda_internal.cuh", "tc_ptx.cuh", "chain_common.cuh", "prep_split_body.cuh"):
             h.update(open(os.path.join(d, fn), "rb").read())
         text = open(os.path.join(d, "kda_chunk_tc.cu"), encoding="utf-8").read()
         for a, b in _TC_SECTIONS[kernel]:

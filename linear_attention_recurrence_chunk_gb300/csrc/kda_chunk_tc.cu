@@ -64,6 +64,7 @@
 #include "chain_common.cuh"
 #include "chain_vm.cuh"
 #include "chain_vm_body.cuh"
+#include "prep_split_body.cuh"
 
 namespace kda {
 namespace {
@@ -80,49 +81,21 @@ using tcu::report_nonfinite;
 using tcu::store_bf16x16;
 using tcu::store_mn_half;
 
-// ------------------------------------------------------------ mma.sync helpers
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-// d += a * b for one m16n8k16 tile with fp16 operands, fp32 accumulators.
-__device__ __forceinline__ void mma16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+// Helpers shared with the two-stream prep (prep_split_body.cuh).
+using ps::ex2_approx;
+using ps::kv_off;
+using ps::later_row0;
+using ps::ld_early_f32;
+using ps::ld_early_v4;
+using ps::ldsm_x4;
+using ps::ldsm_x4_t;
+using ps::mma16816_f16;
+using ps::rcp_approx;
+using ps::split_bf16x2;
+using ps::xs_off;
+using ps::kPublishBatch;
+using ps::publish_records;
 
-
-// 16-byte asynchronous global -> shared copy; src_bytes = 0 zero-fills.
-
-// g_min * Sigmoid(x) with g_min = -5, on the fast exp / reciprocal paths
-// (a huge -x gives exp = inf and a reciprocal of 0, i.e. no decay).
-// log2 of the decay, -5 Sigmoid(x) / ln 2: the prep kernel keeps G in base-2 units so that every
-// factor 2^{G_a - G_b} is one ex2.approx.
-__device__ __forceinline__ float fast_log2_decay(float x) {
-  return __fdividef(-5.f * 1.4426950408889634f, 1.f + __expf(-x));
-}
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -139,38 +112,7 @@ __device__ __forceinline__ float fast_log2_softplus_decay(float x) {
 }
 template <bool kSoftplus>
 __device__ __forceinline__ float log2_decay(float x) {
-  return kSoftplus ? fast_log2_softplus_decay(x) : fast_log2_decay(x);
-}
-
-// bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-
-// Global loads issued where they stand (the compiler may not sink them to the
-// first use), for values needed a task later.
-__device__ __forceinline__ float ld_early_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ int4 ld_early_v4(const int4* p) {
-  int4 v;
-  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// Byte offset of element (row, col) of a [rows][64] fp16 tile, K-major, 128-byte swizzle.
-__device__ __forceinline__ uint32_t xs_off(int row, int col) { return tc::sw128_offset(row, col); }
-// Byte offset of element (k, n) of the [beta k e^G | beta V] operand: MN-major (n contiguous),
-// 128-byte swizzle, 64-column atoms [64 k][128 B].
-__device__ __forceinline__ uint32_t kv_off(int k, int n) {
-  return (uint32_t)(n >> 6) * 8192u + (uint32_t)k * 128u + (((((uint32_t)n & 63u) >> 3) ^ ((uint32_t)k & 7u)) << 4) +
-         ((uint32_t)n & 7u) * 2u;
+  return kSoftplus ? fast_log2_softplus_decay(x) : ps::log2_decay_bounded(x);
 }
 
 // --------------------------------------------------------------- prep kernel
@@ -253,28 +195,12 @@ __device__ __forceinline__ void pair_unrank(int s, int& r, int& i) {
   i = r - 1 - (s - r * (r - 1) / 2);
 }
 
-// Row (in the column operand) of column i of later sub-tile a' = 1..3, minus 128.
-__device__ __forceinline__ int later_row0(int a2) { return a2 == 1 ? 0 : (a2 == 2 ? 16 : 48); }
-
 // Byte offset of (row, channel) in a K-major 128-byte-swizzled operand whose
 // 64-channel atoms hold `rows` rows each.
 __device__ __forceinline__ uint32_t opnd_off(int rows, int row, int ch) {
   return (uint32_t)(ch >> 6) * (uint32_t)rows * 128u + tc::sw128_offset(row, ch & 63);
 }
 
-
-// Record publication for the fused kernel: once every store of the records
-// first, first + step, .., last has completed (the TMA stores by the bulk-group
-// wait, the threads' stores by the CTA barriers since), one release fence and a
-// store of 1 into each record's flag.  The fences cost far more than the flag
-// stores, so records are published a few at a time.
-constexpr int kPublishBatch = 4;
-__device__ __forceinline__ void publish_records(int32_t* ready, int64_t first, int64_t last, int64_t step) {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-  for (int64_t r = first; r <= last; r += step)
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ready + r), "r"(1u) : "memory");
-}
 
 // One CTA's share of the prep tasks, cta + i * ncta (chunk-major), run by the
 // whole CTA.  With `ready`, the records are published (publish_records) in
@@ -1086,6 +1012,20 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                   const float* __restrict__ beta, int32_t num_seqs, int32_t H, ChunkMap map, TcRecords out,
                   int64_t n_tasks, int32_t* __restrict__ dev_err) {
   prep_body<DV, kVariant>(tmG, tmK, tmQ, tmV, tmWs, tmUs, tmPs, beta, num_seqs, H, map, out, n_tasks, dev_err,
+                          (int)blockIdx.x, (int)gridDim.x, nullptr);
+}
+
+// The bounded map's prep with two task streams per CTA (prep_split_body.cuh):
+// the default prep of the plain, gated and snapshot calls.  The single-stream
+// kernel above runs the pair-path variants of the decay-map ablation.
+template <int DV>
+__global__ void __launch_bounds__(ps::kThreads, 1)
+    chunk_prep_split_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmWs,
+                        const __grid_constant__ CUtensorMap tmUs, const __grid_constant__ CUtensorMap tmPs,
+                        const bf16* __restrict__ v, const float* __restrict__ beta, int32_t num_seqs, int32_t H,
+                        ChunkMap map, TcRecords out, int64_t n_tasks, int32_t* __restrict__ dev_err) {
+  ps::prep_split_body<DV>(tmG, tmK, tmQ, tmWs, tmUs, tmPs, v, beta, num_seqs, H, map, out, n_tasks, dev_err,
                           (int)blockIdx.x, (int)gridDim.x, nullptr);
 }
 
@@ -1948,7 +1888,7 @@ __global__ void __launch_bounds__(ChainWideSmem<NC>::kThreads, 1)
 // wait ends.
 __global__ void __launch_bounds__(kPrepTcThreads, 1)
     chunk_fused_tc(const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const bf16* __restrict__ v,
                    const __grid_constant__ CUtensorMap tmWs, const __grid_constant__ CUtensorMap tmUs,
                    const __grid_constant__ CUtensorMap tmPs, const __grid_constant__ CUtensorMap tmWQ,
                    const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmKT,
@@ -1957,16 +1897,17 @@ __global__ void __launch_bounds__(kPrepTcThreads, 1)
                    const int32_t* __restrict__ cu, int32_t num_seqs, int64_t T_seq, int32_t H, ChunkMap map,
                    TcRecords out, int64_t n_tasks, const float* __restrict__ s0, float* __restrict__ s_final,
                    bf16* __restrict__ o, int32_t* __restrict__ dev_err, int32_t* __restrict__ ready, int32_t n_chain) {
-  static_assert(vm::VmWarps<8>::kThreads <= kPrepTcThreads, "the chain role fits the prep CTA");
+  static_assert(vm::VmWarps<8>::kThreads <= kPrepTcThreads && ps::kThreads == kPrepTcThreads,
+                "the chain role fits the prep CTA");
   if ((int)blockIdx.x < n_chain)
     vm::chain_body<8>(tmWQ, tmP, tmKT, tmU, tmGam, tmO, cu, num_seqs, T_seq, H, map, s0, s_final, o, dev_err,
                       (int)blockIdx.x, ready, &out);
   else
-    prep_body<128, kPrepBounded>(tmG, tmK, tmQ, tmV, tmWs, tmUs, tmPs, beta, num_seqs, H, map, out, n_tasks, dev_err,
-                                 (int)blockIdx.x - n_chain, (int)gridDim.x - n_chain, ready);
+    ps::prep_split_body<128>(tmG, tmK, tmQ, tmWs, tmUs, tmPs, v, beta, num_seqs, H, map, out, n_tasks, dev_err,
+                             (int)blockIdx.x - n_chain, (int)gridDim.x - n_chain, ready);
 }
 constexpr size_t kFusedSmem =
-    PrepTcSmem<128, kPrepBounded>::kAlloc > vm::VmSmem::kAlloc ? PrepTcSmem<128, kPrepBounded>::kAlloc : vm::VmSmem::kAlloc;
+    ps::Smem<128>::kAlloc > vm::VmSmem::kAlloc ? ps::Smem<128>::kAlloc : vm::VmSmem::kAlloc;
 
 // --------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -2105,11 +2046,18 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
   bool fused = DV == 128 && !p.out_gate && p.decay_map == KDA_DECAY_BOUNDED && !p.diag_pairs && ws.max_chunks > 0 &&
                p.total_tokens > 0 && n_chain <= sms / 4 && !std::getenv("KDA_CHAIN_COLUMNS");
   if (const char* env = std::getenv("KDA_FUSED")) fused = fused && std::atoi(env) != 0;
+  // The bounded map's prep runs two task streams per CTA over 64-channel halves
+  // of g, k, q (chunk_prep_split_tc); the pair-path variants, or KDA_PREP_STREAMS=1,
+  // run the single-stream kernel over whole rows.
+  bool split = p.decay_map == KDA_DECAY_BOUNDED && !p.diag_pairs;
+  if (const char* env = std::getenv("KDA_PREP_STREAMS")) split = split && std::atoi(env) != 1;
+  fused = fused && split;
   if (ws.max_chunks > 0 && p.total_tokens > 0) {
     CUtensorMap mG, mK, mQ, mV;
     const uint64_t tok = (uint64_t)p.total_tokens;
-    if (!make_input_map(&mG, p.g, DK, p.H, tok) || !make_input_map(&mK, p.k, DK, p.H, tok) ||
-        !make_input_map(&mQ, p.q, DK, p.H, tok) || !make_input_map(&mV, p.v, DV, p.H, tok))
+    const uint32_t box = split ? (uint32_t)ps::KH : 0u;
+    if (!make_input_map(&mG, p.g, DK, p.H, tok, box) || !make_input_map(&mK, p.k, DK, p.H, tok, box) ||
+        !make_input_map(&mQ, p.q, DK, p.H, tok, box) || !make_input_map(&mV, p.v, DV, p.H, tok))
       return cudaErrorInvalidValue;
     CUtensorMap mWs, mUs, mPs;   // record stores of [w | u] and P: 64 x 64 boxes, 128-byte swizzle
     if (!make_map(&mWs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, rec.wq, DK, R * 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -2138,7 +2086,8 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         prof_begin(stream, "chunk_fused_tc");
-        e = cudaLaunchKernelEx(&cfg, chunk_fused_tc, mG, mK, mQ, mV, mWs, mUs, mPs, mWQ, mP, mKT, mU, mGam, mO, p.beta,
+        e = cudaLaunchKernelEx(&cfg, chunk_fused_tc, mG, mK, mQ, static_cast<const bf16*>(p.v), mWs, mUs, mPs, mWQ,
+                               mP, mKT, mU, mGam, mO, p.beta,
                                p.cu, p.num_seqs, p.T_seq, p.H, map, rec, n_tasks, p.s0, p.s_final,
                                static_cast<bf16*>(p.o), p.dev_err, flags, (int32_t)n_chain);
         prof_end(stream);
@@ -2158,12 +2107,25 @@ cudaError_t launch_tc(const ChunkProblem& p, const Workspace& ws, const ChunkMap
       prof_end(stream);
       return cudaGetLastError();
     };
-    if (p.decay_map == KDA_DECAY_SOFTPLUS)
+    if (split) {
+      const size_t smem = ps::Smem<DV>::kAlloc;
+      if ((e = cudaFuncSetAttribute(chunk_prep_split_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem)) != cudaSuccess)
+        return e;
+      // two task streams per CTA: as many CTAs as SMs, or half the tasks (rounded up)
+      const int grid2 = (int)std::min<int64_t>((n_tasks + 1) / 2, sms);
+      prof_begin(stream, "chunk_prep_tc");
+      chunk_prep_split_tc<DV><<<grid2, ps::kThreads, smem, stream>>>(mG, mK, mQ, mWs, mUs, mPs,
+                                                                     static_cast<const bf16*>(p.v), p.beta, p.num_seqs,
+                                                                     p.H, map, rec, n_tasks, p.dev_err);
+      prof_end(stream);
+      e = cudaGetLastError();
+    } else if (p.decay_map == KDA_DECAY_SOFTPLUS)
       e = prep(std::integral_constant<int, kPrepSoftplusPairs>{}, "chunk_prep_tc_softplus_pairs");
     else if (p.diag_pairs)
       e = prep(std::integral_constant<int, kPrepBoundedPairs>{}, "chunk_prep_tc_pairs");
     else
-      e = prep(std::integral_constant<int, kPrepBounded>{}, "chunk_prep_tc");
+      e = prep(std::integral_constant<int, kPrepBounded>{}, "chunk_prep_tc_single");
     if (e != cudaSuccess) return e;
   }
   // Chain variant: 32 value columns per CTA (the most CTAs, for few long

@@ -32,6 +32,9 @@ def test_prep_hash_ignores_the_chain_sections_only(tmp_path):
     open(os.path.join(d, "tc_ptx.cuh"), "a").write("\n// shared header\n")
     open(f, "w", encoding="utf-8").write(text)
     assert bench._kernel_src_sha("chunk_prep_tc", d) != base           # so do shared-header edits
+    d2 = _copy(tmp_path / "b")
+    open(os.path.join(d2, "prep_split_body.cuh"), "a").write("\n// the two-stream prep body\n")
+    assert bench._kernel_src_sha("chunk_prep_tc", d2) != base          # and edits of the prep body's header
 
 
 def test_traffic_line_parsing(tmp_path):

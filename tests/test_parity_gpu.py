@@ -79,6 +79,25 @@ def test_prefill_both_chain_widths(monkeypatch, chain_cols, d_v, B, T, lens):
     _check_all_chains(w, o, sf)
 
 
+@pytest.mark.parametrize("streams", ["1", "2"])
+@pytest.mark.parametrize("d_v,B,T,lens", [(128, 1, 1, None), (128, 3, 200, None), (64, 1, 191, None),
+                                          (64, 2, 130, None), (128, 1, None, [0, 1, 63, 64, 65, 200, 0, 17])])
+def test_prefill_both_prep_kernels(monkeypatch, streams, d_v, B, T, lens):
+    """The bounded map's prep with two task streams per CTA (the default) and
+    with one (KDA_PREP_STREAMS=1) on the same small cases: fewer tasks than
+    streams, odd task counts, ragged tails, empty sequences."""
+    monkeypatch.setenv("KDA_PREP_STREAMS", streams)
+    if lens is not None:
+        lens = np.array(lens)
+        w = ks.PrefillWorkload("streams", "bf16", 1, int(lens.sum()), 3, 128, d_v, seed=654, s0_std=0.05,
+                               seq_lens=lens)
+    else:
+        w = ks.PrefillWorkload("streams", "bf16", B, T, 3, 128, d_v, seed=456 + T, s0_std=0.05)
+    t = prefill_device_inputs(w, DEV)
+    o, sf = _run_prefill(w, t)
+    _check_all_chains(w, o, sf)
+
+
 def test_fp32_b1_h2_t256_d64_workload():
     """The fp32 workload in full (B=1, H=2, T=256, d=64, S0 = 0)."""
     w = ks.workloads()["fp32_b1_h2_t256_d64"]
