@@ -72,6 +72,36 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float log2_decay_bounded(float x) {
   return __fdividef(-5.f * 1.4426950408889634f, 1.f + __expf(-x));
 }
+// A thread's elementwise work is on channel pairs: fp32 pairs in one register pair,
+// multiplied and added by the packed fp32x2 instructions of sm_100 (one
+// instruction per pair, each half rounded as the scalar operation would be).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 ex2_pair(float2 x) { return make_float2(ex2_approx(x.x), ex2_approx(x.y)); }
+__device__ __forceinline__ float2 bf2_to_f2(__nv_bfloat162 x) { return __bfloat1622float2(x); }
+__device__ __forceinline__ uint32_t pack_bf16_pair(float2 x) {
+  const __nv_bfloat162 v = __float22bfloat162_rn(x);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16_pair(float2 x) {
+  const __half2 v = __float22half2_rn(x);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// log2 of the bounded decay of a channel pair (as log2_decay_bounded): e^{-x} as
+// 2^{-x log2 e}, then the quotient.
+__device__ __forceinline__ float2 log2_decay_bounded2(float2 x) {
+  const float2 den = add2(ex2_pair(mul2(x, splat2(-1.4426950408889634f))), splat2(1.f));
+  return make_float2(__fdividef(-5.f * 1.4426950408889634f, den.x), __fdividef(-5.f * 1.4426950408889634f, den.y));
+}
+// bf16 (hi, lo) split of a pair: hi = x rounded to bf16, lo = x - hi (exact in
+// fp32) rounded to bf16; both as bf16x2 words.
+__device__ __forceinline__ void split_bf16_pair(float2 x, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __float22bfloat162_rn(x);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16_pair(fma2(__bfloat1622float2(h), splat2(-1.f), x));
+}
 // bf16 pair (hi, lo) of each of two floats, packed as bf16x2 words.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -131,10 +161,10 @@ __device__ __forceinline__ int later_row0(int a2) { return a2 == 1 ? 0 : (a2 == 
 
 // Record publication for the fused kernel (see prep_split_body): one release
 // fence, then a store of 1 into the flag of each record first, first + step, .., last.
-// The single-stream prep publishes four records per fence, the two-stream prep
-// (whose tasks take twice as long per stream) two.
+// The single-stream prep publishes four records per fence; the two-stream prep,
+// whose control thread is off the inverse's path, publishes each record.
 constexpr int kPublishBatch = 4;
-constexpr int kSplitPublishBatch = 2;
+constexpr int kSplitPublishBatch = 1;
 __device__ __forceinline__ void publish_records(int32_t* ready, int64_t first, int64_t last, int64_t step) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
@@ -190,7 +220,8 @@ struct Smem {
 // at a time, once every store of theirs has completed: the [w | u] record of a
 // task is stored at the start of the next one, so a record joins the batch in
 // the next task's epilogue, right after that task's P store, and is published
-// once the group's thread 0 has waited for all but that most recent bulk group.
+// once the group's control thread has waited for all but that most recent bulk
+// group.
 template <int DV>
 __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CUtensorMap& tmK, const CUtensorMap& tmQ,
                                                 const CUtensorMap& tmWs, const CUtensorMap& tmUs, const CUtensorMap& tmPs,
@@ -214,6 +245,10 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
   const int tid = threadIdx.x, grp = tid >> 8, gt = tid & (NG - 1), gw = gt >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const uint32_t bar_id = 1u + (uint32_t)grp;   // the group's named barrier
+  // The group's control thread (lane 0 of its warp 4, which only writes zeros
+  // during the inverse): raw-row loads, the A / P products, the record stores,
+  // their bulk-group waits and the publication.
+  const bool ctl = gt == 128;
   uint8_t* smem = base + (size_t)grp * L::kStride;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 2 * L::kStride);
   uint8_t* sRow = smem + L::oRow;
@@ -259,8 +294,8 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
   const uint64_t pol_in = ready ? tc::l2_policy_evict_first() : tc::l2_policy_evict_normal();
   const uint64_t pol_rec = ready ? tc::l2_policy_evict_last() : tc::l2_policy_evict_normal();
   const int vc = 2 * cta + grp, nv = 2 * ncta;   // this group's first task and the task stride
-  bool wu_pending = false, bulk_pending = false;   // bulk_pending: thread 0 has record stores in flight
-  // thread 0, with `ready`: the record whose [w | u] stores were issued this task,
+  bool wu_pending = false, bulk_pending = false;   // bulk_pending: the control thread has record stores in flight
+  // control thread, with `ready`: the record whose [w | u] stores were issued this task,
   // and the batch of records waiting for publication
   int64_t pub_rec = -1, batch_first = -1, batch_last = -1, wu_rec = 0;
   int batch_n = 0;
@@ -293,10 +328,10 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
     }
     return okw;
   };
-  // After the group barrier that follows wu_drain_tiles: thread 0 stores the tiles
+  // After the group barrier that follows wu_drain_tiles: the control thread stores the tiles
   // to the record (and does the publication bookkeeping of the fused kernel).
   auto wu_store = [&](bool drained, bool okw) {
-    if (gt != 0 || !drained) return;
+    if (!ctl || !drained) return;
     if (ready) pub_rec = wu_rec;   // complete once its [w | u] stores, issued below, are
     if (okw) {
 #pragma unroll
@@ -345,7 +380,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
   int32_t j_next2 = j_next, h_next2 = h_next;
   advance(j_next2, h_next2);
   int4 ci_next2 = fetch((int64_t)vc + nv, j_next2);
-  if (gt == 0) raw_issue(h_next, ci_next, 0);
+  if (ctl) raw_issue(h_next, ci_next, 0);
 
   // Thread -> channel pair (c, c+1) of the pass and the 8 rows r0..r0+7 of sub-tile a.
   const int rg = gw, a = rg >> 1, c = 2 * lane, r0 = 8 * rg;
@@ -361,7 +396,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
     advance(j_next2, h_next2);
     ci_next2 = fetch(task + 2 * (int64_t)nv, j_next2);
     if (ci.y <= 0) {   // group-uniform
-      if (gt == 0) raw_issue(h_next, ci_next, 0);
+      if (ctl) raw_issue(h_next, ci_next, 0);
       continue;
     }
     const int len = ci.y;
@@ -395,18 +430,14 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * KH + c);
-            run.x += log2_decay_bounded(__low2float(x));
-            run.y += log2_decay_bounded(__high2float(x));
+            run = add2(run, log2_decay_bounded2(bf2_to_f2(x)));
             G[rr] = run;
           }
         } else {               // rows past the sequence end carry no decay
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(rawG + (r0 + rr) * KH + c);
-            if (r0 + rr < len) {
-              run.x += log2_decay_bounded(__low2float(x));
-              run.y += log2_decay_bounded(__high2float(x));
-            }
+            if (r0 + rr < len) run = add2(run, log2_decay_bounded2(bf2_to_f2(x)));
             G[rr] = run;
           }
         }
@@ -424,7 +455,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
         drained = wu_pending;
         okw = wu_drain_tiles();
         // the P tile of the previous task (in the operand area) has been read by the TMA unit
-        if (gt == 0 && bulk_pending) tc::bulk_wait_read0();
+        if (ctl && bulk_pending) tc::bulk_wait_read0();
       }
       tc::fence_proxy_async_smem();   // drain tiles, written by the threads, read by the TMA unit
       tc::tc_fence_before();
@@ -432,15 +463,15 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
       // every thread whether a raw-row copy failed to land.
       const bool any_bad = tc::bar_sync_or(bar_id, NG, !ok);
       wu_store(drained, okw);
-      if (drained && !okw && gt == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      if (drained && !okw && ctl) atomicExch(dev_err, (int32_t)kDevErrTimeout);
       if (any_bad) {   // a staging copy never landed: report, let it finish, stop
-        if (gt == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+        if (ctl) atomicExch(dev_err, (int32_t)kDevErrTimeout);
         tc::mbar_wait(bar, rp, kWaitLimit);
         if (h == 1) tc::mbar_wait(bar + 2, ap_par, kWaitLimit);   // the first pass's products
         failed = true;
         break;
       }
-      if (gt == 0) {   // the raw rows of the next pass
+      if (ctl) {   // the raw rows of the next pass
         if (h == 0)
           raw_issue(h_cur, ci, 1);
         else
@@ -456,26 +487,20 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
         for (int r2 = 0; r2 < 8; ++r2) {
           if ((r2 & 1) == 0) gsA[r2 >> 1] = acc;
           if (r2 == rg) excl = acc;
-          const float2 t2 = *reinterpret_cast<const float2*>(sTot + r2 * KH + c);
-          acc.x += t2.x;
-          acc.y += t2.y;
+          acc = add2(acc, *reinterpret_cast<const float2*>(sTot + r2 * KH + c));
         }
         gl = acc;
 #pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          G[rr].x += excl.x;
-          G[rr].y += excl.y;
-        }
+        for (int rr = 0; rr < 8; ++rr) G[rr] = add2(G[rr], excl);
       }
       float2 gs = gsA[0];   // G_s(a), selected without a dynamic register index
 #pragma unroll
       for (int a2 = 1; a2 < 4; ++a2)
         if (a2 == a) gs = gsA[a2];
+      const float2 ngs = make_float2(-gs.x, -gs.y);
       float2 om[4];
 #pragma unroll
-      for (int a2 = 0; a2 < 4; ++a2)
-        om[a2] = a2 > a ? make_float2(ex2_approx(gsA[a2].x - gs.x), ex2_approx(gsA[a2].y - gs.y))
-                        : make_float2(a2 == a ? 1.f : 0.f, a2 == a ? 1.f : 0.f);
+      for (int a2 = 0; a2 < 4; ++a2) om[a2] = a2 > a ? ex2_pair(add2(gsA[a2], ngs)) : splat2(a2 == a ? 1.f : 0.f);
       if (rg == 0) {
         tc::st_global_hint(o_gam + cg, __float_as_uint(ex2_approx(gl.x)), pol_rec);
         tc::st_global_hint(o_gam + cg + 1, __float_as_uint(ex2_approx(gl.y)), pol_rec);
@@ -484,34 +509,32 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
       // 3. The operand tiles of this pass (the second pass first waits for the first
       //    pass's products, which read the same tiles).
       if (h == 1) {
-        if (!tc::mbar_wait(bar + 2, ap_par, kWaitLimit) && gt == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+        if (!tc::mbar_wait(bar + 2, ap_par, kWaitLimit) && ctl) atomicExch(dev_err, (int32_t)kDevErrTimeout);
         ap_par ^= 1u;
       }
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr) {
         const int r = r0 + rr;
-        const float2 gr = G[rr];
-        const float e0 = ex2_approx(gr.x - gs.x), e1 = ex2_approx(gr.y - gs.y);   // e^{G_r - G_s} in (e^-80, 1]
-        const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
-        const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
-        *reinterpret_cast<uint32_t*>(sRow + xs_off(r, c)) = pack_bf16x2(k0 * e0, k1 * e1);
-        const float f0 = rcp_approx(e0), f1 = rcp_approx(e1);                     // e^{G_s - G_r} in [1, e^80)
+        const float2 e = ex2_pair(add2(G[rr], ngs));   // e^{G_r - G_s} in (e^-80, 1]
+        const float2 k = bf2_to_f2(kq[rr]), q = bf2_to_f2(qq[rr]);
+        *reinterpret_cast<uint32_t*>(sRow + xs_off(r, c)) = pack_bf16_pair(mul2(k, e));
+        const float2 f = make_float2(rcp_approx(e.x), rcp_approx(e.y));   // e^{G_s - G_r} in [1, e^80)
         uint32_t hi, lo;
-        split_bf16x2(q0 * e0, q1 * e1, hi, lo);
+        split_bf16_pair(mul2(q, e), hi, lo);
         *reinterpret_cast<uint32_t*>(sRow + xs_off(C + r, c)) = hi;
         *reinterpret_cast<uint32_t*>(sRow + xs_off(2 * C + r, c)) = lo;
-        const float kf0 = k0 * f0, kf1 = k1 * f1;
-        split_bf16x2(kf0, kf1, hi, lo);   // own sub-tile: high and low parts
+        const float2 kf = mul2(k, f);
+        split_bf16_pair(kf, hi, lo);   // own sub-tile: high and low parts
         *reinterpret_cast<uint32_t*>(sCol + xs_off(r, c)) = hi;
         *reinterpret_cast<uint32_t*>(sCol + xs_off(kLo + r, c)) = lo;
 #pragma unroll
         for (int a2 = 1; a2 < 4; ++a2) {   // later sub-tiles: factors <= 1, high part only
           if (a2 > a)
             *reinterpret_cast<uint32_t*>(sCol + xs_off(kLater + later_row0(a2) + r, c)) =
-                pack_bf16x2(kf0 * om[a2].x, kf1 * om[a2].y);
+                pack_bf16_pair(mul2(kf, om[a2]));
         }
       }
-      if (gt == 0 && bulk_pending) {   // the [w | u] tiles stored above have been read (the
+      if (ctl && bulk_pending) {   // the [w | u] tiles stored above have been read (the
         tc::bulk_wait_read0();         // operand area of [w | u] is rewritten after the barrier)
         bulk_pending = false;
       }
@@ -521,7 +544,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
       tc::tc_fence_after();
 
       // 4. This pass's K = 64 of the A / P products (bf16 operands, fp32 in TMEM).
-      if (gt == 0) {
+      if (ctl) {
         const uint64_t dR = tc::desc_kmajor_sw128(tc::smem_u32(sRow));
         const uint64_t dC = tc::desc_kmajor_sw128(tc::smem_u32(sCol));
         constexpr uint64_t kRowQ = (uint64_t)(C * 128) >> 4, kColLo = (uint64_t)(kLo * 128) >> 4;
@@ -546,15 +569,13 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
           const int r = r0 + rr;
-          const float2 gr = G[rr];
-          const float eg0 = ex2_approx(gr.x), eg1 = ex2_approx(gr.y);                 // e^{G_r}
-          const float el0 = ex2_approx(gl.x - gr.x), el1 = ex2_approx(gl.y - gr.y);   // e^{G_last - G_r}
-          const float k0 = __low2float(kq[rr]), k1 = __high2float(kq[rr]);
-          const float q0 = __low2float(qq[rr]), q1 = __high2float(qq[rr]);
-          const float br = bw[rr];
-          *reinterpret_cast<uint32_t*>(sKV + kv_off(r, cg)) = pack_f16x2(br * k0 * eg0, br * k1 * eg1);
-          tc::st_global_hint(o_wq + (C + r) * DK + cg, pack_f16x2(q0 * eg0, q1 * eg1), pol_rec);
-          const __half2 kt = __floats2half2_rn(k0 * el0, k1 * el1);
+          const float2 eg = ex2_pair(G[rr]);                            // e^{G_r}
+          const float2 el = ex2_pair(fma2(G[rr], splat2(-1.f), gl));    // e^{G_last - G_r}
+          const float2 k = bf2_to_f2(kq[rr]), q = bf2_to_f2(qq[rr]);
+          const float2 keg = mul2(k, eg);
+          *reinterpret_cast<uint32_t*>(sKV + kv_off(r, cg)) = pack_f16_pair(mul2(keg, splat2(bw[rr])));
+          tc::st_global_hint(o_wq + (C + r) * DK + cg, pack_f16_pair(mul2(q, eg)), pol_rec);
+          const __half2 kt = __float22half2_rn(mul2(k, el));
           const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x),
                          hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
           if (rr & 1) {
@@ -571,12 +592,11 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
         for (int e2 = 0; e2 < kPerV; ++e2) {   // beta V (beta is 0 on rows past the sequence end)
           const int idx = gt + e2 * NG, r = idx / (DV / 16);
           const int col = (idx % (DV / 16)) * 8 + (DV / 2) * h;
-          const bf16* x = reinterpret_cast<const bf16*>(&vraw[e2]);
-          const float br = sBeta[r];
+          const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(&vraw[e2]);
+          const float2 br = splat2(sBeta[r]);
           uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            pk[e] = pack_f16x2(br * __bfloat162float(x[2 * e]), br * __bfloat162float(x[2 * e + 1]));
+          for (int e = 0; e < 4; ++e) pk[e] = pack_f16_pair(mul2(bf2_to_f2(x[e]), br));
           *reinterpret_cast<uint4*>(sKV + kv_off(r, DK + col)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
@@ -588,7 +608,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
     //    (rows 32(q%2).. of A for q < 2, of P for q >= 2) and 16-column blocks 2(w/4),
     //    2(w/4)+1; each lane holds one row r of sub-tile ar.
     {
-      if (!tc::mbar_wait(bar + 2, ap_par, kWaitLimit) && gt == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+      if (!tc::mbar_wait(bar + 2, ap_par, kWaitLimit) && ctl) atomicExch(dev_err, (int32_t)kDevErrTimeout);
       ap_par ^= 1u;
       tc::tc_fence_after();
       const int q = gw & 3;
@@ -605,18 +625,22 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
             if (b > ap) continue;
             tc::tmem_ld16(tc::tmem_addr(tm, tl, b == ap ? 16 * b : kLater + later_row0(ap) + 16 * b), x);
             if (ar != ap) continue;
-            const float br = sBeta[rr];
+            const float2 br = splat2(sBeta[rr]);
+            float2 y[8];   // beta_r A_ri
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = mul2(make_float2(x[2 * i], x[2 * i + 1]), br);
             if (b == ap) {   // diagonal block, fp32 (only its strictly lower part is read)
 #pragma unroll
-              for (int i = 0; i < 16; ++i) sA[rr * LDA + i] = br * x[i];
+              for (int i = 0; i < 8; ++i) {
+                sA[rr * LDA + 2 * i] = y[i].x;
+                sA[rr * LDA + 2 * i + 1] = y[i].y;
+              }
             } else {         // below the diagonal, fp16
               uint4* dst = reinterpret_cast<uint4*>(sAh + rr * LDX + 16 * b);
 #pragma unroll
               for (int j = 0; j < 2; ++j)
-                dst[j] = make_uint4(pack_f16x2(br * x[8 * j + 0], br * x[8 * j + 1]),
-                                    pack_f16x2(br * x[8 * j + 2], br * x[8 * j + 3]),
-                                    pack_f16x2(br * x[8 * j + 4], br * x[8 * j + 5]),
-                                    pack_f16x2(br * x[8 * j + 6], br * x[8 * j + 7]));
+                dst[j] = make_uint4(pack_f16_pair(y[4 * j + 0]), pack_f16_pair(y[4 * j + 1]), pack_f16_pair(y[4 * j + 2]),
+                                    pack_f16_pair(y[4 * j + 3]));
             }
           } else {
             if (b > ap) {
@@ -644,7 +668,7 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
     tc::tc_fence_before();
     tc::fence_proxy_async_smem();   // the P tile, written by the threads, read by the TMA unit
     gsync();
-    if (gt == 0) {   // P to the record (the tile is released before the next task's first barrier)
+    if (ctl) {   // P to the record (the tile is released before the next task's first barrier)
       tc::tma_store_2d_hint(&tmPs, 0, (int32_t)(rec * C), sPst, pol_rec);
       tc::bulk_commit();
       bulk_pending = true;
@@ -841,10 +865,10 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
     tc::tc_fence_before();
     gsync();
     wu_store(drained, okw);
-    if (drained && !okw && gt == 0) atomicExch(dev_err, (int32_t)kDevErrTimeout);
+    if (drained && !okw && ctl) atomicExch(dev_err, (int32_t)kDevErrTimeout);
   }
-  if (gt == 0) tc::bulk_wait0();   // every record store of the group has completed
-  if (ready && gt == 0) {
+  if (ctl) tc::bulk_wait0();   // every record store of the group has completed
+  if (ready && ctl) {
     if (pub_rec >= 0) {
       if (batch_first < 0) batch_first = pub_rec;
       batch_last = pub_rec;
