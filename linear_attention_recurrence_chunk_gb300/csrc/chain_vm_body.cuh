@@ -391,12 +391,17 @@ __device__ __forceinline__ void chain_body(const CUtensorMap& tmWQ, const CUtens
         float d[16];
         tc::tmem_ld16(tc::tmem_addr(tmem, tl, kD3 + KPW * part + 16 * g), d);
 #pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
+        for (int e4 = 0; e4 < 4; ++e4) {   // key pairs in packed fp32x2 fused multiply-adds
           const float4 gv = *reinterpret_cast<const float4*>(gam + 16 * g + 4 * e4);
-          S[16 * g + 4 * e4 + 0] = fmaf(gv.x, S[16 * g + 4 * e4 + 0], d[4 * e4 + 0]);
-          S[16 * g + 4 * e4 + 1] = fmaf(gv.y, S[16 * g + 4 * e4 + 1], d[4 * e4 + 1]);
-          S[16 * g + 4 * e4 + 2] = fmaf(gv.z, S[16 * g + 4 * e4 + 2], d[4 * e4 + 2]);
-          S[16 * g + 4 * e4 + 3] = fmaf(gv.w, S[16 * g + 4 * e4 + 3], d[4 * e4 + 3]);
+          float* sp = S + 16 * g + 4 * e4;
+          const float2 s01 = __ffma2_rn(make_float2(gv.x, gv.y), make_float2(sp[0], sp[1]),
+                                        make_float2(d[4 * e4 + 0], d[4 * e4 + 1]));
+          const float2 s23 = __ffma2_rn(make_float2(gv.z, gv.w), make_float2(sp[2], sp[3]),
+                                        make_float2(d[4 * e4 + 2], d[4 * e4 + 3]));
+          sp[0] = s01.x;
+          sp[1] = s01.y;
+          sp[2] = s23.x;
+          sp[3] = s23.y;
         }
       }
       write_sa(b ^ 1u);
