@@ -494,32 +494,32 @@ def bench_decay_ablation(args, r, steps):
     lib = kda.load_library()
     w, t = r["w"], r["t"]
     stream = torch.cuda.current_stream()
-    # The pair paths run prep and the chain as two kernels, so the tensor-core
-    # diagonal is timed the same way here (KDA_FUSED=0) when the plain call fuses them.
+    # The pair paths run the single-stream prep kernel and the chain as two
+    # kernels, so the tensor-core diagonal is timed the same way here: the same
+    # single-stream kernel structure (KDA_PREP_STREAMS=1, which also runs two
+    # kernels), beside the plain call as it runs by default.
     plain_ms = r["elapsed_ms"] / args.steps
-    fused_ms = None
-    if "chunk_prep_tc" in r["per_kernel"]:
-        plain_prep = statistics.mean(r["per_kernel"]["chunk_prep_tc"])
-    else:
-        fused_ms = plain_ms
-        os.environ["KDA_FUSED"] = "0"
-        try:
-            def plain_step():
-                kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["s0"],
-                                  cu_seqlens=t["cu"], o=r["o"], final_state=r["sf"], workspace=r["wsp"],
-                                  stream=stream)
+    default_ms = plain_ms
+    default_prep = statistics.mean(r["per_kernel"]["chunk_prep_tc"]) if "chunk_prep_tc" in r["per_kernel"] else None
+    os.environ["KDA_PREP_STREAMS"] = "1"
+    try:
+        def plain_step():
+            kda.kda_chunk_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], initial_state=t["s0"],
+                              cu_seqlens=t["cu"], o=r["o"], final_state=r["sf"], workspace=r["wsp"],
+                              stream=stream)
 
-            for _ in range(max(3, args.warmup)):
-                plain_step()
-            torch.cuda.synchronize()
-            _prof(lib, True)
-            plain_ms, _ = timed_steps(plain_step, steps, stream)
-            _prof(lib, False)
-            _, recs = _collect(lib)
-            plain_prep = statistics.mean([v for nm, v in recs if nm == "chunk_prep_tc"])
-        finally:
-            del os.environ["KDA_FUSED"]
-    out = {"tensor_core_diagonal": {"ms_per_step": plain_ms, "prep_ms": plain_prep, "fused_call_ms": fused_ms}}
+        for _ in range(max(3, args.warmup)):
+            plain_step()
+        torch.cuda.synchronize()
+        _prof(lib, True)
+        plain_ms, _ = timed_steps(plain_step, steps, stream)
+        _prof(lib, False)
+        _, recs = _collect(lib)
+        plain_prep = statistics.mean([v for nm, v in recs if nm == "chunk_prep_tc_single"])
+    finally:
+        del os.environ["KDA_PREP_STREAMS"]
+    out = {"tensor_core_diagonal": {"ms_per_step": plain_ms, "prep_ms": plain_prep, "prep_kernel": "single-stream",
+                                    "default_call_ms": default_ms, "default_prep_ms": default_prep}}
     for name, dmap in (("bounded_pairs", kda.DECAY_BOUNDED), ("softplus_pairs", kda.DECAY_SOFTPLUS)):
         def step():
             kda.kda_chunk_fwd_decay_variant(t["q"], t["k"], t["v"], t["g"], t["beta"], decay_map=dmap,
