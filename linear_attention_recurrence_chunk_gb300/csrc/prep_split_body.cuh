@@ -89,11 +89,12 @@ __device__ __forceinline__ uint32_t pack_f16_pair(float2 x) {
   const __half2 v = __float22half2_rn(x);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-// log2 of the bounded decay of a channel pair (as log2_decay_bounded): e^{-x} as
-// 2^{-x log2 e}, then the quotient.
+// log2 of the bounded decay of a channel pair, -5 Sigmoid(x) / ln 2: e^{-x} as
+// 2^{-x log2 e}, then -5 / ln 2 times the approximate reciprocal of 1 + e^{-x}
+// (a huge -x gives inf and a reciprocal of 0: no decay).
 __device__ __forceinline__ float2 log2_decay_bounded2(float2 x) {
   const float2 den = add2(ex2_pair(mul2(x, splat2(-1.4426950408889634f))), splat2(1.f));
-  return make_float2(__fdividef(-5.f * 1.4426950408889634f, den.x), __fdividef(-5.f * 1.4426950408889634f, den.y));
+  return mul2(make_float2(rcp_approx(den.x), rcp_approx(den.y)), splat2(-5.f * 1.4426950408889634f));
 }
 // bf16 (hi, lo) split of a pair: hi = x rounded to bf16, lo = x - hi (exact in
 // fp32) rounded to bf16; both as bf16x2 words.
@@ -575,15 +576,13 @@ __device__ __forceinline__ void prep_split_body(const CUtensorMap& tmG, const CU
           const float2 keg = mul2(k, eg);
           *reinterpret_cast<uint32_t*>(sKV + kv_off(r, cg)) = pack_f16_pair(mul2(keg, splat2(bw[rr])));
           tc::st_global_hint(o_wq + (C + r) * DK + cg, pack_f16_pair(mul2(q, eg)), pol_rec);
-          const __half2 kt = __float22half2_rn(mul2(k, el));
-          const uint32_t lo16 = *reinterpret_cast<const uint16_t*>(&kt.x),
-                         hi16 = *reinterpret_cast<const uint16_t*>(&kt.y);
-          if (rr & 1) {
-            kt0[rr >> 1] |= lo16 << 16;
-            kt1[rr >> 1] |= hi16 << 16;
+          const uint32_t kt = pack_f16_pair(mul2(k, el));   // channels cg, cg + 1 of token r
+          if (rr & 1) {   // tokens r - 1, r of each channel as one fp16 pair
+            kt0[rr >> 1] = __byte_perm(kt0[rr >> 1], kt, 0x5410);
+            kt1[rr >> 1] = __byte_perm(kt1[rr >> 1], kt, 0x7632);
           } else {
-            kt0[rr >> 1] = lo16;
-            kt1[rr >> 1] = hi16;
+            kt0[rr >> 1] = kt;
+            kt1[rr >> 1] = kt;
           }
         }
         tc::st_global_hint(o_kt + cg * C + r0, make_uint4(kt0[0], kt0[1], kt0[2], kt0[3]), pol_rec);
