@@ -5,22 +5,22 @@
 // the end of this file: the chains, in the value-major form of
 // chain_vm_body.cuh, trail the prep CTAs chunk by chunk):
 //
-//  chunk_prep_tc   persistent, one 512-thread CTA per SM over (64-token chunk,
-//                  head) tasks in chunk-major order; the next task's raw rows
-//                  arrive by TMA while the current one is processed.  Gate,
-//                  cumulative log-decay, the exp(+-G) scalings as bf16
-//                  operand tiles (128-byte swizzle), then the beta-weighted
-//                  decayed k k^T matrix A and the intra-chunk read-out matrix
-//                  P as two tcgen05 products (M = 128: the rows of every
-//                  16-row sub-tile against the columns it needs, fp32 in
-//                  TMEM) while the threads write the q e^G and K~^T records
-//                  and the [beta k e^G | beta V] operand; X = (I + A)^{-1} by
-//                  blocked forward substitution (diagonal blocks in registers,
-//                  blocks below on mma.sync), then w, u = X [beta k e^G |
-//                  beta V] as one tcgen05 product whose TMEM result is drained
-//                  and stored by TMA during the next task.  Writes fp16
-//                  records: [w; q e^G], P, (k e^{G_last - G})^T, u and fp32
-//                  e^{G_last}.
+//  chunk_prep_tc   persistent over (64-token chunk, head) tasks in chunk-major
+//                  order, the next raw rows arriving by TMA during the current
+//                  task: gate, cumulative log-decay, the exp(+-G) scalings as
+//                  bf16 operand tiles (128-byte swizzle), then the
+//                  beta-weighted decayed k k^T matrix A and the read-out matrix
+//                  P as tcgen05 products (M = 128, fp32 in TMEM) while the
+//                  threads write the q e^G and K~^T records and the
+//                  [beta k e^G | beta V] operand; X = (I + A)^{-1} (diagonal
+//                  blocks in registers, blocks below on mma.sync), then
+//                  w, u = X [beta k e^G | beta V] on tcgen05, drained and stored
+//                  by TMA during the next task.  Records: fp16 [w; q e^G], P,
+//                  (k e^{G_last - G})^T, u and fp32 e^{G_last}.  The bounded
+//                  map runs it with two task streams per CTA, a task in two
+//                  64-channel passes (chunk_prep_split_tc, prep_split_body.cuh,
+//                  also chunk_fused_tc's prep role); the single-stream kernel
+//                  below runs the ablation's pair paths.
 //
 //  chunk_chain_tc  one CTA per (sequence, head, 32 value columns); the wide
 //  (_wide_tc)      form takes 64 or all value columns per CTA (the value-major
