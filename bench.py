@@ -810,6 +810,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_size, "steps": steps,
         "warmup": args.warmup, "ms_per_step": r["max_ms"] / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "head_tokens_per_s": value * w.H,   # a token is one position across all H heads
         "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "d_k": w.d_k, "d_v": w.d_v,
                    "state": "fp32, S0 ~ N(0, 0.01)", "chunk": 64,
                    "l2": "no flush: 2.1 GB of inputs per step, larger than L2",
